@@ -1,0 +1,267 @@
+"""Pins for the fp64 oracle: checks that tie it to something other than itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with a hand-worked example, a closed form, an independent
+library routine or the pure-Python brute force.  ``test_oracle_pins.py`` runs
+them on the committed oracle; ``test_oracle_mutants.py`` runs them on copies of
+the oracle with a plausible mistake planted, and requires that some pin fails.
+"""
+from __future__ import annotations
+
+import json
+import os
+import struct
+
+import numpy as np
+
+from oracle import brute
+from weight_only_int4_codes_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _hex16(h: str) -> int:
+    return int(h, 16)
+
+
+def _f16_exact(vals) -> np.ndarray:
+    a = np.asarray(vals, dtype=np.float64)
+    h = a.astype(np.float16)
+    assert np.array_equal(h.astype(np.float64), a), "fixture value not exact in fp16"
+    return h
+
+
+# --------------------------------------------------------------------- codec
+def pin_half_decode_exhaustive(orc):
+    """Every one of the 65,536 binary16 patterns decodes like numpy's float16."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0])
+
+
+def pin_half_encode(orc):
+    """Round-to-nearest-even encoding: all finite patterns round-trip, midpoints
+    between neighbours go to the even one, and random doubles match both numpy
+    and Python's struct 'e' packing."""
+    for b in range(65536):
+        e = (b >> 10) & 31
+        if e == 31:
+            continue
+        v = struct.unpack("<e", struct.pack("<H", b))[0]
+        if b == 0x8000:
+            v = -0.0
+        assert orc.double_to_half(v) == b, hex(b)
+    # exact midpoints between consecutive positive finite halves
+    for b in range(0, 0x7bff):
+        lo = struct.unpack("<e", struct.pack("<H", b))[0]
+        hi = struct.unpack("<e", struct.pack("<H", b + 1))[0]
+        mid = (lo + hi) / 2.0
+        want = b if b % 2 == 0 else b + 1
+        assert orc.double_to_half(mid) == want, hex(b)
+        assert orc.double_to_half(-mid) == (want | 0x8000), hex(b)
+    rng = np.random.Generator(np.random.PCG64(12345))
+    vals = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 5, 20000),
+                           rng.uniform(-70000, 70000, 2000)])
+    with np.errstate(over="ignore"):
+        want_np = vals.astype(np.float16).view(np.uint16)
+    for v, w in zip(vals, want_np):
+        got = orc.double_to_half(float(v))
+        assert got == int(w), v
+        if abs(v) < 65520:
+            assert got == struct.unpack("<H", struct.pack("<e", float(v)))[0], v
+    assert orc.double_to_half(65519.99) == 0x7BFF
+    assert orc.double_to_half(65520.0) == 0x7C00
+    assert orc.double_to_half(-1e9) == 0xFC00
+    assert orc.double_to_half(2.0 ** -25) == 0x0000        # tie to even (0)
+    assert orc.double_to_half(3 * 2.0 ** -25) == 0x0002    # tie to even (2)
+
+
+# -------------------------------------------------------------------- packing
+def pin_pack_closed_forms(orc):
+    """codes 0..7 along k -> 0x76543210; 8..15 -> 0xFEDCBA98; all 15 -> 0xFFFFFFFF."""
+    W = _f16_exact(np.arange(16, dtype=np.float64)[:, None] * np.ones((1, 3)))
+    packed, scales, zeros = orc.quantize_pack(W, group=16)
+    assert packed[:, 0].tolist() == [0x76543210, 0xFEDCBA98]
+    assert scales.view(np.uint16)[0, 0] == 0x3C00 and zeros.view(np.uint16)[0, 0] == 0
+    W15 = _f16_exact(np.full((8, 2), 15.0))
+    p15, s15, z15 = orc.quantize_pack(W15, group=8)
+    assert p15.tolist() == [[0xFFFFFFFF, 0xFFFFFFFF]]
+    assert s15.view(np.uint16).tolist() == [[0x3C00, 0x3C00]]
+
+
+def pin_pack_roundtrip(orc):
+    """unpack(pack(q)) == q on random weights (codes from the oracle's own
+    quantizer), and every code appears in every nibble position."""
+    W = _f16_exact(((np.arange(16)[:, None] + np.arange(16)[None, :]) % 16).astype(np.float64))
+    packed, _, _, q = orc.quantize_pack(W, group=16, return_codes=True)
+    assert np.array_equal(q, ((np.arange(16)[:, None] + np.arange(16)[None, :]) % 16))
+    # independent numpy unpack of the words
+    np_unpack = np.stack([(packed >> np.uint32(4 * j)) & np.uint32(15) for j in range(8)], axis=1)
+    np_unpack = np_unpack.reshape(16, 16)
+    assert np.array_equal(np_unpack, q)
+    assert np.array_equal(orc.unpack(packed), q)
+    Wr = synth.weight(256, 24, seed=99)
+    pr, _, _, qr = orc.quantize_pack(Wr, group=128, return_codes=True)
+    assert np.array_equal(orc.unpack(pr), qr)
+
+
+# --------------------------------------------------------------- hand-worked
+def pin_golden_8x8(orc):
+    g = json.load(open(os.path.join(GOLDEN, "hand_8x8_g8.json")))
+    K, N = g["K"], g["N"]
+    W = np.zeros((K, N))
+    for n, col in g["columns"].items():
+        n = int(n)
+        if "w" in col:
+            W[:, n] = col["w"]
+        elif "w_times_2^10" in col:
+            W[:, n] = np.array(col["w_times_2^10"], dtype=np.float64) * 2.0 ** -10
+        else:
+            W[:, n] = np.array(col["w_times_2^24"], dtype=np.float64) * 2.0 ** -24
+    Wh = _f16_exact(W)
+    packed, scales, zeros = orc.quantize_pack(Wh, group=g["group"])
+    assert [int(v) for v in packed[0]] == [int(h, 16) for h in g["packed_hex"]]
+    assert scales.view(np.uint16)[0].tolist() == [_hex16(h) for h in g["scales_hex"]]
+    assert zeros.view(np.uint16)[0].tolist() == [_hex16(h) for h in g["zeros_hex"]]
+    wdq = orc.dequant(packed, scales, zeros, group=g["group"]).view(np.uint16)
+    for n, col in g["wdq_hex_by_column"].items():
+        assert wdq[:, int(n)].tolist() == [_hex16(h) for h in col], n
+    for n in g["wdq_equals_w_columns"]:
+        assert np.array_equal(wdq[:, n], Wh.view(np.uint16)[:, n]), n
+
+
+def pin_golden_zero_from_rounded_scale(orc):
+    g = json.load(open(os.path.join(GOLDEN, "hand_8x1_zero_from_rounded_scale.json")))
+    Wh = _f16_exact(np.array(g["w"], dtype=np.float64)[:, None])
+    packed, scales, zeros = orc.quantize_pack(Wh, group=g["group"])
+    assert int(packed[0, 0]) == int(g["packed_hex"], 16)
+    assert int(scales.view(np.uint16)[0, 0]) == _hex16(g["scale_hex"])
+    assert int(zeros.view(np.uint16)[0, 0]) == _hex16(g["zero_hex"])
+    wdq = orc.dequant(packed, scales, zeros, group=g["group"]).view(np.uint16)
+    assert wdq[:, 0].tolist() == [_hex16(h) for h in g["wdq_hex"]]
+
+
+def _hand_128x4():
+    K = 128
+    W = np.zeros((K, 4))
+    k = np.arange(K)
+    W[:, 0] = (k % 16 - 8) * 0.125
+    W[:, 1] = -3.0
+    cyc2 = [0.125, 0.375, -0.125, -0.375, 0.625, -0.625]
+    W[0, 2], W[1, 2] = -0.75, 3.0
+    W[2:, 2] = [cyc2[(kk - 2) % 6] for kk in range(2, K)]
+    cyc3 = [0.5, 2.0, 1.0, 1.5]
+    W[:, 3] = [cyc3[kk % 4] for kk in range(K)]
+    return _f16_exact(W)
+
+
+def pin_golden_128x4(orc):
+    g = json.load(open(os.path.join(GOLDEN, "hand_128x4_g128.json")))
+    Wh = _hand_128x4()
+    packed, scales, zeros = orc.quantize_pack(Wh, group=128)
+    assert scales.view(np.uint16)[0].tolist() == [_hex16(h) for h in g["scales_hex"]]
+    assert zeros.view(np.uint16)[0].tolist() == [_hex16(h) for h in g["zeros_hex"]]
+    ev, od = [int(h, 16) for h in g["packed_hex_col0_even_odd"]]
+    assert packed[:, 0].tolist() == [ev if r % 2 == 0 else od for r in range(16)]
+    assert packed[:, 1].tolist() == [int(g["packed_hex_col1"], 16)] * 16
+    rows2 = g["packed_hex_col2_rows_r_mod3"]
+    want2 = [int(g["packed_hex_col2_row0"], 16)] + [int(rows2[str(r % 3)], 16)
+                                                    for r in range(1, 16)]
+    assert packed[:, 2].tolist() == want2
+    assert packed[:, 3].tolist() == [int(g["packed_hex_col3"], 16)] * 16
+    wdq = orc.dequant(packed, scales, zeros, group=128)
+    wb = wdq.view(np.uint16)
+    assert np.array_equal(wb[:, 0], Wh.view(np.uint16)[:, 0])
+    assert set(wb[:, 1].tolist()) == {_hex16(g["wdq_hex_col1"])}
+    q2 = orc.unpack(packed)[:, 2]
+    for kk in range(128):
+        assert wb[kk, 2] == _hex16(g["wdq_hex_col2_by_code"][str(int(q2[kk]))])
+        assert wb[kk, 3] == _hex16(g["wdq_hex_col3_by_w"][repr(float(Wh[kk, 3]))])
+
+
+# ------------------------------------------------------------- closed forms
+def pin_dequant_closed_form(orc):
+    """Wdq == fp16((q - z) * s) computed with numpy, and |w - (q-z)s| <= s/2 on
+    every entry whose code is not clipped."""
+    for seed, outl in ((5, False), (6, True)):
+        W = synth.weight(512, 64, seed=seed, outliers=outl)
+        packed, scales, zeros, q = orc.quantize_pack(W, group=128, return_codes=True)
+        s = np.repeat(scales.astype(np.float64), 128, axis=0)
+        z = np.repeat(zeros.astype(np.float64), 128, axis=0)
+        want = ((q.astype(np.float64) - z) * s).astype(np.float16)
+        got = orc.dequant(packed, scales, zeros, group=128)
+        assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+        w = W.astype(np.float64)
+        unclipped = (np.rint(w / s) + z > 0) & (np.rint(w / s) + z < 15)
+        err = np.abs(w - (q - z) * s)
+        assert np.all(err[unclipped] <= s[unclipped] / 2)
+        # min and max of every group are reproduced to within s/2 as well
+        assert np.all(z >= 0) and np.all(z <= 15) and np.all(z == np.rint(z))
+
+
+def pin_gemm_one_hot(orc):
+    """x = e_k picks row k of the dequantized weight exactly."""
+    W = synth.weight(256, 40, seed=11)
+    packed, scales, zeros = orc.quantize_pack(W, group=128)
+    wdq = orc.dequant(packed, scales, zeros, group=128).astype(np.float64)
+    for kk in (0, 1, 7, 8, 127, 128, 200, 255):
+        x = np.zeros((1, 256), dtype=np.float16)
+        x[0, kk] = 1.0
+        out = orc.gemm(x, packed, scales, zeros, group=128)
+        assert np.array_equal(out[0], wdq[kk]), kk
+
+
+def pin_gemm_linear(orc):
+    """x = 0 gives 0; doubling x doubles the output exactly; a matmul of numpy on
+    the dequantized weight agrees to fp64 rounding."""
+    W = synth.weight(384, 24, seed=12)
+    packed, scales, zeros = orc.quantize_pack(W, group=128)
+    x = synth.activations(3, 384, seed=13)
+    out = orc.gemm(x, packed, scales, zeros, group=128)
+    out2 = orc.gemm((x.astype(np.float32) * 2).astype(np.float16), packed, scales, zeros, 128)
+    assert np.array_equal(out2, 2 * out)
+    assert not np.any(orc.gemm(np.zeros_like(x), packed, scales, zeros, 128))
+    wdq = orc.dequant(packed, scales, zeros, group=128).astype(np.float64)
+    ref = x.astype(np.float64) @ wdq
+    assert np.max(np.abs(out - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_brute_force(orc):
+    """The pure-Python brute force (struct fp16, exact Fraction sums) agrees:
+    bit-exact encoding, GEMM to fp64 rounding."""
+    rng = np.random.Generator(np.random.PCG64(2024))
+    for (M, K, N, grp) in ((1, 8, 3, 8), (3, 64, 5, 32), (2, 256, 8, 128), (3, 128, 4, 64)):
+        W = (rng.standard_normal((K, N)) * 0.02).astype(np.float16)
+        x = rng.standard_normal((M, K)).astype(np.float16)
+        Wl = W.astype(np.float64).tolist()
+        bp, bs, bz, bq = brute.quantize_pack(Wl, grp)
+        packed, scales, zeros = orc.quantize_pack(W, group=grp)
+        assert packed.tolist() == bp
+        assert scales.astype(np.float64).tolist() == bs
+        assert zeros.astype(np.float64).tolist() == bz
+        bw = brute.dequant(bq, bs, bz, grp)
+        wdq = orc.dequant(packed, scales, zeros, group=grp)
+        assert wdq.astype(np.float64).tolist() == bw
+        bref = np.array(brute.gemm(x.astype(np.float64).tolist(), bw))
+        ref = orc.gemm(x, packed, scales, zeros, group=grp)
+        assert np.max(np.abs(ref - bref)) <= 1e-13 * max(1.0, float(np.max(np.abs(bref))))
+
+
+ALL_PINS = [
+    pin_half_decode_exhaustive,
+    pin_half_encode,
+    pin_pack_closed_forms,
+    pin_pack_roundtrip,
+    pin_golden_8x8,
+    pin_golden_128x4,
+    pin_golden_zero_from_rounded_scale,
+    pin_dequant_closed_form,
+    pin_gemm_one_hot,
+    pin_gemm_linear,
+    pin_brute_force,
+]

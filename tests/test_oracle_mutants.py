@@ -1,0 +1,80 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and require
+that at least one pin catches each one.  This shows the pins are strong enough
+to detect a dropped term, a wrong sign or index, a wrong rounding rule or a
+reversed operand anywhere in the oracle."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "w4a16_oracle.c")
+
+# (name, text in the committed source, planted replacement)
+MUTANTS = [
+    ("nibble_order_reversed",
+     "packed[(size_t)(k / 8) * N + n] |= q << (4 * (k % 8));",
+     "packed[(size_t)(k / 8) * N + n] |= q << (4 * (7 - k % 8));"),
+    ("hqq_style_rounding",
+     "double qd = rint(w / s) + (double)z;",
+     "double qd = rint(w / s + (double)z);"),
+    ("half_away_rounding",
+     "double qd = rint(w / s) + (double)z;",
+     "double qd = round(w / s) + (double)z;"),
+    ("scale_divisor_16",
+     "oracle_double_to_half((mx - mn) / 15.0);",
+     "oracle_double_to_half((mx - mn) / 16.0);"),
+    ("zero_from_unrounded_scale",
+     "double zr = rint(-mn / s);",
+     "double zr = rint(-mn / ((mx - mn) / 15.0 + (mx == mn)));"),
+    ("zero_not_clamped_high",
+     "if (zr > 15.0) zr = 15.0;",
+     "if (zr > 31.0) zr = 31.0;"),
+    ("dequant_sign",
+     "Wdq[(size_t)k * N + n] = oracle_double_to_half((q - z) * s);",
+     "Wdq[(size_t)k * N + n] = oracle_double_to_half((q + z) * s);"),
+    ("unpack_mask_3_bits",
+     "(uint8_t)((packed[(size_t)(k / 8) * N + n] >> (4 * (k % 8))) & 15u);",
+     "(uint8_t)((packed[(size_t)(k / 8) * N + n] >> (4 * (k % 8))) & 7u);"),
+    ("gemm_drops_last_term",
+     "for (int k = 0; k < K; ++k) acc += xm[k] * w[k];",
+     "for (int k = 0; k < K - 1; ++k) acc += xm[k] * w[k];"),
+    ("gemm_reversed_k",
+     "for (int k = 0; k < K; ++k) acc += xm[k] * w[k];",
+     "for (int k = 0; k < K; ++k) acc += xm[k] * w[K - 1 - k];"),
+    ("codec_subnormal_threshold",
+     "if (a < ldexp(1.0, -14)) {",
+     "if (a < ldexp(1.0, -15)) {"),
+    ("codec_truncates",
+     "double m = rint(ldexp(f, 11));",
+     "double m = floor(ldexp(f, 11));"),
+    ("codec_decode_bias",
+     "v = ldexp((double)(1024 + frac), expo - 25);",
+     "v = ldexp((double)(1024 + frac), expo - 24);"),
+    ("degenerate_scale_kept_zero",
+     "s_bits = 0x3c00;     /* 1.0 */\n                s = 1.0;",
+     "s_bits = 0x3c00;     /* 1.0 */\n                s = 1e-300;"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    return open(SRC).read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, source, name, old, new):
+    assert source.count(old) == 1, "mutation anchor not unique: " + name
+    mutated = source.replace(old, new)
+    src = tmp_path / "mutant.c"
+    src.write_text(mutated)
+    lib = oracle.compile_source(str(src), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except Exception:  # any failure of a pin counts as detection
+            caught.append(pin.__name__)
+    assert caught, "no pin detects the planted mistake " + name

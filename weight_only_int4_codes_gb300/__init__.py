@@ -1,0 +1,24 @@
+"""GB300-native W4A16 weight-only GEMM.
+
+out[M,N] = x[M,K] @ W[K,N] with x fp16, fp32 accumulation and an fp16 output,
+where W is held as unsigned 4-bit codes packed eight per int32 along K and
+each group of 128 K-rows of each column carries one fp16 scale and one fp16
+zero (W = (q - z) * s, dequantized inside the kernel).
+
+All compute runs in the CUDA library ``libw4a16.so`` (hand-written sm_103a
+kernels behind a C ABI, declared in ``include/w4a16.h``).  ``native`` is a thin
+ctypes binding with the same names; it raises if the library is missing.  The
+binding is imported on first attribute access, so ``synth`` (input generation)
+can be used without the native library.
+"""
+_NATIVE_NAMES = {
+    "W4A16Error", "gemm", "gemm_ex", "dequantize", "quantize_pack", "kernel_status",
+    "library_path", "load_library", "plan",
+}
+
+
+def __getattr__(name):
+    if name in _NATIVE_NAMES:
+        from . import native
+        return getattr(native, name)
+    raise AttributeError(name)
