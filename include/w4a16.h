@@ -1,0 +1,162 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 weight-only GEMM library,
+ * libw4a16.so.
+ *
+ * The operation (page "Beating FP16 with 4-bit Weights: A Portable W4A16 GEMM
+ * in Triton", sections "The design" and "Code"; GemLite README, usage section):
+ *
+ *     out[M,N] = x[M,K] . W[K,N],   x fp16, fp32 accumulation, out fp16,
+ *     W[k,n]   = (q[k,n] - z[k/g,n]) * s[k/g,n]
+ *
+ * where q is an unsigned 4-bit code, g the group size (128 by default), and
+ * s, z one fp16 scale and one fp16 zero per (group, column).
+ *
+ * Data layout (all row-major, all DEVICE memory owned by the caller):
+ *   x       [M, K]    fp16 (binary16 bit patterns, uint16_t)
+ *   packed  [K/8, N]  uint32: the code of row k sits at bits 4*(k%8) of word
+ *                     (k/8, n) -- eight codes per word along K, LSB first
+ *   scales  [K/g, N]  fp16
+ *   zeros   [K/g, N]  fp16 holding an integer in [0, 15]
+ *   out     [M, N]    fp16
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers are device pointers; nothing is allocated per call and no
+ *     ownership is taken.  Calls are asynchronous on `stream` (0 = the legacy
+ *     default stream) and return once the work is enqueued.
+ *   - Arguments are validated on the host before anything is enqueued; a bad
+ *     argument returns a non-zero status and enqueues nothing.  The message for
+ *     the last non-OK status of the calling thread is w4a16_last_error().
+ *   - Shapes: K % group == 0, group % 32 == 0 (group in [32, 1024]),
+ *     N % 4 == 0, all of M, N, K >= 0 and below 2^31 elements per array.
+ *     M == 0 (or N == 0) is a no-op that returns W4A16_OK.
+ *   - Alignment: x, packed, scales, zeros and out must be 16-byte aligned
+ *     (W4A16_ERR_MISALIGNED otherwise).
+ *   - `out` is fully overwritten, never accumulated into, so repeated calls
+ *     into a dirty buffer give the same bits.
+ *   - For a fixed device, shape and configuration the result is bitwise
+ *     reproducible run to run (all split-K reductions are in a fixed order).
+ */
+#ifndef W4A16_H_
+#define W4A16_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum w4a16_status {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,   /* bad shape, group or null pointer */
+    W4A16_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+    W4A16_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    W4A16_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    W4A16_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (see
+                                    w4a16_get_kernel_status) */
+} w4a16_status;
+
+/* Kernel family a GEMM call runs on. */
+typedef enum w4a16_path {
+    W4A16_PATH_AUTO = 0,     /* pick from the measured dispatch table */
+    W4A16_PATH_DECODE = 1,   /* CUDA-core unpack + register-fed tensor-core MMA,
+                                split-K across a thread-block cluster (M <= 16
+                                per pass; larger M is processed in 16-row passes) */
+    W4A16_PATH_PREFILL = 2   /* TMA-staged tiles, tcgen05 MMA, TMEM accumulator */
+} w4a16_path;
+
+/* flags */
+#define W4A16_FLAG_PDL 0x1   /* launch with programmatic dependent launch: the
+                                kernel streams its weights before waiting for the
+                                previous kernel on the stream.  Only valid when
+                                packed/scales/zeros are NOT written by the kernel
+                                immediately before it on the same stream. */
+
+/*
+ * Launch configuration of one GEMM call.  Zero in any field means "choose
+ * automatically"; w4a16_plan() returns the choice for a shape.
+ */
+typedef struct w4a16_config {
+    int path;       /* w4a16_path */
+    int split_k;    /* decode: CTAs of one cluster that split K (1..8) */
+    int warps_k;    /* decode: warps per CTA that split K */
+    int warps_n;    /* decode: 32-column strips per CTA */
+    int steps;      /* decode: 32-row K steps per warp */
+    int tile_m;     /* prefill: rows of x per CTA tile (16..256, multiple of 16) */
+    int flags;      /* W4A16_FLAG_* */
+    int reserved;
+} w4a16_config;
+
+/*
+ * Group-wise asymmetric 4-bit quantization and packing of an fp16 weight.
+ * (page "Beating FP16 with 4-bit Weights", section "The design": one scale and
+ * one zero-point per group of rows, eight codes per int32 along K.)
+ *
+ * Per (group j, column n), over rows k in [j*g, (j+1)*g):
+ *     s = fp16((max_k W - min_k W) / 15)     fp64 arithmetic, one rounding;
+ *                                            s = 1.0 if that rounds to 0
+ *     z = clamp(rint(-min / s), 0, 15)       rint = round half to even
+ *     q = clamp(rint(W / s) + z, 0, 15)
+ * using the rounded s throughout.  Bit-exact with the fp64 oracle.
+ *   W       [K, N] fp16 device input
+ *   packed  [K/8, N], scales [K/g, N], zeros [K/g, N] device outputs
+ * Offline step: not on the timed path.
+ */
+W4A16_API w4a16_status w4a16_quantize_pack(const uint16_t *W, int K, int N, int group,
+                                 uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                 cudaStream_t stream);
+
+/*
+ * Dequantize the packed weight back to fp16: W_out[k,n] = fp16((q - z) * s),
+ * one rounding of the exact product.  Test aid (bit-exact with the oracle).
+ */
+W4A16_API w4a16_status w4a16_dequantize(const uint32_t *packed, const uint16_t *scales,
+                              const uint16_t *zeros, uint16_t *W_out,
+                              int K, int N, int group, cudaStream_t stream);
+
+/*
+ * out[M,N] = x[M,K] . dequant(packed, scales, zeros), fp32 accumulation,
+ * fp16 output (round to nearest even).  The weight is dequantized inside the
+ * kernel and never materialized.  Automatic path selection.
+ */
+W4A16_API w4a16_status w4a16_gemm(const uint16_t *x, const uint32_t *packed,
+                        const uint16_t *scales, const uint16_t *zeros, uint16_t *out,
+                        int M, int N, int K, int group, cudaStream_t stream);
+
+/* As w4a16_gemm, with an explicit (possibly partial) launch configuration;
+ * cfg == NULL is the same as w4a16_gemm.  Unsupported combinations return
+ * W4A16_ERR_UNSUPPORTED without enqueuing anything. */
+W4A16_API w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed,
+                           const uint16_t *scales, const uint16_t *zeros, uint16_t *out,
+                           int M, int N, int K, int group, const w4a16_config *cfg,
+                           cudaStream_t stream);
+
+/* Host-only: the launch configuration w4a16_gemm_ex would use for this shape
+ * with `request` (may be NULL) filled in.  Touches no GPU.  Returns the same
+ * validation status the GEMM would (pointer checks excepted). */
+W4A16_API w4a16_status w4a16_plan(int M, int N, int K, int group, const w4a16_config *request,
+                        w4a16_config *plan_out);
+
+/* Reads and clears the device-side status word that bounded waits inside the
+ * kernels set when they give up (W4A16_ERR_TIMEOUT), after synchronizing
+ * `stream`.  W4A16_OK if no kernel reported a problem. */
+W4A16_API w4a16_status w4a16_get_kernel_status(cudaStream_t stream);
+
+/* Message for the last non-OK status returned to the calling thread
+ * ("" if none).  The pointer stays valid until the thread's next call. */
+W4A16_API const char *w4a16_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+W4A16_API int w4a16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H_ */

@@ -1,0 +1,108 @@
+"""Host-only checks of the C-ABI library: it loads, exports every entry point
+include/w4a16.h declares, and its host logic (validation, planning) behaves.
+No test here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__  # noqa: F401  (puts the repo root on sys.path)
+import weight_only_int4_codes_gb300 as w4
+from weight_only_int4_codes_gb300 import build as wbuild
+from weight_only_int4_codes_gb300 import native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wbuild.build()
+    return native.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w4a16_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for required in ("w4a16_quantize_pack", "w4a16_gemm", "w4a16_gemm_ex", "w4a16_dequantize",
+                     "w4a16_plan", "w4a16_get_kernel_status", "w4a16_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_no_internal_symbols_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", native.library_path()],
+                         capture_output=True, text=True).stdout
+    text_syms = [ln.split()[-1] for ln in out.splitlines() if " T " in ln]
+    assert text_syms and all(s.startswith("w4a16_") for s in text_syms), text_syms
+
+
+def test_version(lib):
+    assert lib.w4a16_version() >= 100
+
+
+@pytest.mark.parametrize("M,N,K,group,status", [
+    (1, 4096, 4000, 128, 1),    # K not a multiple of group
+    (1, 4096, 4096, 100, 1),    # group not a multiple of 8
+    (1, 4096, 4096, 8, 2),      # valid format, group below this build's minimum
+    (1, 4094, 4096, 128, 3),    # N % 4 != 0
+    (-1, 4096, 4096, 128, 1),   # negative size
+    (1, 4096, 0, 128, 1),       # K == 0
+])
+def test_validation_statuses(lib, M, N, K, group, status):
+    out = native.Config()
+    assert lib.w4a16_plan(M, N, K, group, None, ctypes.byref(out)) == status
+    assert lib.w4a16_last_error().decode()
+
+
+def test_gemm_rejects_before_touching_the_gpu(lib):
+    # shape errors and null pointers are caught on the host; M == 0 is a no-op
+    assert lib.w4a16_gemm(None, None, None, None, None, 1, 256, 500, 128, None) == 1
+    assert lib.w4a16_gemm(None, None, None, None, None, 0, 256, 512, 128, None) == 0
+    assert lib.w4a16_gemm(None, None, None, None, None, 1, 256, 512, 128, None) == 1
+    assert b"null" in lib.w4a16_last_error()
+    # misaligned pointers (never dereferenced: validation fails first)
+    assert lib.w4a16_gemm(8, 16, 16, 16, 16, 1, 256, 512, 128, None) == 3
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 4096, 4096), (4, 14336, 4096),
+                                   (8, 4096, 14336), (1, 768, 2048), (16, 2048, 768),
+                                   (3, 260, 512), (40, 1024, 1024)])
+def test_decode_plan_covers_k(M, N, K):
+    p = w4.plan(M, N, K, 128, path="decode")
+    assert p["path"] == 1
+    assert 1 <= p["split_k"] <= 8
+    assert p["warps_k"] * p["steps"] * 4 * p["split_k"] >= K // 8
+    assert p["steps"] % 4 == 0
+
+
+def test_plan_respects_requests():
+    p = w4.plan(1, 4096, 4096, 128, path="decode", split_k=4, warps_k=4, warps_n=1)
+    assert (p["split_k"], p["warps_k"], p["warps_n"]) == (4, 4, 1)
+    assert p["steps"] * 4 * 4 * 4 >= 4096 // 8
+    with pytest.raises(native.W4A16Error) as e:
+        w4.plan(1, 4096, 4096, 128, path="decode", split_k=9)
+    assert e.value.status == 2
+
+
+def test_auto_path_small_m_is_decode():
+    for M in (1, 2, 4, 8, 16):
+        assert w4.plan(M, 4096, 4096)["path"] == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(native, "_lib", None)
+    monkeypatch.setattr(native, "_PKG", str(tmp_path))
+    with pytest.raises(native.W4A16Error):
+        native.load_library()

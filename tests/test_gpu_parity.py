@@ -1,0 +1,241 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Bars: packing, scales, zeros and dequantized weights bit-exact; GEMM outputs
+max |out - ref| / max(1, |ref|) <= 5e-3 elementwise; one-hot activations give
+the dequantized row bit-exactly; repeated calls give identical bits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_int4_codes_gb300 as w4
+from weight_only_int4_codes_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def quantize_both(W, group):
+    """GPU quantize + oracle quantize of the same fp16 weight; asserts bit-exact."""
+    ref = oracle.quantize_pack(W, group)
+    got = w4.quantize_pack(to_dev(W), group)
+    torch.cuda.synchronize()
+    assert np.array_equal(got[0].cpu().numpy().view(np.uint32), ref[0]), "packed words differ"
+    assert np.array_equal(got[1].cpu().numpy().view(np.uint16), ref[1].view(np.uint16)), "scales"
+    assert np.array_equal(got[2].cpu().numpy().view(np.uint16), ref[2].view(np.uint16)), "zeros"
+    return got, ref
+
+
+def check_gemm(x, dev_w, ref_w, group, config=None, tol=TOL):
+    out = w4.gemm_ex(to_dev(x), *dev_w, group=group, config=config)
+    torch.cuda.synchronize()
+    assert w4.kernel_status() == 0
+    ref = oracle.gemm(x, *ref_w, group=group)
+    err = oracle.rel_err(out.cpu().numpy(), ref)
+    assert err <= tol, "rel err %.3g > %g (M=%d, config=%s)" % (err, tol, x.shape[0], config)
+    return out
+
+
+# ----------------------------------------------------------------- packing
+@pytest.mark.parametrize("K,N,group,outliers", [
+    (512, 256, 128, False),      # tiny correctness case
+    (4096, 4096, 128, False),    # decode square projection
+    (4096, 14336, 128, True),    # FFN gate/up with outliers
+    (14336, 4096, 128, True),    # FFN down with outliers
+    (2048, 768, 128, False),     # MoE expert
+    (768, 2048, 128, False),
+    (256, 260, 128, False),      # ragged N
+    (256, 64, 32, False),        # other group sizes
+    (512, 96, 64, True),
+    (1024, 128, 256, False),
+])
+def test_quantize_pack_and_dequantize_bit_exact(K, N, group, outliers):
+    W = synth.weight(K, N, seed=K + N + group, outliers=outliers)
+    got, ref = quantize_both(W, group)
+    wdq = w4.dequantize(*got, group=group)
+    torch.cuda.synchronize()
+    assert np.array_equal(wdq.cpu().numpy().view(np.uint16),
+                          oracle.dequant(*ref, group=group).view(np.uint16))
+
+
+def test_quantize_special_columns():
+    """Constant, all-positive, all-negative, zero and subnormal-range groups."""
+    K, N = 256, 16
+    W = synth.weight(K, N, seed=3).astype(np.float64)
+    W[:, 0] = 0.0
+    W[:, 1] = -3.0
+    W[:, 2] = np.abs(W[:, 2]) + 0.5
+    W[:, 3] = -np.abs(W[:, 3]) - 0.5
+    W[:, 4] = np.arange(K) % 16 * 2.0 ** -24
+    W[:128, 5] = 7.0
+    W[:, 6] = np.where(np.arange(K) % 2 == 0, 65504.0, -65504.0)
+    quantize_both(W.astype(np.float16), 128)
+
+
+def test_quantize_prefill_size_sampled_columns():
+    """K=8192, N=28672 (the largest prefill weight): all scales/zeros and the
+    packed words of 64 sampled columns against the oracle on those columns."""
+    K, N = 8192, 28672
+    W = synth.weight(K, N, seed=synth.weight_seed(4, shape_index=1))
+    packed, scales, zeros = w4.quantize_pack(to_dev(W), 128)
+    torch.cuda.synchronize()
+    cols = np.sort(np.random.Generator(np.random.PCG64(5)).choice(N, 64, replace=False))
+    ref = oracle.quantize_pack(np.ascontiguousarray(W[:, cols]), 128)
+    assert np.array_equal(packed.cpu().numpy().view(np.uint32)[:, cols], ref[0])
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16)[:, cols], ref[1].view(np.uint16))
+    assert np.array_equal(zeros.cpu().numpy().view(np.uint16)[:, cols], ref[2].view(np.uint16))
+
+
+# -------------------------------------------------------------------- GEMM
+@pytest.mark.parametrize("K,N,outliers", [
+    (512, 256, False), (4096, 4096, False), (2048, 768, False), (768, 2048, False),
+    (4096, 14336, True), (14336, 4096, True),
+])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_gemm_decode_configs(K, N, outliers, M):
+    W = synth.weight(K, N, seed=synth.weight_seed(1) + K + N, outliers=outliers)
+    dev_w, ref_w = quantize_both(W, 128)
+    x = synth.activations(M, K, seed=synth.x_seed(1, M) + K)
+    check_gemm(x, dev_w, ref_w, 128)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(path="decode", split_k=1, warps_k=8, warps_n=1),
+    dict(path="decode", split_k=2, warps_k=8, warps_n=1),
+    dict(path="decode", split_k=3, warps_k=4, warps_n=1),
+    dict(path="decode", split_k=8, warps_k=4, warps_n=1),
+    dict(path="decode", split_k=4, warps_k=4, warps_n=2),
+    dict(path="decode", split_k=5, warps_k=2, warps_n=4),
+    dict(path="decode", split_k=2, warps_k=2, warps_n=2),
+    dict(path="decode", split_k=7, warps_k=8, warps_n=1, steps=4),
+    dict(path="decode", pdl=True),
+])
+@pytest.mark.parametrize("M", [1, 3, 9, 16])
+def test_gemm_decode_launch_shapes(cfg, M):
+    """Every compiled kernel shape, several cluster sizes (including ones that
+    leave some CTAs of the cluster without K rows), ragged N."""
+    K, N = 1536, 1000
+    W = synth.weight(K, N, seed=21)
+    dev_w, ref_w = quantize_both(W, 128)
+    x = synth.activations(M, K, seed=22 + M)
+    check_gemm(x, dev_w, ref_w, 128, config=cfg)
+
+
+@pytest.mark.parametrize("group", [32, 64, 256])
+@pytest.mark.parametrize("M", [1, 12])
+def test_gemm_other_groups(group, M):
+    K, N = 1024, 384
+    W = synth.weight(K, N, seed=31 + group, outliers=True)
+    dev_w, ref_w = quantize_both(W, group)
+    x = synth.activations(M, K, seed=32)
+    check_gemm(x, dev_w, ref_w, group)
+
+
+@pytest.mark.parametrize("M", [17, 40, 100])
+def test_gemm_larger_m(M):
+    K, N = 1024, 512
+    W = synth.weight(K, N, seed=41)
+    dev_w, ref_w = quantize_both(W, 128)
+    x = synth.activations(M, K, seed=42)
+    check_gemm(x, dev_w, ref_w, 128)
+
+
+def test_gemm_random_encodings():
+    """Arbitrary valid codes, scales and zeros (not produced by the quantizer)."""
+    K, N = 2048, 512
+    packed, scales, zeros = synth.codes_and_params(K, N, 128, seed=51)
+    dev_w = (to_dev(packed.view(np.int32)), to_dev(scales), to_dev(zeros))
+    for M in (1, 7, 16):
+        x = synth.activations(M, K, seed=52 + M)
+        check_gemm(x, dev_w, (packed, scales, zeros), 128)
+
+
+def test_one_hot_is_exact():
+    """x = e_k: a single nonzero product, so out equals the dequantized row bit-exactly."""
+    K, N = 1024, 768
+    W = synth.weight(K, N, seed=61, outliers=True)
+    dev_w, ref_w = quantize_both(W, 128)
+    wdq = oracle.dequant(*ref_w, group=128).view(np.uint16)
+    ks = np.array([0, 1, 7, 8, 127, 128, 500, 1023, 640, 64, 333, 900, 17, 256, 1000, 2])
+    for M in (1, 16):
+        x = np.zeros((M, K), dtype=np.float16)
+        x[np.arange(M), ks[:M]] = 1.0
+        out = w4.gemm(to_dev(x), *dev_w, group=128)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), wdq[ks[:M]])
+
+
+def test_zero_input_and_dirty_output_and_determinism():
+    K, N, M = 4096, 4096, 8
+    W = synth.weight(K, N, seed=71)
+    dev_w, _ = quantize_both(W, 128)
+    x = to_dev(synth.activations(M, K, seed=72))
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    w4.gemm(torch.zeros_like(x), *dev_w, group=128, out=out)
+    torch.cuda.synchronize()
+    assert not out.isnan().any() and (out == 0).all()
+    first = w4.gemm(x, *dev_w, group=128).clone()
+    for _ in range(5):
+        out.fill_(float("nan"))
+        w4.gemm(x, *dev_w, group=128, out=out)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+    # scaling x by 2 doubles the output exactly (power-of-two scaling is exact)
+    out2 = w4.gemm((x.float() * 2).half(), *dev_w, group=128)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, first * 2)
+
+
+def test_matches_cublas_on_dequantized_weight():
+    """A library cross-check: cuBLAS fp16 on the dequantized weight agrees with
+    both the oracle and the fused kernel within the tolerance."""
+    K, N, M = 4096, 4096, 16
+    W = synth.weight(K, N, seed=81)
+    dev_w, ref_w = quantize_both(W, 128)
+    x = synth.activations(M, K, seed=82)
+    out = w4.gemm(to_dev(x), *dev_w, group=128)
+    wdq = w4.dequantize(*dev_w, group=128)
+    cub = to_dev(x) @ wdq
+    torch.cuda.synchronize()
+    ref = oracle.gemm(x, *ref_w, group=128)
+    assert oracle.rel_err(cub.cpu().numpy(), ref) <= TOL
+    assert oracle.rel_err(out.cpu().numpy(), cub.cpu().numpy().astype(np.float64)) <= 2 * TOL
+
+
+def test_empty_inputs():
+    K, N = 256, 128
+    W = synth.weight(K, N, seed=91)
+    dev_w, _ = quantize_both(W, 128)
+    out = w4.gemm(torch.empty((0, K), dtype=torch.float16, device=DEV), *dev_w, group=128)
+    assert out.shape == (0, N)
+
+
+def test_bench_launch_config_full_size_sampled():
+    """The decode-square workload at full size in the configuration the
+    benchmark times (automatic plan, programmatic dependent launch), checked on
+    every row and 256 sampled columns."""
+    K, N = 4096, 4096
+    W = synth.weight(K, N, seed=synth.weight_seed(1))
+    dev_w = w4.quantize_pack(to_dev(W), 128)
+    cols = np.sort(np.random.Generator(np.random.PCG64(9)).choice(N, 256, replace=False))
+    ref_w = oracle.quantize_pack(np.ascontiguousarray(W[:, cols]), 128)
+    for M in (1, 2, 4, 8, 16):
+        x = synth.activations(M, K, seed=synth.x_seed(1, M))
+        out = w4.gemm_ex(to_dev(x), *dev_w, group=128, config=dict(pdl=True))
+        torch.cuda.synchronize()
+        ref = oracle.gemm(x, *ref_w, group=128)
+        assert oracle.rel_err(out.cpu().numpy()[:, cols], ref) <= TOL

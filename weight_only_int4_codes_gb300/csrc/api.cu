@@ -1,0 +1,265 @@
+// api.cu -- the extern "C" boundary of libw4a16.so: argument validation,
+// launch planning (dispatch), error reporting.  Every compute step runs in the
+// kernels of quant.cu, decode.cu and prefill.cu.
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string>
+
+#include "common.cuh"
+
+namespace w4a16 {
+
+__device__ int g_kernel_status = 0;
+
+cudaError_t kernel_status_address(int **ptr) {
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_kernel_status);
+}
+
+cudaError_t kernel_status_read_clear(int *value) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_kernel_status, sizeof(int));
+    if (e == cudaSuccess && *value != 0)
+        e = cudaMemcpyToSymbol(g_kernel_status, &zero, sizeof(int));
+    return e;
+}
+
+namespace {
+
+thread_local std::string t_last_error;
+
+w4a16_status fail(w4a16_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+w4a16_status fail(w4a16_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+w4a16_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(W4A16_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr long long kMaxElems = (1ll << 31) - 1;
+
+// Shape rules common to all entry points (pointer checks done by callers).
+w4a16_status check_shape(int M, int N, int K, int group) {
+    if (M < 0 || N < 0 || K < 0)
+        return fail(W4A16_ERR_INVALID_ARG, "negative size (M=%d N=%d K=%d)", M, N, K);
+    if (group <= 0 || group % 8 != 0)
+        return fail(W4A16_ERR_INVALID_ARG, "group must be a positive multiple of 8 (got %d)", group);
+    if (group % 32 != 0 || group > 1024)
+        return fail(W4A16_ERR_UNSUPPORTED,
+                    "group %d: this library implements groups that are multiples of 32 up to 1024",
+                    group);
+    if (K == 0 || K % group != 0)
+        return fail(W4A16_ERR_INVALID_ARG, "K (%d) must be a positive multiple of group (%d)", K,
+                    group);
+    if (N % 4 != 0)
+        return fail(W4A16_ERR_MISALIGNED,
+                    "N (%d) must be a multiple of 4 so that packed rows are 16-byte aligned", N);
+    if ((long long)M * K > kMaxElems || (long long)K * N > kMaxElems ||
+        (long long)M * N > kMaxElems)
+        return fail(W4A16_ERR_UNSUPPORTED, "an operand exceeds 2^31-1 elements");
+    return W4A16_OK;
+}
+
+DeviceInfo query_device() {
+    DeviceInfo d{152, 10, 3};   // GB300 when no GPU is visible (host-only planning)
+    int dev = 0, n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) {
+        cudaGetLastError();
+        return d;
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return d;
+    }
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) d.sm_count = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess) d.cc_major = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess) d.cc_minor = v;
+    cudaGetLastError();
+    return d;
+}
+
+// -------------------------------------------------------------- planning
+// Decode path.  A column tile of 32*warps_n columns is covered by
+// warps_k * split warps along K, each streaming `steps` 32-row steps.  The
+// choice aims at enough CTAs to fill the SMs about twice (so that every SM has
+// loads from several warps in flight) with the fewest CTAs per cluster.
+void plan_decode(int M, int N, int K, int group, int sm_count, w4a16_config &c) {
+    const int U = decode_steps_per_batch(group);
+    if (c.warps_n <= 0) c.warps_n = M > 8 ? 2 : 1;
+    if (c.warps_k <= 0) c.warps_k = c.warps_n == 1 ? 8 : (c.warps_n == 2 ? 4 : 2);
+    const int strips = (N + 32 * c.warps_n - 1) / (32 * c.warps_n);
+    const int total_steps = K / 32;
+    if (c.split_k <= 0 && c.steps <= 0) {
+        // Most CTAs that still fit in one wave; ties go to the smaller cluster.
+        const long long capacity = (long long)sm_count * decode_ctas_per_sm(c, M, group);
+        int best_split = 0, best_steps = 0;
+        long long best_ctas = -1;
+        for (int s = 1; s <= 8; ++s) {
+            int st = (total_steps + c.warps_k * s - 1) / (c.warps_k * s);
+            st = (st + U - 1) / U * U;
+            const int s_eff = (total_steps + c.warps_k * st - 1) / (c.warps_k * st);
+            const long long ctas = (long long)strips * s_eff;
+            const bool fits = ctas <= capacity;
+            const bool better = best_ctas < 0 ||
+                                (fits && (best_ctas > capacity || ctas > best_ctas)) ||
+                                (!fits && best_ctas > capacity && ctas < best_ctas);
+            if (better) {
+                best_split = s_eff;
+                best_steps = st;
+                best_ctas = ctas;
+            }
+        }
+        c.split_k = best_split;
+        c.steps = best_steps;
+    } else if (c.steps <= 0) {
+        int st = (total_steps + c.warps_k * c.split_k - 1) / (c.warps_k * c.split_k);
+        c.steps = (st + U - 1) / U * U;
+    } else if (c.split_k <= 0) {
+        c.split_k = (total_steps + c.warps_k * c.steps - 1) / (c.warps_k * c.steps);
+    }
+}
+
+// Crossover between the decode path and the tcgen05 prefill path, in rows of x
+// (measured on GB300; see the dispatch notes in the design document).
+constexpr int kDecodeMaxM = 16;
+
+w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
+                       w4a16_config &c) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    c = req ? *req : w4a16_config{};
+    if (c.path == W4A16_PATH_AUTO) {
+        c.path = W4A16_PATH_DECODE;
+        if (M > kDecodeMaxM) {
+            w4a16_config pc = c;
+            pc.path = W4A16_PATH_PREFILL;
+            if (prefill_config_supported(pc, M, N, K, group)) c.path = W4A16_PATH_PREFILL;
+        }
+    }
+    if (c.path == W4A16_PATH_DECODE) {
+        plan_decode(M, N, K, group, device_info().sm_count, c);
+        if (!decode_config_supported(c, M) || c.steps % decode_steps_per_batch(group) != 0 ||
+            (long long)c.warps_k * c.steps * 4 * c.split_k < K / 8)
+            return fail(W4A16_ERR_UNSUPPORTED,
+                        "decode configuration not available (split_k=%d warps_k=%d warps_n=%d "
+                        "steps=%d)",
+                        c.split_k, c.warps_k, c.warps_n, c.steps);
+    } else if (c.path == W4A16_PATH_PREFILL) {
+        if (c.tile_m <= 0) c.tile_m = M >= 256 ? 256 : ((M + 15) / 16) * 16;
+        if (!prefill_config_supported(c, M, N, K, group))
+            return fail(W4A16_ERR_UNSUPPORTED, "prefill path not available for M=%d N=%d K=%d "
+                        "group=%d tile_m=%d", M, N, K, group, c.tile_m);
+    } else {
+        return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", c.path);
+    }
+    return W4A16_OK;
+}
+
+}  // namespace
+
+const DeviceInfo &device_info() {
+    static DeviceInfo info;
+    static std::once_flag once;
+    std::call_once(once, [] { info = query_device(); });
+    return info;
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+w4a16_status w4a16_quantize_pack(const uint16_t *W, int K, int N, int group, uint32_t *packed,
+                                 uint16_t *scales, uint16_t *zeros, cudaStream_t stream) {
+    w4a16_status st = check_shape(0, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if (!W || !packed || !scales || !zeros)
+        return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+    if (((uintptr_t)W & 1) || ((uintptr_t)packed & 3) || ((uintptr_t)scales & 1) ||
+        ((uintptr_t)zeros & 1))
+        return fail(W4A16_ERR_MISALIGNED, "pointer not aligned to its element size");
+    cudaError_t e = launch_quantize_pack(W, K, N, group, packed, scales, zeros, stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "quantize_pack launch");
+}
+
+w4a16_status w4a16_dequantize(const uint32_t *packed, const uint16_t *scales,
+                              const uint16_t *zeros, uint16_t *W_out, int K, int N, int group,
+                              cudaStream_t stream) {
+    w4a16_status st = check_shape(0, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if (!W_out || !packed || !scales || !zeros)
+        return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+    if (((uintptr_t)W_out & 1) || ((uintptr_t)packed & 3) || ((uintptr_t)scales & 1) ||
+        ((uintptr_t)zeros & 1))
+        return fail(W4A16_ERR_MISALIGNED, "pointer not aligned to its element size");
+    cudaError_t e = launch_dequantize(packed, scales, zeros, W_out, K, N, group, stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "dequantize launch");
+}
+
+w4a16_status w4a16_plan(int M, int N, int K, int group, const w4a16_config *request,
+                        w4a16_config *plan_out) {
+    if (!plan_out) return fail(W4A16_ERR_INVALID_ARG, "plan_out is null");
+    w4a16_config c;
+    w4a16_status st = make_plan(M, N, K, group, request, c);
+    if (st == W4A16_OK) *plan_out = c;
+    return st;
+}
+
+w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed, const uint16_t *scales,
+                           const uint16_t *zeros, uint16_t *out, int M, int N, int K, int group,
+                           const w4a16_config *cfg, cudaStream_t stream) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if (!x || !packed || !scales || !zeros || !out)
+        return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales) || !aligned16(zeros) ||
+        !aligned16(out))
+        return fail(W4A16_ERR_MISALIGNED, "x, packed, scales, zeros and out must be 16-byte "
+                    "aligned");
+    w4a16_config c;
+    st = make_plan(M, N, K, group, cfg, c);
+    if (st != W4A16_OK) return st;
+    GemmArgs a{x, packed, scales, zeros, out, M, N, K, group};
+    cudaError_t e = c.path == W4A16_PATH_DECODE ? launch_decode(a, c, stream)
+                                                : launch_prefill(a, c, stream);
+    if (e == cudaErrorNotSupported)
+        return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "gemm launch");
+}
+
+w4a16_status w4a16_gemm(const uint16_t *x, const uint32_t *packed, const uint16_t *scales,
+                        const uint16_t *zeros, uint16_t *out, int M, int N, int K, int group,
+                        cudaStream_t stream) {
+    return w4a16_gemm_ex(x, packed, scales, zeros, out, M, N, K, group, nullptr, stream);
+}
+
+w4a16_status w4a16_get_kernel_status(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int v = 0;
+    e = kernel_status_read_clear(&v);
+    if (e != cudaSuccess) return cuda_fail(e, "read/clear the device status word");
+    if (v != 0)
+        return fail((w4a16_status)v, "a kernel reported status %d (bounded wait gave up)", v);
+    return W4A16_OK;
+}
+
+const char *w4a16_last_error(void) { return t_last_error.c_str(); }
+
+int w4a16_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// common.cuh -- internal declarations shared by the libw4a16 translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "w4a16.h"
+
+namespace w4a16 {
+
+// Device-side status word: kernels with bounded waits receive its address and
+// write W4A16_ERR_TIMEOUT there (first writer wins) when a wait gives up;
+// w4a16_get_kernel_status reads and clears it.  The word lives in api.cu
+// (one copy per device); these host helpers are the only way to reach it.
+cudaError_t kernel_status_address(int **ptr);        // current device
+cudaError_t kernel_status_read_clear(int *value);    // current device, synchronous
+
+__device__ __forceinline__ void report_status(int *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- launchers
+struct GemmArgs {
+    const uint16_t *x;
+    const uint32_t *packed;
+    const uint16_t *scales;
+    const uint16_t *zeros;
+    uint16_t *out;
+    int M, N, K, group;
+};
+
+// Each returns cudaSuccess or the launch error; they never synchronize.
+cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group,
+                                 uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                 cudaStream_t stream);
+cudaError_t launch_dequantize(const uint32_t *packed, const uint16_t *scales,
+                              const uint16_t *zeros, uint16_t *W_out, int K, int N,
+                              int group, cudaStream_t stream);
+// Decode path: cfg already fully resolved (split_k, warps_k, warps_n, steps > 0).
+// Returns cudaErrorNotSupported for a configuration with no compiled kernel.
+cudaError_t launch_decode(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
+bool decode_config_supported(const w4a16_config &cfg, int M);
+int decode_steps_per_batch(int group);
+// Resident CTAs per SM of the decode kernel that `cfg` selects (occupancy
+// query on the current device; a fixed estimate when no GPU is present).
+int decode_ctas_per_sm(const w4a16_config &cfg, int M, int group);
+// Prefill path (tcgen05).  Returns cudaErrorNotSupported if unavailable.
+cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
+bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group);
+
+// Hardware facts used by the planner (queried once per device, cached).
+struct DeviceInfo {
+    int sm_count;
+    int cc_major, cc_minor;
+};
+const DeviceInfo &device_info();   // host; falls back to GB300 numbers when no GPU
+
+// ------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+    // (a & mask) | bits in one LOP3 (truth table 0xEA)
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(bits));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// griddepcontrol (programmatic dependent launch); no-ops without the launch
+// attribute.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace w4a16

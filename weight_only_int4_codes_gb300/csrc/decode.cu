@@ -1,0 +1,471 @@
+// decode.cu -- W4A16 GEMM for small M (the decode regime, M <= 16 per pass).
+//
+// What it computes: out[m,n] = sum_k x[m,k] * (q[k,n] - z[g(k),n]) * s[g(k),n],
+// fp32 accumulation, fp16 result (page "Beating FP16 with 4-bit Weights: A
+// Portable W4A16 GEMM in Triton", sections "The design" and "Things I got wrong
+// along the way"; page "Triton Kernel Matches bitsandbytes: Why Both Lose to
+// Math", sections "Three Kernel Versions" and "Why Marlin Is Still Faster").
+//
+// At M <= 16 the GEMM is a race to stream the packed weight out of HBM; the
+// design follows from that:
+//   * Every packed word is loaded exactly once, as part of a 128-bit load of
+//     four neighbouring columns (coalesced along N), with an L2 evict-first
+//     hint and no L1 allocation.  (The 8x redundant word load is the first
+//     mistake the first page describes.)
+//   * Nibbles become fp16 in registers with the magic-exponent trick: OR-ing a
+//     nibble into the mantissa of 1024.0 (0x6400, low nibble) or 64.0 (0x5400,
+//     nibble shifted by 4) yields 1024+q or 64+q exactly, one LOP3 per two
+//     codes.  Subtracting the matching 1024+z / 64+z gives q - z exactly.
+//   * The multiply-accumulate runs on the tensor cores through register-fed
+//     mma.m16n8k16 with the roles swapped: the 16 "rows" of the MMA are 16
+//     output columns of W, the 8 "columns" are batch rows of x.  K may be
+//     permuted freely inside the reduction as long as x and W use the same
+//     permutation, so each thread's 128-bit word load maps directly onto A
+//     fragments, and x is permuted to match with four PRMTs.  CUDA-core FMA
+//     cannot keep up with HBM at M >= 2 (it needs M FMAs per weight).
+//   * The scale is applied once per group in fp32 to the MMA's group partial
+//     (acc += s * sum_k x (q - z)), not per weight.
+//   * Split-K: a column tile's K range is split across the warps of a CTA and
+//     across the CTAs of one thread-block cluster.  Partials are reduced in a
+//     FIXED order: warps through shared memory, then CTAs through distributed
+//     shared memory after a cluster barrier.  No atomics, no global workspace,
+//     no spin-waits, bitwise reproducible.  (The pages merge split-K partials
+//     with fp32 atomics; the second page names a second-stage reduction as the
+//     alternative, which this is.)
+#include <cooperative_groups.h>
+#include <map>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace w4a16 {
+namespace {
+
+struct DecodeArgs {
+    const uint16_t *x;
+    const uint32_t *packed;
+    const uint16_t *scales;
+    const uint16_t *zeros;
+    uint16_t *out;
+    int M, N, K, group;
+    int steps;          // 32-row K steps per warp (a multiple of U)
+    int rows_per_cta;   // packed rows per CTA = warps_k * steps * 4
+    int split;          // CTAs along K = gridDim.y = cluster size
+};
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Weight stream: read once, never reused by this SM -> no L1 allocation,
+// evict-first in L2.
+__device__ __forceinline__ uint4 ld_weights(const uint32_t *ptr, uint64_t pol) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr), "l"(pol));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *ptr) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr));
+    return r;
+}
+
+__device__ __forceinline__ uint2 ld_nc_v2(const void *ptr) {
+    uint2 r;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(ptr));
+    return r;
+}
+
+// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr uint32_t kMaskLo = 0x000F000Fu;   // nibbles 0 and 4 of a word
+constexpr uint32_t kMaskHi = 0x00F000F0u;   // nibbles 1 and 5
+constexpr uint32_t kMagicLo = 0x64006400u;  // 1024.0 | 1024.0 (ulp 1 at bits 0..3)
+constexpr uint32_t kMagicHi = 0x54005400u;  // 64.0 | 64.0 (ulp 1 at bits 4..7)
+
+// One K-batch of U steps: the words of 4 columns x U steps, plus that batch's
+// group scale and zero (a batch never straddles a group).
+template <int U>
+struct Batch {
+    uint4 w[U];
+    uint2 s, z;
+};
+
+template <int U>
+__device__ __forceinline__ void load_batch(Batch<U> &b, const uint32_t *wptr, size_t wstride,
+                                           const uint16_t *sz_s, const uint16_t *sz_z,
+                                           uint64_t pol) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) b.w[u] = ld_weights(wptr + u * wstride, pol);
+    b.s = ld_nc_v2(sz_s);
+    b.z = ld_nc_v2(sz_z);
+}
+
+// Per-thread state and the MMA work of one batch.
+//   thread (g = lane/4, t = lane%4) owns columns col0..col0+3 (col0 = 4g + ...)
+//   and, in step u, packed row  row = row0 + 4*(batch*U + u) + t.
+//   MMA tile j (j = 0, 1) has rows {g -> column col0+2j, g+8 -> column col0+2j+1}.
+//   K slots of the MMA map onto the word's nibbles as
+//       kk = 0: slots (2t, 2t+1, 2t+8, 2t+9) <- nibbles (0, 4, 1, 5)
+//       kk = 1: slots (2t, 2t+1, 2t+8, 2t+9) <- nibbles (2, 6, 3, 7)
+//   so the B (x) fragment needs x[k0+0], x[k0+4] | x[k0+1], x[k0+5] for kk=0.
+template <int NT, int U>
+__device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batch<U> &b,
+                                              const uint16_t *xrow0, const uint16_t *xrow1,
+                                              bool m0_ok, bool m1_ok, int krow_first,
+                                              int t) {
+    // zero biases (1024+z, 64+z) broadcast per column, fp32 scales per column
+    const uint32_t zlo01 = hadd2_u32(b.z.x, kMagicLo);   // (1024+z0, 1024+z1)
+    const uint32_t zlo23 = hadd2_u32(b.z.y, kMagicLo);
+    const uint32_t zhi01 = hadd2_u32(b.z.x, kMagicHi);   // (64+z0, 64+z1)
+    const uint32_t zhi23 = hadd2_u32(b.z.y, kMagicHi);
+    const uint32_t zA[4] = {__byte_perm(zlo01, 0, 0x1010), __byte_perm(zlo01, 0, 0x3232),
+                            __byte_perm(zlo23, 0, 0x1010), __byte_perm(zlo23, 0, 0x3232)};
+    const uint32_t zB[4] = {__byte_perm(zhi01, 0, 0x1010), __byte_perm(zhi01, 0, 0x3232),
+                            __byte_perm(zhi23, 0, 0x1010), __byte_perm(zhi23, 0, 0x3232)};
+    const __half2 s01 = *reinterpret_cast<const __half2 *>(&b.s.x);
+    const __half2 s23 = *reinterpret_cast<const __half2 *>(&b.s.y);
+    const float sc[4] = {__low2float(s01), __high2float(s01), __low2float(s23),
+                         __high2float(s23)};
+
+    // x fragments of all U steps first (several loads in flight)
+    uint4 xr[NT][U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int koff = 8 * (krow_first + 4 * u + t);
+        xr[0][u] = m0_ok ? ld_nc_v4(xrow0 + koff) : make_uint4(0, 0, 0, 0);
+        if (NT > 1) xr[NT - 1][u] = m1_ok ? ld_nc_v4(xrow1 + koff) : make_uint4(0, 0, 0, 0);
+    }
+
+    float gacc[NT][2][4];
+#pragma unroll
+    for (int p = 0; p < NT; ++p)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) gacc[p][j][r] = 0.f;
+
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        uint32_t bx[NT][4];
+#pragma unroll
+        for (int p = 0; p < NT; ++p) {
+            const uint4 v = xr[p][u];            // (x0x1, x2x3, x4x5, x6x7)
+            bx[p][0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
+            bx[p][1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
+            bx[p][2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
+            bx[p][3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
+        }
+        const uint32_t wv[4] = {b.w[u].x, b.w[u].y, b.w[u].z, b.w[u].w};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t c0 = wv[2 * j], c1 = wv[2 * j + 1];
+            // kk = 0: nibbles (0,4) and (1,5)
+            {
+                const uint32_t a0 = hsub2_u32(lop3_and_or(c0, kMaskLo, kMagicLo), zA[2 * j]);
+                const uint32_t a1 = hsub2_u32(lop3_and_or(c1, kMaskLo, kMagicLo), zA[2 * j + 1]);
+                const uint32_t a2 = hsub2_u32(lop3_and_or(c0, kMaskHi, kMagicHi), zB[2 * j]);
+                const uint32_t a3 = hsub2_u32(lop3_and_or(c1, kMaskHi, kMagicHi), zB[2 * j + 1]);
+#pragma unroll
+                for (int p = 0; p < NT; ++p)
+                    mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][0], bx[p][1]);
+            }
+            // kk = 1: nibbles (2,6) and (3,7)
+            {
+                const uint32_t d0 = c0 >> 8, d1 = c1 >> 8;
+                const uint32_t a0 = hsub2_u32(lop3_and_or(d0, kMaskLo, kMagicLo), zA[2 * j]);
+                const uint32_t a1 = hsub2_u32(lop3_and_or(d1, kMaskLo, kMagicLo), zA[2 * j + 1]);
+                const uint32_t a2 = hsub2_u32(lop3_and_or(d0, kMaskHi, kMagicHi), zB[2 * j]);
+                const uint32_t a3 = hsub2_u32(lop3_and_or(d1, kMaskHi, kMagicHi), zB[2 * j + 1]);
+#pragma unroll
+                for (int p = 0; p < NT; ++p)
+                    mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][2], bx[p][3]);
+            }
+        }
+    }
+    // apply the group scale in fp32: rows g (c0, c1) -> column col0+2j,
+    // rows g+8 (c2, c3) -> column col0+2j+1
+#pragma unroll
+    for (int p = 0; p < NT; ++p)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            acc[p][j][0] = fmaf(sc[2 * j], gacc[p][j][0], acc[p][j][0]);
+            acc[p][j][1] = fmaf(sc[2 * j], gacc[p][j][1], acc[p][j][1]);
+            acc[p][j][2] = fmaf(sc[2 * j + 1], gacc[p][j][2], acc[p][j][2]);
+            acc[p][j][3] = fmaf(sc[2 * j + 1], gacc[p][j][3], acc[p][j][3]);
+        }
+}
+
+// Grid: (ceil(N / (32*WN)), split, ceil(M / 16)); cluster (1, split, 1).
+// Block: 32*WN*WK threads; dynamic shared memory (WK + 1) * 16 * 32*WN floats.
+template <int NT, int WN, int WK, int U>
+__global__ void __launch_bounds__(32 * WN * WK)
+decode_kernel(const DecodeArgs a)
+{
+    extern __shared__ float smem[];
+    constexpr int BN = 32 * WN;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wn = warp % WN, wk = warp / WN;
+    const int g = lane >> 2, t = lane & 3;
+    const int m_base = blockIdx.z * 16;
+    const int Mc = min(16, a.M - m_base);
+    const int col0 = blockIdx.x * BN + wn * 32 + 4 * g;
+    const bool col_ok = col0 < a.N;                 // N % 4 == 0: all 4 columns valid
+    const int KB = a.K >> 3;                        // packed rows
+    const int row0 = blockIdx.y * a.rows_per_cta + wk * a.steps * 4;
+    const int nsteps = col_ok ? max(0, min(a.steps, (KB - row0) >> 2)) : 0;
+    const int nbatch = nsteps / U;                  // nsteps is a multiple of U
+
+    const uint64_t pol = evict_first_policy();
+    const size_t wstride = (size_t)4 * a.N;         // one step = 4 packed rows
+    const uint32_t *wptr = a.packed + (size_t)(row0 + t) * a.N + col0;
+    const uint16_t *sptr = a.scales + col0;
+    const uint16_t *zptr = a.zeros + col0;
+    // group row of batch b: (8 * (row0 + 4*U*b)) / group
+    const int rows_per_group = a.group >> 3;
+
+    float acc[NT][2][4];
+#pragma unroll
+    for (int p = 0; p < NT; ++p)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[p][j][r] = 0.f;
+
+    const int m0 = g, m1 = 8 + g;
+    const bool m0_ok = m0 < Mc, m1_ok = m1 < Mc;
+    const uint16_t *xrow0 = a.x + (size_t)(m_base + (m0_ok ? m0 : 0)) * a.K;
+    const uint16_t *xrow1 = a.x + (size_t)(m_base + (m1_ok ? m1 : 0)) * a.K;
+
+    Batch<U> ba, bb;
+    if (nbatch > 0) {
+        const size_t grow = (size_t)(row0 / rows_per_group) * a.N;
+        load_batch<U>(ba, wptr, wstride, sptr + grow, zptr + grow, pol);
+    }
+    // Everything above only touches the weights.  x and out may belong to the
+    // previous kernel on the stream (programmatic dependent launch).
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (int bi = 0; bi < nbatch; bi += 2) {
+        if (bi + 1 < nbatch) {
+            const int r = row0 + 4 * U * (bi + 1);
+            const size_t grow = (size_t)(r / rows_per_group) * a.N;
+            load_batch<U>(bb, wptr + (size_t)(bi + 1) * U * wstride, wstride, sptr + grow,
+                          zptr + grow, pol);
+        }
+        compute_batch<NT, U>(acc, ba, xrow0, xrow1, m0_ok, m1_ok, row0 + 4 * U * bi, t);
+        if (bi + 1 < nbatch) {
+            if (bi + 2 < nbatch) {
+                const int r = row0 + 4 * U * (bi + 2);
+                const size_t grow = (size_t)(r / rows_per_group) * a.N;
+                load_batch<U>(ba, wptr + (size_t)(bi + 2) * U * wstride, wstride, sptr + grow,
+                              zptr + grow, pol);
+            }
+            compute_batch<NT, U>(acc, bb, xrow0, xrow1, m0_ok, m1_ok,
+                                 row0 + 4 * U * (bi + 1), t);
+        }
+    }
+
+    // ---- reduction 1: the WK warps of this CTA, through shared memory
+    float *red = smem;                    // [WK][16][BN]
+    float *part = smem + WK * 16 * BN;    // [16][BN] this CTA's partial
+#pragma unroll
+    for (int p = 0; p < NT; ++p)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int m = 8 * p + 2 * t + (r & 1);
+                const int c = wn * 32 + 4 * g + 2 * j + (r >> 1);
+                if (m < Mc) red[(wk * 16 + m) * BN + c] = acc[p][j][r];
+            }
+    __syncthreads();
+    const int E = Mc * BN;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int m = e / BN, c = e - m * BN;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < WK; ++w) v += red[(w * 16 + m) * BN + c];
+        if (a.split == 1) {
+            const int col = blockIdx.x * BN + c;
+            if (col < a.N)
+                a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
+        } else {
+            part[e] = v;
+        }
+    }
+    if (a.split == 1) return;
+
+    // ---- reduction 2: the CTAs of the cluster, through distributed shared
+    // memory, in rank order.  Rank r finalizes a contiguous slice of outputs.
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int rank = (int)cluster.block_rank();
+    const int per = (E + a.split - 1) / a.split;
+    const int e_end = min(E, (rank + 1) * per);
+    for (int e = rank * per + threadIdx.x; e < e_end; e += blockDim.x) {
+        float v = 0.f;
+        for (int q = 0; q < a.split; ++q) v += cluster.map_shared_rank(part, q)[e];
+        const int m = e / BN, c = e - m * BN;
+        const int col = blockIdx.x * BN + c;
+        if (col < a.N)
+            a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
+    }
+    cluster.sync();   // keep this CTA's shared memory alive until all peers have read it
+}
+
+template <int NT, int WN, int WK, int U>
+cudaError_t launch_one(const DecodeArgs &da, int strips, int mchunks, bool pdl,
+                       cudaStream_t stream) {
+    constexpr int BN = 32 * WN;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(strips, da.split, mchunks);
+    lc.blockDim = dim3(32 * WN * WK, 1, 1);
+    lc.dynamicSmemBytes = (size_t)(WK + 1) * 16 * BN * sizeof(float);
+    lc.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (da.split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = da.split;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    lc.attrs = attrs;
+    lc.numAttrs = na;
+    return cudaLaunchKernelEx(&lc, decode_kernel<NT, WN, WK, U>, da);
+}
+
+template <int NT, int U>
+cudaError_t launch_shape(const DecodeArgs &da, int wn, int wk, int strips, int mchunks,
+                         bool pdl, cudaStream_t s) {
+    if (wn == 1 && wk == 4) return launch_one<NT, 1, 4, U>(da, strips, mchunks, pdl, s);
+    if (wn == 1 && wk == 8) return launch_one<NT, 1, 8, U>(da, strips, mchunks, pdl, s);
+    if (wn == 2 && wk == 4) return launch_one<NT, 2, 4, U>(da, strips, mchunks, pdl, s);
+    if (wn == 4 && wk == 2) return launch_one<NT, 4, 2, U>(da, strips, mchunks, pdl, s);
+    if (wn == 2 && wk == 2) return launch_one<NT, 2, 2, U>(da, strips, mchunks, pdl, s);
+    return cudaErrorNotSupported;
+}
+
+int steps_per_batch(int group) {
+    const int spg = group / 32;
+    return spg % 4 == 0 ? 4 : (spg % 2 == 0 ? 2 : 1);
+}
+
+}  // namespace
+
+namespace {
+template <int NT, int U>
+const void *kernel_for(int wn, int wk) {
+    if (wn == 1 && wk == 4) return (const void *)decode_kernel<NT, 1, 4, U>;
+    if (wn == 1 && wk == 8) return (const void *)decode_kernel<NT, 1, 8, U>;
+    if (wn == 2 && wk == 4) return (const void *)decode_kernel<NT, 2, 4, U>;
+    if (wn == 4 && wk == 2) return (const void *)decode_kernel<NT, 4, 2, U>;
+    if (wn == 2 && wk == 2) return (const void *)decode_kernel<NT, 2, 2, U>;
+    return nullptr;
+}
+}  // namespace
+
+int decode_ctas_per_sm(const w4a16_config &cfg, int M, int group) {
+    const int U = steps_per_batch(group);
+    const bool nt2 = M > 8;
+    const void *fn = nullptr;
+    if (U == 4) fn = nt2 ? kernel_for<2, 4>(cfg.warps_n, cfg.warps_k) : kernel_for<1, 4>(cfg.warps_n, cfg.warps_k);
+    else if (U == 2) fn = nt2 ? kernel_for<2, 2>(cfg.warps_n, cfg.warps_k) : kernel_for<1, 2>(cfg.warps_n, cfg.warps_k);
+    else fn = nt2 ? kernel_for<2, 1>(cfg.warps_n, cfg.warps_k) : kernel_for<1, 1>(cfg.warps_n, cfg.warps_k);
+    const int threads = 32 * cfg.warps_n * cfg.warps_k;
+    const size_t smem = (size_t)(cfg.warps_k + 1) * 16 * 32 * cfg.warps_n * sizeof(float);
+    // occupancy is a property of the kernel, so the answer is cached per kernel
+    static std::mutex mu;
+    static std::map<const void *, int> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(fn);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0, ndev = 0;
+    if (!(fn && cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0 &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) == cudaSuccess &&
+          n > 0)) {
+        cudaGetLastError();
+        // no GPU: registers (about 100 per thread at M <= 8, 128 above) bound it
+        const int regs = nt2 ? 128 : 104;
+        n = 65536 / (regs * threads);
+        if (n < 1) n = 1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[fn] = n;
+    return n;
+}
+
+bool decode_config_supported(const w4a16_config &cfg, int /*M*/) {
+    const int wn = cfg.warps_n, wk = cfg.warps_k;
+    const bool shape_ok = (wn == 1 && (wk == 4 || wk == 8)) || (wn == 2 && (wk == 4 || wk == 2)) ||
+                          (wn == 4 && wk == 2);
+    return shape_ok && cfg.split_k >= 1 && cfg.split_k <= 8 && cfg.steps >= 1;
+}
+
+cudaError_t launch_decode(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
+    if (!decode_config_supported(cfg, a.M)) return cudaErrorNotSupported;
+    const int U = steps_per_batch(a.group);
+    if (cfg.steps % U != 0) return cudaErrorNotSupported;
+    DecodeArgs da;
+    da.x = a.x;
+    da.packed = a.packed;
+    da.scales = a.scales;
+    da.zeros = a.zeros;
+    da.out = a.out;
+    da.M = a.M;
+    da.N = a.N;
+    da.K = a.K;
+    da.group = a.group;
+    da.steps = cfg.steps;
+    da.rows_per_cta = cfg.warps_k * cfg.steps * 4;
+    da.split = cfg.split_k;
+    // the split CTAs must cover K
+    const long long covered = (long long)da.rows_per_cta * da.split;
+    if (covered < a.K / 8) return cudaErrorInvalidValue;
+    const int strips = (a.N + 32 * cfg.warps_n - 1) / (32 * cfg.warps_n);
+    const int mchunks = (a.M + 15) / 16;
+    if (mchunks > 65535) return cudaErrorInvalidValue;
+    const bool pdl = (cfg.flags & W4A16_FLAG_PDL) != 0;
+    const bool nt2 = a.M > 8;
+    switch (U) {
+    case 4:
+        return nt2 ? launch_shape<2, 4>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream)
+                   : launch_shape<1, 4>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream);
+    case 2:
+        return nt2 ? launch_shape<2, 2>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream)
+                   : launch_shape<1, 2>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream);
+    default:
+        return nt2 ? launch_shape<2, 1>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream)
+                   : launch_shape<1, 1>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream);
+    }
+}
+
+int decode_steps_per_batch(int group) { return steps_per_batch(group); }
+
+}  // namespace w4a16

@@ -1,0 +1,193 @@
+"""ctypes binding of libw4a16.so (declared in include/w4a16.h).
+
+Argument marshalling only: tensors are checked for device, dtype and
+contiguity, their data pointers and the current CUDA stream are handed to the
+C ABI, and a non-OK status becomes a ``W4A16Error``.  Every step of the
+computation runs in the library's CUDA kernels; if the library is missing this
+module raises instead of falling back to anything else.
+
+PyTorch is used here only for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libw4a16.so"
+
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA",
+                5: "TIMEOUT"}
+PATHS = {"auto": 0, "decode": 1, "prefill": 2}
+FLAG_PDL = 0x1
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("w4a16 %s (%d): %s" % (STATUS_NAMES.get(status, "?"), status, message))
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("warps_k", ctypes.c_int),
+                ("warps_n", ctypes.c_int), ("steps", ctypes.c_int), ("tile_m", ctypes.c_int),
+                ("flags", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+    @classmethod
+    def make(cls, cfg):
+        if cfg is None:
+            return None
+        if isinstance(cfg, Config):
+            return cfg
+        c = cls()
+        for k, v in dict(cfg).items():
+            if k == "path" and isinstance(v, str):
+                v = PATHS[v]
+            if k == "pdl":
+                c.flags |= FLAG_PDL if v else 0
+                continue
+            setattr(c, k, int(v))
+        return c
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, _LIB_NAME)
+
+
+def load_library():
+    """Load libw4a16.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise W4A16Error(4, "%s is not built; run `python -c 'import __graft_entry__ as g; "
+                                "g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        sig = {
+            "w4a16_quantize_pack": [P, I, I, I, P, P, P, P],
+            "w4a16_dequantize": [P, P, P, P, I, I, I, P],
+            "w4a16_gemm": [P, P, P, P, P, I, I, I, I, P],
+            "w4a16_gemm_ex": [P, P, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
+            "w4a16_plan": [I, I, I, I, ctypes.POINTER(Config), ctypes.POINTER(Config)],
+            "w4a16_get_kernel_status": [P],
+            "w4a16_last_error": [],
+            "w4a16_version": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.w4a16_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load_library().w4a16_last_error().decode(errors="replace")
+        raise W4A16Error(status, msg)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def quantize_pack(W: torch.Tensor, group: int = 128, stream=None):
+    """fp16 W [K,N] -> (packed int32 [K/8,N], scales fp16 [K/g,N], zeros fp16 [K/g,N])."""
+    K, N = W.shape
+    packed = torch.empty((K // 8, N), dtype=torch.int32, device=W.device)
+    scales = torch.empty((K // group, N), dtype=torch.float16, device=W.device)
+    zeros = torch.empty((K // group, N), dtype=torch.float16, device=W.device)
+    _check(load_library().w4a16_quantize_pack(
+        _dev(W, "W", torch.float16), K, N, group, _dev(packed, "packed", torch.int32),
+        _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
+        _stream_handle(stream)))
+    return packed, scales, zeros
+
+
+def dequantize(packed, scales, zeros, group: int = 128, stream=None) -> torch.Tensor:
+    """-> fp16 W [K,N] = fp16((q - z) * s)."""
+    K, N = packed.shape[0] * 8, packed.shape[1]
+    W = torch.empty((K, N), dtype=torch.float16, device=packed.device)
+    _check(load_library().w4a16_dequantize(
+        _dev(packed, "packed", torch.int32), _dev(scales, "scales", torch.float16),
+        _dev(zeros, "zeros", torch.float16), _dev(W, "W_out", torch.float16), K, N, group,
+        _stream_handle(stream)))
+    return W
+
+
+def gemm_ex(x, packed, scales, zeros, group: int = 128, out=None, config=None, stream=None):
+    """out [M,N] fp16 = x [M,K] @ dequant(packed, scales, zeros); ``config`` is a
+    dict of w4a16_config fields (path may be 'auto' | 'decode' | 'prefill',
+    pdl=True sets W4A16_FLAG_PDL)."""
+    M, K = x.shape
+    N = packed.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    cfg = Config.make(config)
+    _check(load_library().w4a16_gemm_ex(
+        _dev(x, "x", torch.float16), _dev(packed, "packed", torch.int32),
+        _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
+        _dev(out, "out", torch.float16), M, N, K, group,
+        ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
+    return out
+
+
+def gemm(x, packed, scales, zeros, group: int = 128, out=None, stream=None):
+    """out [M,N] fp16 = x [M,K] @ dequant(packed, scales, zeros), automatic path."""
+    M, K = x.shape
+    N = packed.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(load_library().w4a16_gemm(
+        _dev(x, "x", torch.float16), _dev(packed, "packed", torch.int32),
+        _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
+        _dev(out, "out", torch.float16), M, N, K, group, _stream_handle(stream)))
+    return out
+
+
+def plan(M: int, N: int, K: int, group: int = 128, **request) -> dict:
+    """Launch configuration the library would use (host only, nothing enqueued)."""
+    req = Config.make(request) if request else None
+    out = Config()
+    _check(load_library().w4a16_plan(M, N, K, group, ctypes.byref(req) if req else None,
+                                     ctypes.byref(out)))
+    return out.as_dict()
+
+
+def kernel_status(stream=None) -> int:
+    """Synchronize ``stream`` and read-and-clear the device status word."""
+    lib = load_library()
+    return int(lib.w4a16_get_kernel_status(_stream_handle(stream)))
+
+
+def raw():
+    """The loaded ctypes library, for callers that pass raw pointers."""
+    return load_library()
