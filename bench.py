@@ -265,6 +265,26 @@ def run_reference(args, rank, world, pg):
 
 
 # -------------------------------------------------------------------- GPU
+def timed_replays(graph, stream, reps, calls_per_replay):
+    """Microseconds per call of `reps` replays of a graph holding
+    `calls_per_replay` calls, each replay bracketed by events on `stream`
+    (replay() launches on the current stream, so `stream` is made current)."""
+    import torch
+    out = []
+    with torch.cuda.stream(stream):
+        graph.replay()                       # upload + warm
+        stream.synchronize()
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            b.synchronize()
+            out.append(a.elapsed_time(b) * 1e3 / calls_per_replay)
+    return out
+
+
 def run_ours(args, rank, local, world, pg):
     import numpy as np
     import torch
@@ -331,7 +351,8 @@ def run_ours(args, rank, local, world, pg):
     with torch.cuda.graph(graph, stream=stream):
         for _ in range(args.steps):
             one_step()
-    graph.replay()                     # untimed replay (graph upload)
+    with torch.cuda.stream(stream):
+        graph.replay()                 # untimed replay (graph upload)
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local) if rank == 0 else None
@@ -341,9 +362,10 @@ def run_ours(args, rank, local, world, pg):
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    graph.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):          # replay() launches on the current stream
+        ev0.record(stream)
+        graph.replay()
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(pg)
     clock_rec = clocks.stop() if clocks else None
@@ -362,16 +384,7 @@ def run_ours(args, rank, local, world, pg):
                 for i in range(R):
                     w4.gemm_ex(s["xs"][M], *s["copies"][i], group=GROUP, out=s["outs"][M],
                                config=gemm_cfg)
-            g.replay()
-            torch.cuda.synchronize(dev)
-            ts = []
-            for _ in range(args.reps):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                g.replay()
-                b.record(stream)
-                b.synchronize()
-                ts.append(a.elapsed_time(b) * 1e3 / R)
+            ts = timed_replays(g, stream, args.reps, R)
             us = statistics.median(ts)
             K, N = s["K"], s["N"]
             rec = {"us_per_call": round(us, 3),
@@ -381,21 +394,14 @@ def run_ours(args, rank, local, world, pg):
                                           / (us * 1e-6), 4)}
             if s["dq"] is not None:
                 Rq = len(s["dq"])
+                with torch.cuda.stream(stream):       # cuBLAS handle/workspace outside capture
+                    torch.matmul(s["xs"][M], s["dq"][0], out=s["outs"][M])
+                torch.cuda.synchronize(dev)
                 gq = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gq, stream=stream):
                     for i in range(Rq):
                         torch.matmul(s["xs"][M], s["dq"][i], out=s["outs"][M])
-                gq.replay()
-                torch.cuda.synchronize(dev)
-                tq = []
-                for _ in range(args.reps):
-                    a, b = (torch.cuda.Event(enable_timing=True),
-                            torch.cuda.Event(enable_timing=True))
-                    a.record(stream)
-                    gq.replay()
-                    b.record(stream)
-                    b.synchronize()
-                    tq.append(a.elapsed_time(b) * 1e3 / Rq)
+                tq = timed_replays(gq, stream, args.reps, Rq)
                 rec["cublas_fp16_us_per_call"] = round(statistics.median(tq), 3)
                 rec["speedup_vs_cublas"] = round(rec["cublas_fp16_us_per_call"] / us, 3)
             key = "M=%d" % M if len(shapes) == 1 else "K=%d,N=%d,M=%d" % (K, N, M)

@@ -77,6 +77,16 @@ typedef enum w4a16_path {
                                 previous kernel on the stream.  Only valid when
                                 packed/scales/zeros are NOT written by the kernel
                                 immediately before it on the same stream. */
+#define W4A16_FLAG_TEST_TIMEOUT 0x100  /* test aid (TMA decode kernel only): arm the
+                                last pipeline stage without loading it, so its
+                                bounded wait runs out (5 ms); the output is
+                                undefined and w4a16_get_kernel_status reports
+                                W4A16_ERR_TIMEOUT.  Never set in production. */
+
+/* Decode kernel variants (w4a16_config.variant). */
+#define W4A16_DECODE_AUTO 0
+#define W4A16_DECODE_TMA 1        /* weights staged by TMA into a shared-memory ring */
+#define W4A16_DECODE_REGISTERS 2  /* weights streamed by 128-bit loads into registers */
 
 /*
  * Launch configuration of one GEMM call.  Zero in any field means "choose
@@ -85,12 +95,13 @@ typedef enum w4a16_path {
 typedef struct w4a16_config {
     int path;       /* w4a16_path */
     int split_k;    /* decode: CTAs of one cluster that split K (1..8) */
-    int warps_k;    /* decode: warps per CTA that split K */
-    int warps_n;    /* decode: 32-column strips per CTA */
-    int steps;      /* decode: 32-row K steps per warp */
+    int warps_k;    /* decode (registers variant): warps per CTA that split K */
+    int warps_n;    /* decode: 32-column strips per CTA (TMA variant: 2 or 4) */
+    int steps;      /* decode: K per warp in 32-row steps (registers variant) or
+                       K per CTA in 256-row stages (TMA variant) */
     int tile_m;     /* prefill: rows of x per CTA tile (16..256, multiple of 16) */
     int flags;      /* W4A16_FLAG_* */
-    int reserved;
+    int variant;    /* decode: W4A16_DECODE_* */
 } w4a16_config;
 
 /*

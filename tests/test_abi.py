@@ -80,25 +80,37 @@ def test_gemm_rejects_before_touching_the_gpu(lib):
                                    (8, 4096, 14336), (1, 768, 2048), (16, 2048, 768),
                                    (3, 260, 512), (40, 1024, 1024)])
 def test_decode_plan_covers_k(M, N, K):
-    p = w4.plan(M, N, K, 128, path="decode")
-    assert p["path"] == 1
+    p = w4.plan(M, N, K, 128, path="decode", variant="registers")
+    assert p["path"] == 1 and p["variant"] == 2
     assert 1 <= p["split_k"] <= 8
     assert p["warps_k"] * p["steps"] * 4 * p["split_k"] >= K // 8
     assert p["steps"] % 4 == 0
+    if N % 8:
+        with pytest.raises(native.W4A16Error) as e:   # scale rows would not be 16-byte pitched
+            w4.plan(M, N, K, 128, path="decode", variant="tma")
+        assert e.value.status == 2
+        return
+    t = w4.plan(M, N, K, 128, path="decode", variant="tma")
+    assert t["variant"] == 1 and t["warps_n"] in (2, 4) and 1 <= t["split_k"] <= 8
+    assert t["steps"] * 256 * t["split_k"] >= K
 
 
 def test_plan_respects_requests():
-    p = w4.plan(1, 4096, 4096, 128, path="decode", split_k=4, warps_k=4, warps_n=1)
+    p = w4.plan(1, 4096, 4096, 128, path="decode", variant="registers", split_k=4, warps_k=4,
+                warps_n=1)
     assert (p["split_k"], p["warps_k"], p["warps_n"]) == (4, 4, 1)
     assert p["steps"] * 4 * 4 * 4 >= 4096 // 8
     with pytest.raises(native.W4A16Error) as e:
-        w4.plan(1, 4096, 4096, 128, path="decode", split_k=9)
+        w4.plan(1, 4096, 4096, 128, path="decode", variant="registers", split_k=9)
     assert e.value.status == 2
 
 
 def test_auto_path_small_m_is_decode():
     for M in (1, 2, 4, 8, 16):
-        assert w4.plan(M, 4096, 4096)["path"] == 1
+        p = w4.plan(M, 4096, 4096)
+        assert p["path"] == 1 and p["variant"] == 1      # TMA decode kernel
+    assert w4.plan(1, 4092, 4096)["variant"] == 2         # N % 8 != 0: registers variant
+    assert w4.plan(1, 4096, 4096, 512)["variant"] == 2    # group 512: registers variant
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -4,6 +4,8 @@ Bars: packing, scales, zeros and dequantized weights bit-exact; GEMM outputs
 max |out - ref| / max(1, |ref|) <= 5e-3 elementwise; one-hot activations give
 the dequantized row bit-exactly; repeated calls give identical bits.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -40,6 +42,14 @@ def quantize_both(W, group):
     return got, ref
 
 
+@functools.lru_cache(maxsize=6)
+def quantized(K, N, group, seed, outliers=False):
+    """Seeded fp16 weight quantized by both sides (bit-exactness asserted once)."""
+    W = synth.weight(K, N, seed=seed, outliers=outliers)
+    dev_w, ref_w = quantize_both(W, group)
+    return W, dev_w, ref_w
+
+
 def check_gemm(x, dev_w, ref_w, group, config=None, tol=TOL):
     out = w4.gemm_ex(to_dev(x), *dev_w, group=group, config=config)
     torch.cuda.synchronize()
@@ -64,8 +74,7 @@ def check_gemm(x, dev_w, ref_w, group, config=None, tol=TOL):
     (1024, 128, 256, False),
 ])
 def test_quantize_pack_and_dequantize_bit_exact(K, N, group, outliers):
-    W = synth.weight(K, N, seed=K + N + group, outliers=outliers)
-    got, ref = quantize_both(W, group)
+    _, got, ref = quantized(K, N, group, synth.weight_seed(1) + K + N, outliers)
     wdq = w4.dequantize(*got, group=group)
     torch.cuda.synchronize()
     assert np.array_equal(wdq.cpu().numpy().view(np.uint16),
@@ -101,46 +110,51 @@ def test_quantize_prefill_size_sampled_columns():
 
 
 # -------------------------------------------------------------------- GEMM
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("K,N,outliers", [
     (512, 256, False), (4096, 4096, False), (2048, 768, False), (768, 2048, False),
     (4096, 14336, True), (14336, 4096, True),
 ])
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 def test_gemm_decode_configs(K, N, outliers, M):
-    W = synth.weight(K, N, seed=synth.weight_seed(1) + K + N, outliers=outliers)
-    dev_w, ref_w = quantize_both(W, 128)
+    _, dev_w, ref_w = quantized(K, N, 128, synth.weight_seed(1) + K + N, outliers)
     x = synth.activations(M, K, seed=synth.x_seed(1, M) + K)
     check_gemm(x, dev_w, ref_w, 128)
 
 
 @pytest.mark.parametrize("cfg", [
-    dict(path="decode", split_k=1, warps_k=8, warps_n=1),
-    dict(path="decode", split_k=2, warps_k=8, warps_n=1),
-    dict(path="decode", split_k=3, warps_k=4, warps_n=1),
-    dict(path="decode", split_k=8, warps_k=4, warps_n=1),
-    dict(path="decode", split_k=4, warps_k=4, warps_n=2),
-    dict(path="decode", split_k=5, warps_k=2, warps_n=4),
-    dict(path="decode", split_k=2, warps_k=2, warps_n=2),
-    dict(path="decode", split_k=7, warps_k=8, warps_n=1, steps=4),
+    # registers variant: every compiled CTA shape, several cluster sizes
+    dict(path="decode", variant="registers", split_k=1, warps_k=8, warps_n=1),
+    dict(path="decode", variant="registers", split_k=2, warps_k=8, warps_n=1),
+    dict(path="decode", variant="registers", split_k=3, warps_k=4, warps_n=1),
+    dict(path="decode", variant="registers", split_k=8, warps_k=4, warps_n=1),
+    dict(path="decode", variant="registers", split_k=4, warps_k=4, warps_n=2),
+    dict(path="decode", variant="registers", split_k=5, warps_k=2, warps_n=4),
+    dict(path="decode", variant="registers", split_k=2, warps_k=2, warps_n=2),
+    dict(path="decode", variant="registers", split_k=7, warps_k=8, warps_n=1, steps=4),
+    # TMA variant: both tile widths, cluster sizes 1..8, CTAs left without K
+    dict(path="decode", variant="tma", warps_n=4, split_k=1),
+    dict(path="decode", variant="tma", warps_n=4, split_k=3),
+    dict(path="decode", variant="tma", warps_n=2, split_k=2),
+    dict(path="decode", variant="tma", warps_n=2, split_k=8),
+    dict(path="decode", variant="tma", warps_n=4, split_k=2, steps=4),
+    dict(path="decode", variant="tma", warps_n=4, split_k=8, steps=1),
     dict(path="decode", pdl=True),
-])
+], ids=lambda c: "-".join("%s%s" % (k, v) for k, v in c.items()))
 @pytest.mark.parametrize("M", [1, 3, 9, 16])
 def test_gemm_decode_launch_shapes(cfg, M):
     """Every compiled kernel shape, several cluster sizes (including ones that
     leave some CTAs of the cluster without K rows), ragged N."""
     K, N = 1536, 1000
-    W = synth.weight(K, N, seed=21)
-    dev_w, ref_w = quantize_both(W, 128)
+    _, dev_w, ref_w = quantized(K, N, 128, 21)
     x = synth.activations(M, K, seed=22 + M)
     check_gemm(x, dev_w, ref_w, 128, config=cfg)
 
 
-@pytest.mark.parametrize("group", [32, 64, 256])
+@pytest.mark.parametrize("group", [32, 64, 256, 512])
 @pytest.mark.parametrize("M", [1, 12])
 def test_gemm_other_groups(group, M):
     K, N = 1024, 384
-    W = synth.weight(K, N, seed=31 + group, outliers=True)
-    dev_w, ref_w = quantize_both(W, group)
+    _, dev_w, ref_w = quantized(K, N, group, 31 + group, True)
     x = synth.activations(M, K, seed=32)
     check_gemm(x, dev_w, ref_w, group)
 
@@ -148,10 +162,35 @@ def test_gemm_other_groups(group, M):
 @pytest.mark.parametrize("M", [17, 40, 100])
 def test_gemm_larger_m(M):
     K, N = 1024, 512
-    W = synth.weight(K, N, seed=41)
-    dev_w, ref_w = quantize_both(W, 128)
+    _, dev_w, ref_w = quantized(K, N, 128, 41)
     x = synth.activations(M, K, seed=42)
     check_gemm(x, dev_w, ref_w, 128)
+
+
+@pytest.mark.parametrize("N", [260, 1004])
+@pytest.mark.parametrize("M", [1, 16])
+def test_gemm_n_not_multiple_of_8(N, M):
+    """N % 8 != 0 rules out the TMA variant (16-byte row pitch of the scales);
+    the registers variant serves it."""
+    K = 512
+    _, dev_w, ref_w = quantized(K, N, 128, 43)
+    assert w4.plan(M, N, K)["variant"] == 2
+    x = synth.activations(M, K, seed=44)
+    check_gemm(x, dev_w, ref_w, 128)
+
+
+def test_bounded_wait_times_out_and_reports():
+    """A pipeline wait that nothing will satisfy gives up after its limit, the
+    kernel ends, the host reads W4A16_ERR_TIMEOUT, and the context stays usable."""
+    K, N, M = 2048, 1024, 4
+    _, dev_w, ref_w = quantized(K, N, 128, 45)
+    x = synth.activations(M, K, seed=46)
+    assert w4.kernel_status() == 0
+    w4.gemm_ex(to_dev(x), *dev_w, group=128,
+               config=dict(path="decode", variant="tma", flags=w4.native.FLAG_TEST_TIMEOUT))
+    assert w4.kernel_status() == 5          # W4A16_ERR_TIMEOUT, then cleared
+    assert w4.kernel_status() == 0
+    check_gemm(x, dev_w, ref_w, 128)       # the next call is correct
 
 
 def test_gemm_random_encodings():

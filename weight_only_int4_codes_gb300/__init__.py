@@ -13,12 +13,13 @@ can be used without the native library.
 """
 _NATIVE_NAMES = {
     "W4A16Error", "gemm", "gemm_ex", "dequantize", "quantize_pack", "kernel_status",
-    "library_path", "load_library", "plan",
+    "library_path", "load_library", "plan", "native",
 }
 
 
 def __getattr__(name):
     if name in _NATIVE_NAMES:
-        from . import native
-        return getattr(native, name)
+        import importlib
+        native = importlib.import_module(__name__ + ".native")
+        return native if name == "native" else getattr(native, name)
     raise AttributeError(name)

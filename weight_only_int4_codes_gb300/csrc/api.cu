@@ -129,6 +129,39 @@ void plan_decode(int M, int N, int K, int group, int sm_count, w4a16_config &c) 
     }
 }
 
+// Decode path, TMA variant: a CTA covers 32*warps_n columns and `steps`
+// 256-row stages of K; split_k CTAs of a cluster cover K.  The choice
+// minimizes the stages streamed by the busiest SM, then the cluster size.
+void plan_decode_tma(int M, int N, int K, int sm_count, w4a16_config &c) {
+    (void)M;
+    if (c.warps_n <= 0) c.warps_n = 4;
+    const int BN = 32 * c.warps_n;
+    const int tiles = (N + BN - 1) / BN;
+    const int total = (K / 8 + 31) / 32;    // 256-row stages
+    if (c.split_k <= 0 && c.steps <= 0) {
+        long long best_cost = -1;
+        for (int s = 1; s <= 8; ++s) {
+            const int st = (total + s - 1) / s;
+            const int s_eff = (total + st - 1) / st;
+            const long long ctas = (long long)tiles * s_eff;
+            const long long cost = (ctas + sm_count - 1) / sm_count * st;
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                c.split_k = s_eff;
+                c.steps = st;
+            }
+        }
+    } else if (c.steps <= 0) {
+        c.steps = (total + c.split_k - 1) / c.split_k;
+    } else if (c.split_k <= 0) {
+        c.split_k = (total + c.steps - 1) / c.steps;
+    }
+}
+
+bool tma_variant_possible(int N, int group) {
+    return (group == 32 || group == 64 || group == 128 || group == 256) && N % 8 == 0;
+}
+
 // Crossover between the decode path and the tcgen05 prefill path, in rows of x
 // (measured on GB300; see the dispatch notes in the design document).
 constexpr int kDecodeMaxM = 16;
@@ -147,13 +180,27 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
         }
     }
     if (c.path == W4A16_PATH_DECODE) {
-        plan_decode(M, N, K, group, device_info().sm_count, c);
-        if (!decode_config_supported(c, M) || c.steps % decode_steps_per_batch(group) != 0 ||
-            (long long)c.warps_k * c.steps * 4 * c.split_k < K / 8)
-            return fail(W4A16_ERR_UNSUPPORTED,
-                        "decode configuration not available (split_k=%d warps_k=%d warps_n=%d "
-                        "steps=%d)",
-                        c.split_k, c.warps_k, c.warps_n, c.steps);
+        if (c.variant == W4A16_DECODE_AUTO)
+            c.variant = tma_variant_possible(N, group) ? W4A16_DECODE_TMA : W4A16_DECODE_REGISTERS;
+        if (c.variant == W4A16_DECODE_TMA) {
+            plan_decode_tma(M, N, K, device_info().sm_count, c);
+            if (!tma_variant_possible(N, group) || !decode_tma_supported(c, group) ||
+                (long long)c.steps * 256 * c.split_k < K)
+                return fail(W4A16_ERR_UNSUPPORTED,
+                            "TMA decode configuration not available (split_k=%d warps_n=%d "
+                            "steps=%d, group=%d, N=%d)",
+                            c.split_k, c.warps_n, c.steps, group, N);
+        } else if (c.variant == W4A16_DECODE_REGISTERS) {
+            plan_decode(M, N, K, group, device_info().sm_count, c);
+            if (!decode_config_supported(c, M) || c.steps % decode_steps_per_batch(group) != 0 ||
+                (long long)c.warps_k * c.steps * 4 * c.split_k < K / 8)
+                return fail(W4A16_ERR_UNSUPPORTED,
+                            "decode configuration not available (split_k=%d warps_k=%d "
+                            "warps_n=%d steps=%d)",
+                            c.split_k, c.warps_k, c.warps_n, c.steps);
+        } else {
+            return fail(W4A16_ERR_INVALID_ARG, "unknown decode variant %d", c.variant);
+        }
     } else if (c.path == W4A16_PATH_PREFILL) {
         if (c.tile_m <= 0) c.tile_m = M >= 256 ? 256 : ((M + 15) / 16) * 16;
         if (!prefill_config_supported(c, M, N, K, group))
@@ -234,8 +281,12 @@ w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed, const uint
     st = make_plan(M, N, K, group, cfg, c);
     if (st != W4A16_OK) return st;
     GemmArgs a{x, packed, scales, zeros, out, M, N, K, group};
-    cudaError_t e = c.path == W4A16_PATH_DECODE ? launch_decode(a, c, stream)
-                                                : launch_prefill(a, c, stream);
+    cudaError_t e;
+    if (c.path == W4A16_PATH_DECODE)
+        e = c.variant == W4A16_DECODE_TMA ? launch_decode_tma(a, c, stream)
+                                          : launch_decode(a, c, stream);
+    else
+        e = launch_prefill(a, c, stream);
     if (e == cudaErrorNotSupported)
         return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "gemm launch");

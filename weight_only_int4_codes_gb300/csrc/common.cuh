@@ -45,6 +45,9 @@ int decode_steps_per_batch(int group);
 // Resident CTAs per SM of the decode kernel that `cfg` selects (occupancy
 // query on the current device; a fixed estimate when no GPU is present).
 int decode_ctas_per_sm(const w4a16_config &cfg, int M, int group);
+// Decode path, TMA variant (decode_tma.cu).
+bool decode_tma_supported(const w4a16_config &cfg, int group);
+cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 // Prefill path (tcgen05).  Returns cudaErrorNotSupported if unavailable.
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group);

@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_math.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -85,20 +86,6 @@ __device__ __forceinline__ uint2 ld_nc_v2(const void *ptr) {
     return r;
 }
 
-// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-constexpr uint32_t kMaskLo = 0x000F000Fu;   // nibbles 0 and 4 of a word
-constexpr uint32_t kMaskHi = 0x00F000F0u;   // nibbles 1 and 5
-constexpr uint32_t kMagicLo = 0x64006400u;  // 1024.0 | 1024.0 (ulp 1 at bits 0..3)
-constexpr uint32_t kMagicHi = 0x54005400u;  // 64.0 | 64.0 (ulp 1 at bits 4..7)
-
 // One K-batch of U steps: the words of 4 columns x U steps, plus that batch's
 // group scale and zero (a batch never straddles a group).
 template <int U>
@@ -107,43 +94,33 @@ struct Batch {
     uint2 s, z;
 };
 
+// Threads whose columns lie past N (ragged last tile) load nothing and feed
+// zeros: the batch loop itself must stay warp-uniform because mma.sync is a
+// warp-collective (.aligned) instruction.
 template <int U>
-__device__ __forceinline__ void load_batch(Batch<U> &b, const uint32_t *wptr, size_t wstride,
-                                           const uint16_t *sz_s, const uint16_t *sz_z,
-                                           uint64_t pol) {
+__device__ __forceinline__ void load_batch(Batch<U> &b, bool col_ok, const uint32_t *wptr,
+                                           size_t wstride, const uint16_t *sz_s,
+                                           const uint16_t *sz_z, uint64_t pol) {
+    if (col_ok) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) b.w[u] = ld_weights(wptr + u * wstride, pol);
-    b.s = ld_nc_v2(sz_s);
-    b.z = ld_nc_v2(sz_z);
+        for (int u = 0; u < U; ++u) b.w[u] = ld_weights(wptr + u * wstride, pol);
+        b.s = ld_nc_v2(sz_s);
+        b.z = ld_nc_v2(sz_z);
+    } else {
+#pragma unroll
+        for (int u = 0; u < U; ++u) b.w[u] = make_uint4(0, 0, 0, 0);
+        b.s = make_uint2(0, 0);
+        b.z = make_uint2(0, 0);
+    }
 }
 
-// Per-thread state and the MMA work of one batch.
-//   thread (g = lane/4, t = lane%4) owns columns col0..col0+3 (col0 = 4g + ...)
-//   and, in step u, packed row  row = row0 + 4*(batch*U + u) + t.
-//   MMA tile j (j = 0, 1) has rows {g -> column col0+2j, g+8 -> column col0+2j+1}.
-//   K slots of the MMA map onto the word's nibbles as
-//       kk = 0: slots (2t, 2t+1, 2t+8, 2t+9) <- nibbles (0, 4, 1, 5)
-//       kk = 1: slots (2t, 2t+1, 2t+8, 2t+9) <- nibbles (2, 6, 3, 7)
-//   so the B (x) fragment needs x[k0+0], x[k0+4] | x[k0+1], x[k0+5] for kk=0.
+// The MMA work of one batch (see decode_math.cuh for the fragment mapping):
+// thread (g, t) handles, in step u, packed row  row = krow_first + 4u + t.
 template <int NT, int U>
 __device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batch<U> &b,
                                               const uint16_t *xrow0, const uint16_t *xrow1,
                                               bool m0_ok, bool m1_ok, int krow_first,
                                               int t) {
-    // zero biases (1024+z, 64+z) broadcast per column, fp32 scales per column
-    const uint32_t zlo01 = hadd2_u32(b.z.x, kMagicLo);   // (1024+z0, 1024+z1)
-    const uint32_t zlo23 = hadd2_u32(b.z.y, kMagicLo);
-    const uint32_t zhi01 = hadd2_u32(b.z.x, kMagicHi);   // (64+z0, 64+z1)
-    const uint32_t zhi23 = hadd2_u32(b.z.y, kMagicHi);
-    const uint32_t zA[4] = {__byte_perm(zlo01, 0, 0x1010), __byte_perm(zlo01, 0, 0x3232),
-                            __byte_perm(zlo23, 0, 0x1010), __byte_perm(zlo23, 0, 0x3232)};
-    const uint32_t zB[4] = {__byte_perm(zhi01, 0, 0x1010), __byte_perm(zhi01, 0, 0x3232),
-                            __byte_perm(zhi23, 0, 0x1010), __byte_perm(zhi23, 0, 0x3232)};
-    const __half2 s01 = *reinterpret_cast<const __half2 *>(&b.s.x);
-    const __half2 s23 = *reinterpret_cast<const __half2 *>(&b.s.y);
-    const float sc[4] = {__low2float(s01), __high2float(s01), __low2float(s23),
-                         __high2float(s23)};
-
     // x fragments of all U steps first (several loads in flight)
     uint4 xr[NT][U];
 #pragma unroll
@@ -152,7 +129,7 @@ __device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batc
         xr[0][u] = m0_ok ? ld_nc_v4(xrow0 + koff) : make_uint4(0, 0, 0, 0);
         if (NT > 1) xr[NT - 1][u] = m1_ok ? ld_nc_v4(xrow1 + koff) : make_uint4(0, 0, 0, 0);
     }
-
+    const GroupConsts k = make_group_consts(b.z, b.s);
     float gacc[NT][2][4];
 #pragma unroll
     for (int p = 0; p < NT; ++p)
@@ -160,56 +137,14 @@ __device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batc
         for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int r = 0; r < 4; ++r) gacc[p][j][r] = 0.f;
-
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         uint32_t bx[NT][4];
 #pragma unroll
-        for (int p = 0; p < NT; ++p) {
-            const uint4 v = xr[p][u];            // (x0x1, x2x3, x4x5, x6x7)
-            bx[p][0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
-            bx[p][1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
-            bx[p][2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
-            bx[p][3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
-        }
-        const uint32_t wv[4] = {b.w[u].x, b.w[u].y, b.w[u].z, b.w[u].w};
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const uint32_t c0 = wv[2 * j], c1 = wv[2 * j + 1];
-            // kk = 0: nibbles (0,4) and (1,5)
-            {
-                const uint32_t a0 = hsub2_u32(lop3_and_or(c0, kMaskLo, kMagicLo), zA[2 * j]);
-                const uint32_t a1 = hsub2_u32(lop3_and_or(c1, kMaskLo, kMagicLo), zA[2 * j + 1]);
-                const uint32_t a2 = hsub2_u32(lop3_and_or(c0, kMaskHi, kMagicHi), zB[2 * j]);
-                const uint32_t a3 = hsub2_u32(lop3_and_or(c1, kMaskHi, kMagicHi), zB[2 * j + 1]);
-#pragma unroll
-                for (int p = 0; p < NT; ++p)
-                    mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][0], bx[p][1]);
-            }
-            // kk = 1: nibbles (2,6) and (3,7)
-            {
-                const uint32_t d0 = c0 >> 8, d1 = c1 >> 8;
-                const uint32_t a0 = hsub2_u32(lop3_and_or(d0, kMaskLo, kMagicLo), zA[2 * j]);
-                const uint32_t a1 = hsub2_u32(lop3_and_or(d1, kMaskLo, kMagicLo), zA[2 * j + 1]);
-                const uint32_t a2 = hsub2_u32(lop3_and_or(d0, kMaskHi, kMagicHi), zB[2 * j]);
-                const uint32_t a3 = hsub2_u32(lop3_and_or(d1, kMaskHi, kMagicHi), zB[2 * j + 1]);
-#pragma unroll
-                for (int p = 0; p < NT; ++p)
-                    mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][2], bx[p][3]);
-            }
-        }
+        for (int p = 0; p < NT; ++p) x_fragments(xr[p][u], bx[p]);
+        step_mma<NT>(gacc, b.w[u], k, bx);
     }
-    // apply the group scale in fp32: rows g (c0, c1) -> column col0+2j,
-    // rows g+8 (c2, c3) -> column col0+2j+1
-#pragma unroll
-    for (int p = 0; p < NT; ++p)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            acc[p][j][0] = fmaf(sc[2 * j], gacc[p][j][0], acc[p][j][0]);
-            acc[p][j][1] = fmaf(sc[2 * j], gacc[p][j][1], acc[p][j][1]);
-            acc[p][j][2] = fmaf(sc[2 * j + 1], gacc[p][j][2], acc[p][j][2]);
-            acc[p][j][3] = fmaf(sc[2 * j + 1], gacc[p][j][3], acc[p][j][3]);
-        }
+    flush_group<NT>(acc, gacc, k);
 }
 
 // Grid: (ceil(N / (32*WN)), split, ceil(M / 16)); cluster (1, split, 1).
@@ -229,7 +164,8 @@ decode_kernel(const DecodeArgs a)
     const bool col_ok = col0 < a.N;                 // N % 4 == 0: all 4 columns valid
     const int KB = a.K >> 3;                        // packed rows
     const int row0 = blockIdx.y * a.rows_per_cta + wk * a.steps * 4;
-    const int nsteps = col_ok ? max(0, min(a.steps, (KB - row0) >> 2)) : 0;
+    // warp-uniform trip count (independent of col_ok)
+    const int nsteps = max(0, min(a.steps, (KB - row0) >> 2));
     const int nbatch = nsteps / U;                  // nsteps is a multiple of U
 
     const uint64_t pol = evict_first_policy();
@@ -256,7 +192,7 @@ decode_kernel(const DecodeArgs a)
     Batch<U> ba, bb;
     if (nbatch > 0) {
         const size_t grow = (size_t)(row0 / rows_per_group) * a.N;
-        load_batch<U>(ba, wptr, wstride, sptr + grow, zptr + grow, pol);
+        load_batch<U>(ba, col_ok, wptr, wstride, sptr + grow, zptr + grow, pol);
     }
     // Everything above only touches the weights.  x and out may belong to the
     // previous kernel on the stream (programmatic dependent launch).
@@ -267,16 +203,16 @@ decode_kernel(const DecodeArgs a)
         if (bi + 1 < nbatch) {
             const int r = row0 + 4 * U * (bi + 1);
             const size_t grow = (size_t)(r / rows_per_group) * a.N;
-            load_batch<U>(bb, wptr + (size_t)(bi + 1) * U * wstride, wstride, sptr + grow,
-                          zptr + grow, pol);
+            load_batch<U>(bb, col_ok, wptr + (size_t)(bi + 1) * U * wstride, wstride,
+                          sptr + grow, zptr + grow, pol);
         }
         compute_batch<NT, U>(acc, ba, xrow0, xrow1, m0_ok, m1_ok, row0 + 4 * U * bi, t);
         if (bi + 1 < nbatch) {
             if (bi + 2 < nbatch) {
                 const int r = row0 + 4 * U * (bi + 2);
                 const size_t grow = (size_t)(r / rows_per_group) * a.N;
-                load_batch<U>(ba, wptr + (size_t)(bi + 2) * U * wstride, wstride, sptr + grow,
-                              zptr + grow, pol);
+                load_batch<U>(ba, col_ok, wptr + (size_t)(bi + 2) * U * wstride, wstride,
+                              sptr + grow, zptr + grow, pol);
             }
             compute_batch<NT, U>(acc, bb, xrow0, xrow1, m0_ok, m1_ok,
                                  row0 + 4 * U * (bi + 1), t);

@@ -1,0 +1,122 @@
+// decode_math.cuh -- the per-step arithmetic shared by the decode kernels:
+// nibble unpack with the magic-exponent trick, exact (q - z) in fp16, and the
+// register-fed tensor-core MMA with swapped roles.
+//
+// Fragment mapping (mma.m16n8k16, A row-major 16x16, B col 16x8, fp32 C):
+//   thread (g = lane/4, t = lane%4) holds one 128-bit load: the packed words of
+//   four neighbouring columns c0..c0+3 for one packed row (8 consecutive k).
+//   MMA tile j (j = 0, 1): A row g <- column c0+2j, A row g+8 <- column c0+2j+1.
+//   K slots (2t, 2t+1, 2t+8, 2t+9) take nibbles (0, 4, 1, 5) for kk = 0 and
+//   (2, 6, 3, 7) for kk = 1 of the thread's word, so every A register is one
+//   LOP3 + one HSUB2 away from the word, and the thread's x fragment is
+//   x[m][k0 + {0,4 | 1,5}] (kk = 0) and x[m][k0 + {2,6 | 3,7}] (kk = 1): a
+//   16-byte load of x[m][k0 .. k0+7] and four byte permutes.  K may be permuted
+//   inside a reduction as long as x and W use the same permutation.
+//   Accumulator: c0, c1 -> (column c0+2j, batch rows 2t, 2t+1); c2, c3 ->
+//   (column c0+2j+1, batch rows 2t, 2t+1).
+#pragma once
+
+#include "common.cuh"
+
+namespace w4a16 {
+
+constexpr uint32_t kMaskLo = 0x000F000Fu;   // nibbles 0 and 4 of a word
+constexpr uint32_t kMaskHi = 0x00F000F0u;   // nibbles 1 and 5
+constexpr uint32_t kMagicLo = 0x64006400u;  // 1024.0 | 1024.0: mantissa ulp 1 at bits 0..3
+constexpr uint32_t kMagicHi = 0x54005400u;  // 64.0 | 64.0: mantissa ulp 1 at bits 4..7
+
+// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Per-group constants of the thread's four columns: the zero biases
+// (1024+z, 64+z) broadcast into both halves, and the fp32 scales.
+struct GroupConsts {
+    uint32_t zA[4], zB[4];
+    float sc[4];
+};
+
+// zraw / sraw: the fp16 zeros / scales of columns c0..c0+3 (two per word).
+__device__ __forceinline__ GroupConsts make_group_consts(uint2 zraw, uint2 sraw) {
+    GroupConsts k;
+    const uint32_t zlo01 = hadd2_u32(zraw.x, kMagicLo);   // (1024+z0, 1024+z1), exact
+    const uint32_t zlo23 = hadd2_u32(zraw.y, kMagicLo);
+    const uint32_t zhi01 = hadd2_u32(zraw.x, kMagicHi);   // (64+z0, 64+z1), exact
+    const uint32_t zhi23 = hadd2_u32(zraw.y, kMagicHi);
+    k.zA[0] = __byte_perm(zlo01, 0, 0x1010);
+    k.zA[1] = __byte_perm(zlo01, 0, 0x3232);
+    k.zA[2] = __byte_perm(zlo23, 0, 0x1010);
+    k.zA[3] = __byte_perm(zlo23, 0, 0x3232);
+    k.zB[0] = __byte_perm(zhi01, 0, 0x1010);
+    k.zB[1] = __byte_perm(zhi01, 0, 0x3232);
+    k.zB[2] = __byte_perm(zhi23, 0, 0x1010);
+    k.zB[3] = __byte_perm(zhi23, 0, 0x3232);
+    const __half2 s01 = *reinterpret_cast<const __half2 *>(&sraw.x);
+    const __half2 s23 = *reinterpret_cast<const __half2 *>(&sraw.y);
+    k.sc[0] = __low2float(s01);
+    k.sc[1] = __high2float(s01);
+    k.sc[2] = __low2float(s23);
+    k.sc[3] = __high2float(s23);
+    return k;
+}
+
+// x[m][k0..k0+7] (natural order, 4 words) -> the two B fragments of kk = 0, 1.
+__device__ __forceinline__ void x_fragments(uint4 v, uint32_t (&b)[4]) {
+    b[0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
+    b[1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
+    b[2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
+    b[3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
+}
+
+// One 32-k step of one thread: 4 words (columns c0..c0+3) x 8 k, MMAs into the
+// group accumulator gacc[p][j] (p = batch tile of 8 rows, j = column pair).
+template <int NT>
+__device__ __forceinline__ void step_mma(float (&gacc)[NT][2][4], uint4 w, const GroupConsts &k,
+                                         const uint32_t (&bx)[NT][4]) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t c0 = wv[2 * j], c1 = wv[2 * j + 1];
+        {   // kk = 0: nibbles (0,4) | (1,5)
+            const uint32_t a0 = hsub2_u32(lop3_and_or(c0, kMaskLo, kMagicLo), k.zA[2 * j]);
+            const uint32_t a1 = hsub2_u32(lop3_and_or(c1, kMaskLo, kMagicLo), k.zA[2 * j + 1]);
+            const uint32_t a2 = hsub2_u32(lop3_and_or(c0, kMaskHi, kMagicHi), k.zB[2 * j]);
+            const uint32_t a3 = hsub2_u32(lop3_and_or(c1, kMaskHi, kMagicHi), k.zB[2 * j + 1]);
+#pragma unroll
+            for (int p = 0; p < NT; ++p) mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][0], bx[p][1]);
+        }
+        {   // kk = 1: nibbles (2,6) | (3,7)
+            const uint32_t d0 = c0 >> 8, d1 = c1 >> 8;
+            const uint32_t a0 = hsub2_u32(lop3_and_or(d0, kMaskLo, kMagicLo), k.zA[2 * j]);
+            const uint32_t a1 = hsub2_u32(lop3_and_or(d1, kMaskLo, kMagicLo), k.zA[2 * j + 1]);
+            const uint32_t a2 = hsub2_u32(lop3_and_or(d0, kMaskHi, kMagicHi), k.zB[2 * j]);
+            const uint32_t a3 = hsub2_u32(lop3_and_or(d1, kMaskHi, kMagicHi), k.zB[2 * j + 1]);
+#pragma unroll
+            for (int p = 0; p < NT; ++p) mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][2], bx[p][3]);
+        }
+    }
+}
+
+// acc += s * gacc (the group scale, applied once per group in fp32), then gacc = 0.
+template <int NT>
+__device__ __forceinline__ void flush_group(float (&acc)[NT][2][4], float (&gacc)[NT][2][4],
+                                            const GroupConsts &k) {
+#pragma unroll
+    for (int p = 0; p < NT; ++p)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            acc[p][j][0] = fmaf(k.sc[2 * j], gacc[p][j][0], acc[p][j][0]);
+            acc[p][j][1] = fmaf(k.sc[2 * j], gacc[p][j][1], acc[p][j][1]);
+            acc[p][j][2] = fmaf(k.sc[2 * j + 1], gacc[p][j][2], acc[p][j][2]);
+            acc[p][j][3] = fmaf(k.sc[2 * j + 1], gacc[p][j][3], acc[p][j][3]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) gacc[p][j][r] = 0.f;
+        }
+}
+
+}  // namespace w4a16

@@ -1,0 +1,18 @@
+// tmap.cuh -- host helper: 2-D TMA tensor maps (see tmap.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+// A row-major 2-D tensor of `outer` rows x `inner` elements (row pitch
+// `row_stride_bytes`, a multiple of 16), loaded in boxes of
+// box_outer x box_inner elements.  Out-of-bounds box elements read as zero.
+// Returns false if the driver rejects the description.
+bool make_tmap_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+}  // namespace w4a16

@@ -22,7 +22,9 @@ _LIB_NAME = "libw4a16.so"
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA",
                 5: "TIMEOUT"}
 PATHS = {"auto": 0, "decode": 1, "prefill": 2}
+VARIANTS = {"auto": 0, "tma": 1, "registers": 2}
 FLAG_PDL = 0x1
+FLAG_TEST_TIMEOUT = 0x100
 
 
 class W4A16Error(RuntimeError):
@@ -34,7 +36,7 @@ class W4A16Error(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("warps_k", ctypes.c_int),
                 ("warps_n", ctypes.c_int), ("steps", ctypes.c_int), ("tile_m", ctypes.c_int),
-                ("flags", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("flags", ctypes.c_int), ("variant", ctypes.c_int)]
 
     @classmethod
     def make(cls, cfg):
@@ -46,6 +48,8 @@ class Config(ctypes.Structure):
         for k, v in dict(cfg).items():
             if k == "path" and isinstance(v, str):
                 v = PATHS[v]
+            if k == "variant" and isinstance(v, str):
+                v = VARIANTS[v]
             if k == "pdl":
                 c.flags |= FLAG_PDL if v else 0
                 continue
@@ -53,7 +57,7 @@ class Config(ctypes.Structure):
         return c
 
     def as_dict(self):
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 _lock = threading.Lock()
