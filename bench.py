@@ -300,6 +300,8 @@ def run_ours(args, rank, local, world, pg):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     stream = torch.cuda.Stream(device=dev)
     gemm_cfg = dict(pdl=not args.no_pdl)
+    if args.variant != "auto":
+        gemm_cfg.update(path="decode", variant=args.variant)
 
     # weights: quantize once per shape on the GPU (offline step), then R
     # byte-identical copies at distinct addresses per shape so that the
@@ -466,7 +468,8 @@ def run_ours(args, rank, local, world, pg):
                        "l2": "inputs larger than L2: every call reads a distinct weight copy "
                              "(rotation footprint >= 3x L2)",
                        "timing": "one CUDA-graph replay of exactly `steps` steps, CUDA events",
-                       "pdl": not args.no_pdl, "parallelism": "replicas" if world > 1 else "1gpu"},
+                       "pdl": not args.no_pdl, "variant": args.variant,
+                       "parallelism": "replicas" if world > 1 else "1gpu"},
             "us_per_call": per_m,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -489,6 +492,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_square")
     ap.add_argument("--reps", type=int, default=20, help="repeats of the per-M timing graphs")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--variant", choices=["auto", "tma", "registers"], default="auto",
+                    help="decode kernel variant (auto = the library's dispatch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cublas", action=argparse.BooleanOptionalAction, default=True)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

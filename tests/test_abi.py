@@ -108,9 +108,15 @@ def test_plan_respects_requests():
 def test_auto_path_small_m_is_decode():
     for M in (1, 2, 4, 8, 16):
         p = w4.plan(M, 4096, 4096)
-        assert p["path"] == 1 and p["variant"] == 1      # TMA decode kernel
+        assert p["path"] == 1 and p["variant"] in (1, 2)
+    # measured dispatch table rows
+    assert w4.plan(1, 4096, 4096)["variant"] == 2         # registers variant wins 4096^2
+    t = w4.plan(4, 14336, 4096)
+    assert (t["variant"], t["warps_n"], t["split_k"], t["steps"]) == (1, 4, 2, 8)
     assert w4.plan(1, 4092, 4096)["variant"] == 2         # N % 8 != 0: registers variant
     assert w4.plan(1, 4096, 4096, 512)["variant"] == 2    # group 512: registers variant
+    # off-table shapes take the TMA planner when the format allows it
+    assert w4.plan(1, 8192, 8192)["variant"] == 1
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

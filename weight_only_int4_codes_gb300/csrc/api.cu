@@ -132,19 +132,24 @@ void plan_decode(int M, int N, int K, int group, int sm_count, w4a16_config &c) 
 // Decode path, TMA variant: a CTA covers 32*warps_n columns and `steps`
 // 256-row stages of K; split_k CTAs of a cluster cover K.  The choice
 // minimizes the stages streamed by the busiest SM, then the cluster size.
-void plan_decode_tma(int M, int N, int K, int sm_count, w4a16_config &c) {
-    (void)M;
+void plan_decode_tma(int M, int N, int K, int group, int sm_count, w4a16_config &c) {
     if (c.warps_n <= 0) c.warps_n = 4;
     const int BN = 32 * c.warps_n;
     const int tiles = (N + BN - 1) / BN;
     const int total = (K / 8 + 31) / 32;    // 256-row stages
     if (c.split_k <= 0 && c.steps <= 0) {
+        // prefer configurations that leave room for a second CTA per SM
+        // (about half of the shared memory), then the smallest busiest-SM load
         long long best_cost = -1;
         for (int s = 1; s <= 8; ++s) {
             const int st = (total + s - 1) / s;
             const int s_eff = (total + st - 1) / st;
+            w4a16_config t = c;
+            t.split_k = s_eff;
+            t.steps = st;
+            const bool fits_half = decode_tma_smem_bytes(t, M, group) <= 113 * 1024;
             const long long ctas = (long long)tiles * s_eff;
-            const long long cost = (ctas + sm_count - 1) / sm_count * st;
+            const long long cost = ((ctas + sm_count - 1) / sm_count * st) * 2 + (fits_half ? 0 : 1);
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 c.split_k = s_eff;
@@ -156,6 +161,41 @@ void plan_decode_tma(int M, int N, int K, int sm_count, w4a16_config &c) {
     } else if (c.split_k <= 0) {
         c.split_k = (total + c.steps - 1) / c.steps;
     }
+}
+
+// Measured dispatch table (GB300, group 128, one call per distinct weight copy
+// in a CUDA graph with programmatic dependent launch): the fastest decode
+// configuration for the projection shapes of the benchmark workloads.
+struct TableEntry {
+    int K, N, m_max;        // shape and the largest M the row covers
+    w4a16_config cfg;
+};
+constexpr TableEntry kDecodeTable[] = {
+    // K      N      M<=   path split warps_k warps_n steps tile flags variant
+    {4096, 4096, 16, {1, 2, 8, 1, 8, 0, 0, W4A16_DECODE_REGISTERS}},
+    {4096, 14336, 8, {1, 2, 8, 4, 8, 0, 0, W4A16_DECODE_TMA}},
+    {4096, 14336, 16, {1, 1, 4, 1, 32, 0, 0, W4A16_DECODE_REGISTERS}},
+    {14336, 4096, 8, {1, 8, 8, 4, 7, 0, 0, W4A16_DECODE_TMA}},
+    {14336, 4096, 16, {1, 4, 8, 2, 14, 0, 0, W4A16_DECODE_TMA}},
+    {2048, 768, 4, {1, 8, 8, 2, 1, 0, 0, W4A16_DECODE_TMA}},
+    {2048, 768, 8, {1, 2, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+    {2048, 768, 16, {1, 4, 4, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+    {768, 2048, 16, {1, 1, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+};
+
+// Fill an all-automatic decode request from the table; false if no row fits.
+bool decode_from_table(int M, int N, int K, int group, w4a16_config &c) {
+    if (group != 128 || c.variant != W4A16_DECODE_AUTO || c.split_k || c.warps_k || c.warps_n ||
+        c.steps)
+        return false;
+    for (const TableEntry &e : kDecodeTable)
+        if (e.K == K && e.N == N && M <= e.m_max) {
+            const int flags = c.flags;
+            c = e.cfg;
+            c.flags = flags;
+            return true;
+        }
+    return false;
 }
 
 bool tma_variant_possible(int N, int group) {
@@ -180,10 +220,11 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
         }
     }
     if (c.path == W4A16_PATH_DECODE) {
+        if (M <= 16) decode_from_table(M, N, K, group, c);
         if (c.variant == W4A16_DECODE_AUTO)
             c.variant = tma_variant_possible(N, group) ? W4A16_DECODE_TMA : W4A16_DECODE_REGISTERS;
         if (c.variant == W4A16_DECODE_TMA) {
-            plan_decode_tma(M, N, K, device_info().sm_count, c);
+            plan_decode_tma(M, N, K, group, device_info().sm_count, c);
             if (!tma_variant_possible(N, group) || !decode_tma_supported(c, group) ||
                 (long long)c.steps * 256 * c.split_k < K)
                 return fail(W4A16_ERR_UNSUPPORTED,

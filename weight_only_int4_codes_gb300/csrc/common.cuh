@@ -47,6 +47,7 @@ int decode_steps_per_batch(int group);
 int decode_ctas_per_sm(const w4a16_config &cfg, int M, int group);
 // Decode path, TMA variant (decode_tma.cu).
 bool decode_tma_supported(const w4a16_config &cfg, int group);
+int decode_tma_smem_bytes(const w4a16_config &cfg, int M, int group);
 cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 // Prefill path (tcgen05).  Returns cudaErrorNotSupported if unavailable.
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);

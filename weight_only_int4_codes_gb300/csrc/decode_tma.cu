@@ -23,7 +23,6 @@
 //   * every mbarrier wait is bounded in wall time; a wait that gives up records
 //     W4A16_ERR_TIMEOUT in the device status word and the kernel runs to its
 //     end without touching memory it does not own.
-#include <cooperative_groups.h>
 #include <mutex>
 
 #include "common.cuh"
@@ -31,16 +30,29 @@
 #include "sm100_ptx.cuh"
 #include "tmap.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace w4a16 {
+
+#ifdef W4A16_TRACE
+// Optional timeline instrumentation (compiled only with -DW4A16_TRACE):
+// per CTA, clock64 offsets of: [0] entry (globaltimer), [1] smid, [2] barriers
+// ready, [3] producer done issuing, [4..11] consumer warp 0 got stage s,
+// [12] main loop done, [13] epilogue done.
+__device__ unsigned long long g_trace[4096][16];
+#define W4A16_TRACE_AT(slot, v)                                                         \
+    do {                                                                                 \
+        const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z); \
+        if (cta_ < 4096) g_trace[cta_][slot] = (v);                                     \
+    } while (0)
+#else
+#define W4A16_TRACE_AT(slot, v) do { } while (0)
+#endif
+
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kStageRows = 32;                 // packed rows per stage
 constexpr int kStageK = 8 * kStageRows;        // 256 k per stage
-constexpr int kRingBudget = 100 * 1024;        // bytes of ring per CTA (<= half an SM)
+constexpr int kSmemBudget = 108 * 1024;        // ring + slots per CTA (about half an SM)
+constexpr int kSmemMax = 220 * 1024;           // opt-in limit set on the kernels
 
 struct TmaDecodeArgs {
     uint16_t *out;
@@ -52,6 +64,7 @@ struct TmaDecodeArgs {
     int stage_bytes;          // bytes per ring slot (multiple of 1024)
     int s_off, z_off, x_off;  // tile offsets inside a slot
     int tx_bytes;             // bytes the TMA loads of one stage deliver
+    int slots_off;            // cluster reduction slots [split][Mc][BN] (leader only)
     unsigned long long timeout_ns;
     int test_skip_last;       // test hook: arm but never load the CTA's last stage
 };
@@ -59,22 +72,38 @@ struct TmaDecodeArgs {
 // consumer lane group g reads 16-byte chunk perm8(g) of its 128-byte row
 __device__ __forceinline__ int perm8(int g) { return (g >> 1) + ((g & 1) << 2); }
 
-template <int NT, int BNS>
-__global__ void __launch_bounds__(kThreads, 2)
+// ONE_GROUP: a warp's share of a stage (8*BNS*... k rows) lies inside one
+// quantization group (group >= 32 * steps per warp), so the group constants
+// are formed once per stage and the step loop has no branches.
+template <int NT, int BNS, int CW, bool ONE_GROUP>
+__global__ void __launch_bounds__(32 * (CW + 1), CW == 8 ? 2 : 1)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_x,
                   const TmaDecodeArgs a)
 {
+    constexpr int kConsumerWarps = CW;
+    constexpr int kThreads = 32 * (CW + 1);
     constexpr int BN = 32 * BNS;                 // columns per CTA
     constexpr int WK = kConsumerWarps / BNS;     // consumer warps along a stage's 8 steps
     constexpr int SPW = 8 / WK;                  // steps per warp per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + a.stages * a.stage_bytes);
+    constexpr int MB = 8 * NT;                    // batch rows a thread's fragments cover
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + a.slots_off +
+                                                  (a.split + WK) * MB * BN * 4);
     uint64_t *empty = full + a.stages;
+    uint64_t *cl_done = empty + a.stages;          // leader: the other CTAs' partials landed
+    float *slots = reinterpret_cast<float *>(ring + a.slots_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == kConsumerWarps * 32) {
+        // the descriptors live in parameter memory: start fetching them first
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_s);
+        prefetch_tmap(&tm_z);
+        prefetch_tmap(&tm_x);
+    }
     const int KB = a.K >> 3;
     const int cta_row0 = blockIdx.y * a.rows_per_cta;
     const int rows_here = min(a.rows_per_cta, KB - cta_row0);
@@ -84,15 +113,34 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     const int Mc = min(16, a.M - m_base);
 
     pdl_launch_dependents();
+#ifdef W4A16_TRACE
+    const long long t_entry = clock64();
+    if (threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        W4A16_TRACE_AT(0, globaltimer_ns());
+        W4A16_TRACE_AT(1, smid);
+    }
+#endif
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerWarps);
         }
+        mbar_init(cl_done, 1);
         fence_mbar_init();
     }
     __syncthreads();
+    // the leader expects the other CTAs' partials as bulk-copy bytes
+    if (a.split > 1 && threadIdx.x == 0 && cluster_ctarank() == 0)
+        mbar_arrive_expect_tx(cl_done, (uint32_t)((a.split - 1) * Mc * BN * 4));
+    // first half of a split cluster barrier: every CTA's barriers exist before
+    // any CTA signals another (the wait comes just before the reduction)
+    if (a.split > 1) cluster_arrive();
+#ifdef W4A16_TRACE
+    if (threadIdx.x == 0) W4A16_TRACE_AT(2, clock64() - t_entry);
+#endif
 
     float acc[NT][2][4];
 #pragma unroll
@@ -109,10 +157,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tmap(&tm_w);
-            prefetch_tmap(&tm_s);
-            prefetch_tmap(&tm_z);
-            prefetch_tmap(&tm_x);
             const uint64_t pol_stream = l2_evict_first_policy();
             const uint64_t pol_keep = l2_evict_last_policy();
             const int skip = (a.test_skip_last && n_st > 0) ? n_st - 1 : -1;
@@ -154,7 +198,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 tma_load_2d(sl + a.z_off, &tm_z, &full[slot], col_base, grow, pol_stream);
                 tma_load_2d(sl + a.x_off, &tm_x, &full[slot], row * 8, m_base, pol_keep);
             }
-            // no copy of this CTA may still be landing when it exits
+#ifdef W4A16_TRACE
+            W4A16_TRACE_AT(3, clock64() - t_entry);
+#endif
+            // no copy of this CTA may still be landing when it exits (normally
+            // the consumers have long seen every stage complete; after a
+            // timed-out wait this bounds the rest)
             for (int st = max(0, n_st - a.stages); st < n_st; ++st) {
                 if (st == skip) continue;
                 if (!mbar_wait_bounded(&full[st % a.stages], (st / a.stages) & 1, a.timeout_ns))
@@ -163,113 +212,154 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         }
     } else {
         // ------------------------------------------------------ consumers
-        const int spg = a.group >> 5;              // 32-k steps per group
-        const int spf = min(SPW, spg);             // steps between scale flushes
+        const int x0_row = g < Mc ? g : 0;         // rows past M read row 0, then zeroed
+        const int x1_row = g + 8 < Mc ? g + 8 : 0;
         const bool x0_ok = g < Mc, x1_ok = g + 8 < Mc;
-        float gacc[NT][2][4];
-#pragma unroll
-        for (int p = 0; p < NT; ++p)
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) gacc[p][j][r] = 0.f;
-
         for (int st = 0; st < n_st; ++st) {
             const int slot = st % a.stages;
             if (!mbar_wait_bounded(&full[slot], (st / a.stages) & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
-            const uint8_t *base = ring + slot * a.stage_bytes;
-            const uint8_t *wtile = base + wn * 4096;
-            GroupConsts k;
+#ifdef W4A16_TRACE
+            if (threadIdx.x == 0 && st < 8) W4A16_TRACE_AT(4 + st, clock64() - t_entry);
+#endif
+            const uint32_t base = smem_u32(ring) + slot * a.stage_bytes;
+            const uint32_t wtile = base + wn * 4096;
+            const int r0 = wk * 4 * SPW;                // first row of this warp in the stage
+            // all of this warp's operands of the stage first (then the slot is
+            // released): the steps below are independent and their MMAs overlap
+            uint4 wv[SPW], xv[NT][SPW];
+            uint2 sraw[ONE_GROUP ? 1 : SPW], zraw[ONE_GROUP ? 1 : SPW];
+#pragma unroll
+            for (int u = 0; u < (ONE_GROUP ? 1 : SPW); ++u) {
+                const int gi = ((r0 + 4 * u) * 8) / a.group;       // group within the stage
+                sraw[u] = lds64(base + a.s_off + (gi * BN + cl) * 2);
+                zraw[u] = lds64(base + a.z_off + (gi * BN + cl) * 2);
+            }
 #pragma unroll
             for (int u = 0; u < SPW; ++u) {
-                const int r = wk * 4 * SPW + 4 * u + t;        // row within the stage
-                if (u % spf == 0) {
-                    const int gi = (r * 8) / a.group;           // group within the stage
-                    const uint2 sraw = *reinterpret_cast<const uint2 *>(base + a.s_off + (gi * BN + cl) * 2);
-                    const uint2 zraw = *reinterpret_cast<const uint2 *>(base + a.z_off + (gi * BN + cl) * 2);
-                    k = make_group_consts(zraw, sraw);
-                }
-                const uint4 w = *reinterpret_cast<const uint4 *>(
-                    wtile + r * 128 + ((perm8(g) ^ (r & 7)) << 4));
-                uint32_t bx[NT][4];
-                {
-                    const uint4 v = x0_ok ? *reinterpret_cast<const uint4 *>(
-                                                base + a.x_off + (g * kStageK + 8 * r) * 2)
-                                          : make_uint4(0, 0, 0, 0);
-                    x_fragments(v, bx[0]);
-                }
+                const int r = r0 + 4 * u + t;           // row within the stage
+                wv[u] = lds128(wtile + r * 128 + ((perm8(g) ^ (r & 7)) << 4));
+                const uint4 v0 = lds128(base + a.x_off + (x0_row * kStageK + 8 * r) * 2);
+                xv[0][u] = x0_ok ? v0 : make_uint4(0, 0, 0, 0);
                 if (NT > 1) {
-                    const uint4 v = x1_ok ? *reinterpret_cast<const uint4 *>(
-                                                base + a.x_off + ((g + 8) * kStageK + 8 * r) * 2)
-                                          : make_uint4(0, 0, 0, 0);
-                    x_fragments(v, bx[NT - 1]);
+                    const uint4 v1 = lds128(base + a.x_off + (x1_row * kStageK + 8 * r) * 2);
+                    xv[NT - 1][u] = x1_ok ? v1 : make_uint4(0, 0, 0, 0);
                 }
-                step_mma<NT>(gacc, w, k, bx);
-                if ((u + 1) % spf == 0) flush_group<NT>(acc, gacc, k);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (lane == 0) mbar_arrive(&empty[slot]);   // operands are in registers
+            GroupConsts k = make_group_consts(zraw[0], sraw[0]);
+#pragma unroll
+            for (int u = 0; u < SPW; ++u) {
+                if (!ONE_GROUP && u > 0) k = make_group_consts(zraw[u], sraw[u]);
+                uint32_t bx[NT][4];
+#pragma unroll
+                for (int p = 0; p < NT; ++p) x_fragments(xv[p][u], bx[p]);
+                float gs[NT][2][4];
+#pragma unroll
+                for (int p = 0; p < NT; ++p)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) gs[p][j][r] = 0.f;
+                step_mma<NT>(gs, wv[u], k, bx);
+                flush_group<NT>(acc, gs, k);
+            }
+#ifdef W4A16_TRACE
+            if (threadIdx.x == 0 && st < 2) {
+                // make the timestamp wait for this stage's arithmetic
+                float sink = 0.f;
+#pragma unroll
+                for (int p = 0; p < NT; ++p) sink += acc[p][0][0] + acc[p][1][3];
+                W4A16_TRACE_AT(14 + st, (clock64() - t_entry) + (sink == 12345.f ? 1 : 0));
+            }
+#endif
         }
     }
 
     // ---------------------------------------------------------- epilogue
-    __syncthreads();   // ring drained: reuse it for the reduction
-    pdl_wait();        // out may still be in use by the previous kernel
-    float *red = reinterpret_cast<float *>(ring);        // [WK][16][BN]
-    float *part = red + WK * 16 * BN;                     // [16][BN]
+#ifdef W4A16_TRACE
+    if (threadIdx.x == 0) W4A16_TRACE_AT(12, clock64() - t_entry);
+#endif
+    // The consumer warps sum their fragment partials in shared memory (fixed
+    // warp order) into this CTA's partial tile [Mc][BN].  With split-K, every
+    // CTA but the cluster leader (rank 0) then ships its tile with one bulk
+    // copy into its slot of the leader's shared memory -- the copy completes
+    // bytes on the leader's barrier -- and exits once the copy has read its
+    // source.  The leader sums the slots in rank order: the result does not
+    // depend on timing, and there are no atomics and no global workspace.
+    float *red = slots + a.split * MB * BN;           // [WK][MB][BN] warp partials
+    const int rank = a.split > 1 ? (int)cluster_ctarank() : 0;
+    const int E = Mc * BN;
     if (warp < kConsumerWarps) {
 #pragma unroll
         for (int p = 0; p < NT; ++p)
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int m = 8 * p + 2 * t + (r & 1);
-                    const int c = cl + 2 * j + (r >> 1);
-                    if (m < Mc) red[(wk * 16 + m) * BN + c] = acc[p][j][r];
-                }
-    }
-    __syncthreads();
-    const int E = Mc * BN;
-    for (int e = threadIdx.x; e < E; e += kThreads) {
-        const int m = e / BN, c = e - m * BN;
-        float v = 0.f;
+                for (int r = 0; r < 4; ++r)
+                    red[(wk * MB + 8 * p + 2 * t + (r & 1)) * BN + cl + 2 * j + (r >> 1)] =
+                        acc[p][j][r];
+        named_bar_sync(1, kConsumerWarps * 32);
+        float *mine = slots + rank * E;            // this CTA's partial (slot `rank`)
+        for (int e = threadIdx.x; e < E; e += kConsumerWarps * 32) {
+            const int m = e / BN, c = e - m * BN;
+            float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < WK; ++w) v += red[(w * 16 + m) * BN + c];
-        if (a.split == 1) {
-            const int col = col_base + c;
-            if (col < a.N)
-                a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
-        } else {
-            part[e] = v;
+            for (int w = 0; w < WK; ++w) v += red[(w * MB + m) * BN + c];
+            mine[e] = v;
+        }
+        if (a.split > 1 && rank != 0) {
+            fence_proxy_async_smem();              // the bulk copy reads these writes
+            named_bar_sync(1, kConsumerWarps * 32);
+            if (threadIdx.x == 0) {
+                cluster_wait();                    // the leader's barrier is initialized
+                bulk_copy_to_cluster(map_to_rank(smem_u32(mine), 0), mine, (uint32_t)E * 4,
+                                     map_to_rank(smem_u32(cl_done), 0));
+                bulk_commit();
+                bulk_wait_read();
+            }
         }
     }
-    if (a.split == 1) return;
-
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    const int rank = (int)cluster.block_rank();
-    const int per = (E + a.split - 1) / a.split;
-    const int e_end = min(E, (rank + 1) * per);
-    for (int e = rank * per + threadIdx.x; e < e_end; e += kThreads) {
+    if (rank != 0) {
+        // the producer warp and the non-leader consumers only complete the
+        // split cluster barrier (thread 0 already waited on it)
+        if (threadIdx.x != 0) cluster_wait();
+#ifdef W4A16_TRACE
+        if (threadIdx.x == 0) W4A16_TRACE_AT(13, clock64() - t_entry);
+#endif
+        return;
+    }
+    __syncthreads();                               // the leader's own partial is in slot 0
+    if (a.split > 1) {
+        cluster_wait();
+        if (!mbar_wait_cluster_bounded(cl_done, 0, a.timeout_ns))
+            report_status(a.status, W4A16_ERR_TIMEOUT);
+    }
+    pdl_wait();        // out may still be in use by the previous kernel
+    for (int e = threadIdx.x; e < E; e += kThreads) {
         float v = 0.f;
-        for (int q = 0; q < a.split; ++q) v += cluster.map_shared_rank(part, q)[e];
+        for (int q = 0; q < a.split; ++q) v += slots[q * E + e];
         const int m = e / BN, c = e - m * BN;
         const int col = col_base + c;
         if (col < a.N)
             a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
     }
-    cluster.sync();    // peers may still be reading this CTA's partials
+#ifdef W4A16_TRACE
+    if (threadIdx.x == 0) W4A16_TRACE_AT(13, clock64() - t_entry);
+#endif
 }
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 struct Layout {
-    int gps, s_off, z_off, x_off, stage_bytes, tx_bytes, stages, smem_bytes;
+    int gps, s_off, z_off, x_off, stage_bytes, tx_bytes, stages, slots_off, smem_bytes;
 };
 
-Layout layout_for(int group, int bns, int nt, int n_st) {
+// Shared memory: the ring of stages, then (split-K only) the leader's
+// reduction slots, then the mbarriers.  The total stays near half an SM so two
+// CTAs (of this GEMM and the next one on the stream) can be resident at once.
+Layout layout_for(int group, int bns, int nt, int n_st, int split, int cw) {
     Layout L;
     const int BN = 32 * bns;
     const int mb = 8 * nt;
@@ -280,31 +370,31 @@ Layout layout_for(int group, int bns, int nt, int n_st) {
     L.x_off = L.z_off + round_up(sz, 128);
     L.stage_bytes = round_up(L.x_off + kStageK * mb * 2, 1024);
     L.tx_bytes = bns * 4096 + 2 * sz + kStageK * mb * 2;
-    int ns = kRingBudget / L.stage_bytes;
+    // [split][MB][BN] CTA partials, then [WK][MB][BN] warp partials (fp32)
+    const int slots_bytes = (split + cw / bns) * mb * BN * 4;
+    int ns = (kSmemBudget - slots_bytes) / L.stage_bytes;
     ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
     if (n_st > 0 && ns > n_st) ns = n_st < 2 ? 2 : n_st;
-    // the epilogue reuses the ring for WK + 1 partial tiles
-    const int red_bytes = (kConsumerWarps / bns + 1) * 16 * BN * 4;
-    while (ns * L.stage_bytes < red_bytes) ++ns;
     L.stages = ns;
-    L.smem_bytes = ns * L.stage_bytes + 2 * ns * 8 + 1024;
+    L.slots_off = ns * L.stage_bytes;
+    L.smem_bytes = L.slots_off + slots_bytes + (2 * ns + 1) * 8 + 1024;
     return L;
 }
 
-template <int NT, int BNS>
+template <int NT, int BNS, int CW, bool OG>
 cudaError_t launch_tma(const CUtensorMap &w, const CUtensorMap &s, const CUtensorMap &z,
                        const CUtensorMap &x, const TmaDecodeArgs &da, int tiles, int mchunks,
                        int smem, bool pdl, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_tma_kernel<NT, BNS>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 116 * 1024);
+        attr_err = cudaFuncSetAttribute(decode_tma_kernel<NT, BNS, CW, OG>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(tiles, da.split, mchunks);
-    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.blockDim = dim3(32 * (CW + 1), 1, 1);
     lc.dynamicSmemBytes = smem;
     lc.stream = stream;
     cudaLaunchAttribute attrs[2];
@@ -323,7 +413,7 @@ cudaError_t launch_tma(const CUtensorMap &w, const CUtensorMap &s, const CUtenso
     }
     lc.attrs = attrs;
     lc.numAttrs = na;
-    return cudaLaunchKernelEx(&lc, decode_tma_kernel<NT, BNS>, w, s, z, x, da);
+    return cudaLaunchKernelEx(&lc, decode_tma_kernel<NT, BNS, CW, OG>, w, s, z, x, da);
 }
 
 int *status_word() {
@@ -342,9 +432,21 @@ int *status_word() {
 
 }  // namespace
 
+#ifdef W4A16_TRACE
+extern "C" __attribute__((visibility("default"))) int w4a16_trace_read(void *host, size_t bytes) {
+    return (int)cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+#endif
+
+int decode_tma_smem_bytes(const w4a16_config &cfg, int M, int group) {
+    const int cw = cfg.warps_k == 16 ? 16 : 8;
+    return layout_for(group, cfg.warps_n, M > 8 ? 2 : 1, cfg.steps, cfg.split_k, cw).smem_bytes;
+}
+
 bool decode_tma_supported(const w4a16_config &cfg, int group) {
     const bool g_ok = group == 32 || group == 64 || group == 128 || group == 256;
-    return g_ok && (cfg.warps_n == 2 || cfg.warps_n == 4) && cfg.split_k >= 1 &&
+    return g_ok && (cfg.warps_n == 2 || cfg.warps_n == 4) &&
+           (cfg.warps_k == 0 || cfg.warps_k == 8 || cfg.warps_k == 16) && cfg.split_k >= 1 &&
            cfg.split_k <= 8 && cfg.steps >= 1;
 }
 
@@ -357,7 +459,9 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     const int KB = a.K / 8;
     const int rows_per_cta = cfg.steps * kStageRows;
     if ((long long)rows_per_cta * cfg.split_k < KB) return cudaErrorInvalidValue;
-    const Layout L = layout_for(a.group, bns, nt, cfg.steps);
+    const int cw = cfg.warps_k == 16 ? 16 : 8;   // consumer warps per CTA
+    const Layout L = layout_for(a.group, bns, nt, cfg.steps, cfg.split_k, cw);
+    if (L.smem_bytes > kSmemMax) return cudaErrorNotSupported;
     const int BN = 32 * bns;
     const int mb = 8 * nt;
     CUtensorMap tw, ts, tz, tx;
@@ -386,6 +490,7 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     da.z_off = L.z_off;
     da.x_off = L.x_off;
     da.tx_bytes = L.tx_bytes;
+    da.slots_off = L.slots_off;
     const bool test_timeout = (cfg.flags & W4A16_FLAG_TEST_TIMEOUT) != 0;
     da.timeout_ns = test_timeout ? 5000000ull : 1000000000ull;   // 5 ms in the test mode, else 1 s
     da.test_skip_last = test_timeout ? 1 : 0;
@@ -393,11 +498,21 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     const int mchunks = (a.M + 15) / 16;
     if (mchunks > 65535) return cudaErrorInvalidValue;
     const bool pdl = (cfg.flags & W4A16_FLAG_PDL) != 0;
-    if (nt == 1)
-        return bns == 4 ? launch_tma<1, 4>(tw, ts, tz, tx, da, tiles, mchunks, L.smem_bytes, pdl, stream)
-                        : launch_tma<1, 2>(tw, ts, tz, tx, da, tiles, mchunks, L.smem_bytes, pdl, stream);
-    return bns == 4 ? launch_tma<2, 4>(tw, ts, tz, tx, da, tiles, mchunks, L.smem_bytes, pdl, stream)
-                    : launch_tma<2, 2>(tw, ts, tz, tx, da, tiles, mchunks, L.smem_bytes, pdl, stream);
+    // steps per warp per stage: 8 * bns / cw; one group per warp-stage if the
+    // group spans at least that many 32-k steps
+    const bool one_group = a.group >= 32 * (8 * bns / cw);
+#define W4A16_TMA_LAUNCH(NT_, BNS_, CW_)                                                         \
+    (one_group ? launch_tma<NT_, BNS_, CW_, true>(tw, ts, tz, tx, da, tiles, mchunks,          \
+                                                  L.smem_bytes, pdl, stream)                   \
+               : launch_tma<NT_, BNS_, CW_, false>(tw, ts, tz, tx, da, tiles, mchunks,         \
+                                                   L.smem_bytes, pdl, stream))
+    if (cw == 8) {
+        if (nt == 1) return bns == 4 ? W4A16_TMA_LAUNCH(1, 4, 8) : W4A16_TMA_LAUNCH(1, 2, 8);
+        return bns == 4 ? W4A16_TMA_LAUNCH(2, 4, 8) : W4A16_TMA_LAUNCH(2, 2, 8);
+    }
+    if (nt == 1) return bns == 4 ? W4A16_TMA_LAUNCH(1, 4, 16) : W4A16_TMA_LAUNCH(1, 2, 16);
+    return bns == 4 ? W4A16_TMA_LAUNCH(2, 4, 16) : W4A16_TMA_LAUNCH(2, 2, 16);
+#undef W4A16_TMA_LAUNCH
 }
 
 }  // namespace w4a16
