@@ -88,6 +88,10 @@ typedef enum w4a16_path {
 #define W4A16_DECODE_TMA 1        /* weights staged by TMA into a shared-memory ring */
 #define W4A16_DECODE_REGISTERS 2  /* weights streamed by 128-bit loads into registers */
 
+/* Prefill kernel variants (w4a16_config.variant on the prefill path). */
+#define W4A16_PREFILL_A_TMEM 1    /* dequantized W^T operand in tensor memory (default) */
+#define W4A16_PREFILL_A_SMEM 2    /* dequantized W^T operand in shared memory */
+
 /*
  * Launch configuration of one GEMM call.  Zero in any field means "choose
  * automatically"; w4a16_plan() returns the choice for a shape.
@@ -95,13 +99,14 @@ typedef enum w4a16_path {
 typedef struct w4a16_config {
     int path;       /* w4a16_path */
     int split_k;    /* decode: CTAs of one cluster that split K (1..8) */
-    int warps_k;    /* decode (registers variant): warps per CTA that split K */
+    int warps_k;    /* decode (registers variant): warps per CTA that split K;
+                       prefill: dequantizing warps (4 or 8; 16 with A in shared memory) */
     int warps_n;    /* decode: 32-column strips per CTA (TMA variant: 2 or 4) */
     int steps;      /* decode: K per warp in 32-row steps (registers variant) or
                        K per CTA in 256-row stages (TMA variant) */
     int tile_m;     /* prefill: rows of x per CTA tile (16..256, multiple of 16) */
     int flags;      /* W4A16_FLAG_* */
-    int variant;    /* decode: W4A16_DECODE_* */
+    int variant;    /* decode: W4A16_DECODE_*; prefill: W4A16_PREFILL_* */
 } w4a16_config;
 
 /*

@@ -193,6 +193,53 @@ def test_bounded_wait_times_out_and_reports():
     check_gemm(x, dev_w, ref_w, 128)       # the next call is correct
 
 
+# ----------------------------------------------------------- prefill path
+@pytest.mark.parametrize("M", [16, 17, 48, 128, 256, 300, 600])
+@pytest.mark.parametrize("K,N", [(1024, 512), (512, 1000), (2048, 392)])
+def test_gemm_prefill_tcgen05(K, N, M):
+    """tcgen05 path: single and multiple M tiles, ragged M and N, every tile_m
+    width class (16-row multiples up to 256)."""
+    _, dev_w, ref_w = quantized(K, N, 128, 51 + K + N, True)
+    x = synth.activations(M, K, seed=52 + M)
+    check_gemm(x, dev_w, ref_w, 128, config=dict(path="prefill"))
+
+
+@pytest.mark.parametrize("tile_m", [16, 32, 112, 256])
+def test_gemm_prefill_tile_widths(tile_m):
+    K, N, M = 1024, 512, 333
+    _, dev_w, ref_w = quantized(K, N, 128, 51 + K + N, True)
+    x = synth.activations(M, K, seed=53)
+    check_gemm(x, dev_w, ref_w, 128, config=dict(path="prefill", tile_m=tile_m))
+
+
+@pytest.mark.parametrize("group", [64, 256])
+def test_gemm_prefill_other_groups(group):
+    K, N, M = 1024, 384, 200
+    _, dev_w, ref_w = quantized(K, N, group, 31 + group, True)
+    x = synth.activations(M, K, seed=32)
+    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill"))
+
+
+def test_prefill_full_size_sampled():
+    """The largest prefill workload (K=8192, N=28672, M=4096) through the
+    automatic dispatch, checked on every row and 48 sampled columns; and
+    M=1024 on K=4096, N=14336."""
+    for (K, N, Ms, si) in ((8192, 28672, (4096,), 1), (4096, 14336, (1024, 64), 0)):
+        W = synth.weight(K, N, seed=synth.weight_seed(4, shape_index=si))
+        dev_w = w4.quantize_pack(to_dev(W), 128)
+        cols = np.sort(np.random.Generator(np.random.PCG64(11)).choice(N, 48, replace=False))
+        ref_w = oracle.quantize_pack(np.ascontiguousarray(W[:, cols]), 128)
+        del W
+        for M in Ms:
+            x = synth.activations(M, K, seed=synth.x_seed(4, M, shape_index=si))
+            out = w4.gemm(to_dev(x), *dev_w, group=128)
+            torch.cuda.synchronize()
+            assert w4.kernel_status() == 0
+            ref = oracle.gemm(x, *ref_w, group=128)
+            err = oracle.rel_err(out.cpu().numpy()[:, cols], ref)
+            assert err <= TOL, (K, N, M, err)
+
+
 def test_gemm_random_encodings():
     """Arbitrary valid codes, scales and zeros (not produced by the quantizer)."""
     K, N = 2048, 512

@@ -206,6 +206,9 @@ bool tma_variant_possible(int N, int group) {
 // (measured on GB300; see the dispatch notes in the design document).
 constexpr int kDecodeMaxM = 16;
 
+// rows of x per prefill CTA: all of M up to 256, else 256
+int default_tile_m(int M) { return M >= 256 ? 256 : ((M + 15) / 16) * 16; }
+
 w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
                        w4a16_config &c) {
     w4a16_status st = check_shape(M, N, K, group);
@@ -216,6 +219,7 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
         if (M > kDecodeMaxM) {
             w4a16_config pc = c;
             pc.path = W4A16_PATH_PREFILL;
+            if (pc.tile_m <= 0) pc.tile_m = default_tile_m(M);
             if (prefill_config_supported(pc, M, N, K, group)) c.path = W4A16_PATH_PREFILL;
         }
     }
@@ -243,7 +247,10 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
             return fail(W4A16_ERR_INVALID_ARG, "unknown decode variant %d", c.variant);
         }
     } else if (c.path == W4A16_PATH_PREFILL) {
-        if (c.tile_m <= 0) c.tile_m = M >= 256 ? 256 : ((M + 15) / 16) * 16;
+        if (c.tile_m <= 0) c.tile_m = default_tile_m(M);
+        // measured: 8 dequantizing warps from 128-row tiles up, 4 below
+        if (c.warps_k <= 0) c.warps_k = c.tile_m >= 128 ? 8 : 4;
+        if (c.variant <= 0) c.variant = W4A16_PREFILL_A_TMEM;
         if (!prefill_config_supported(c, M, N, K, group))
             return fail(W4A16_ERR_UNSUPPORTED, "prefill path not available for M=%d N=%d K=%d "
                         "group=%d tile_m=%d", M, N, K, group, c.tile_m);

@@ -1,12 +1,455 @@
-// prefill.cu -- placeholder until the tcgen05 prefill kernel lands.
+// prefill.cu -- W4A16 GEMM for larger M on the 5th-generation tensor cores
+// (tcgen05.mma, accumulator in tensor memory).
+//
+// What it computes: out[m,n] = sum_k x[m,k] * Wdq[k,n], Wdq = fp16((q - z) * s),
+// fp32 accumulation, fp16 output (page "Beating FP16 with 4-bit Weights",
+// section "The design": the packed tile is loaded, unpacked in registers,
+// dequantized and fed to a tensor-core dot product with fp32 accumulation;
+// section "Results": once M grows into prefill the unpack must hide under the
+// MMA).
+//
+// Roles are swapped so that one kernel serves every M from 16 up:
+//   D[n, m] (TMEM: 128 lanes = weight columns n, tile_m columns = rows m of x)
+//     += A[n, k] (dequantized W^T, K-major, 128B-swizzled, in shared memory)
+//      * B[k, m] (x tile, K-major = x row-major, TMA-loaded 128B-swizzled).
+//   UMMA shape M = 128 (weight columns), N = tile_m (16..256, rows of x), K = 16.
+// Each weight is dequantized once per tile_m rows of x.
+//
+// Warp roles: warp 0 issues TMA (x tile, packed words, scale and zero rows)
+// into a ring of stages; warp 1 allocates tensor memory and its elected lane
+// issues the MMAs and commits them to mbarriers; the 4 or 8 warps after them
+// dequantize each stage's 8 x 128 packed words into the A operand (a thread
+// owns one weight column -- one tensor-memory lane -- and 8 or 4 of its
+// words) and, at the end, read the accumulator out of tensor memory and store
+// fp16 results.  By default A lives in tensor memory (tcgen05.st, read by the
+// MMA as [a_tmem]): the dequantized weight then never touches shared memory,
+// which otherwise becomes the bottleneck (the MMA re-reads both operands from
+// it).  An A-in-shared-memory variant (one 16-byte 128B-swizzled store per
+// word, 4/8/16 dequantizing warps) is kept for comparison.  Every wait is
+// bounded in wall time; a wait that gives up records W4A16_ERR_TIMEOUT and the
+// kernel still frees its tensor memory before it exits.
+#include <mutex>
+
 #include "common.cuh"
+#include "sm100_ptx.cuh"
+#include "tmap.cuh"
 
 namespace w4a16 {
+namespace {
 
-bool prefill_config_supported(const w4a16_config &, int, int, int, int) { return false; }
+constexpr int kDeqWarp0 = 2;           // warps 2.. dequantize + run the epilogue
+constexpr int kTileN = 128;            // weight columns per CTA (UMMA M)
+constexpr int kStageK = 64;            // k per stage (one 128-byte swizzle row of fp16)
+constexpr int kPackedRows = kStageK / 8;
 
-cudaError_t launch_prefill(const GemmArgs &, const w4a16_config &, cudaStream_t) {
-    return cudaErrorNotSupported;
+struct PrefillArgs {
+    uint16_t *out;
+    int *status;
+    int M, N, K, group;
+    int tile_m;            // rows of x per CTA (multiple of 16, <= 256) = UMMA N
+    int stages;
+    int stage_bytes;
+    int b_off, p_off, s_off, z_off;   // offsets in a stage (A tile at 0)
+    int tx_bytes;
+    int tmem_cols;         // allocated columns
+    int a_col0;            // A-in-TMEM: first column of the A stage ring (D uses [0, tile_m))
+    unsigned long long timeout_ns;
+};
+
+// ------------------------------------------------------------ tcgen05 PTX
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (fp16 in, fp32 accumulate)
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (M rows = TMEM lanes, K
+// fp16 elements packed two per 32-bit column) read from tensor memory.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+// 32 lanes x N consecutive 32-bit columns from registers: thread i writes lane (base + i).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 1024-byte groups of 8 (stride between groups 1024 bytes).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                          // leading-dimension offset (unused: K fits the swizzle row)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride-dimension offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                          // descriptor version (sm_100)
+    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, fp16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int umma_m, int umma_n) {
+    return (1u << 4)                                  // D format: f32
+           | (0u << 7) | (0u << 10)                   // A, B format: f16
+           | ((uint32_t)(umma_n >> 3) << 17)          // N / 8
+           | ((uint32_t)(umma_m >> 4) << 24);         // M / 16
+}
+
+// Byte offset of (row, 16-byte chunk) in a K-major 128B-swizzled tile.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// NDQ: dequantizing warps (4, 8 or 16); they split the stage's 8 packed rows
+// of each column (NDQ/4 warps per column group) and, in the epilogue, the
+// accumulator's columns.
+// ATMEM: the dequantized A operand lives in tensor memory (written with
+// tcgen05.st, read by the MMA as [a_tmem]) instead of shared memory; the
+// stage then carries only x, the packed words and the scale/zero rows.
+template <int NDQ, bool ATMEM>
+__global__ void __launch_bounds__(32 * (NDQ + 2), 1)
+prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
+                       const PrefillArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + a.stages * a.stage_bytes);
+    uint64_t *aready = full + a.stages;      // dequantized A tile written
+    uint64_t *empty = aready + a.stages;     // MMAs of the stage completed
+    uint64_t *accum = empty + a.stages;      // all MMAs of the tile completed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTileN;
+    const int m0 = blockIdx.y * a.tile_m;
+    const int KT = a.K / kStageK;
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_s);
+        prefetch_tmap(&tm_z);
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&aready[i], NDQ);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(accum, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_evict_first_policy();
+            const uint64_t pol_x = l2_evict_last_policy();
+            for (int kt = 0; kt < KT; ++kt) {
+                const int s = kt % a.stages, r = kt / a.stages;
+                if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1, a.timeout_ns))
+                    report_status(a.status, W4A16_ERR_TIMEOUT);
+                uint8_t *st = ring + s * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], a.tx_bytes);
+                const int k0 = kt * kStageK;
+                tma_load_2d(st + a.b_off, &tm_x, &full[s], k0, m0, pol_x);
+                tma_load_2d(st + a.p_off, &tm_w, &full[s], n0, k0 / 8, pol_w);
+                tma_load_2d(st + a.s_off, &tm_s, &full[s], n0, k0 / a.group, pol_w);
+                tma_load_2d(st + a.z_off, &tm_z, &full[s], n0, k0 / a.group, pol_w);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(128, a.tile_m);
+            for (int kt = 0; kt < KT; ++kt) {
+                const int s = kt % a.stages, r = kt / a.stages;
+                if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
+                    report_status(a.status, W4A16_ERR_TIMEOUT);
+                if (!mbar_wait_bounded(&aready[s], r & 1, a.timeout_ns))
+                    report_status(a.status, W4A16_ERR_TIMEOUT);
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(ring + s * a.stage_bytes);
+                const uint32_t b_addr = a_addr + a.b_off;
+                const uint32_t a_tmem = tmem_d + (uint32_t)(a.a_col0 + s * (kStageK / 2));
+#pragma unroll
+                for (int kk = 0; kk < kStageK / 16; ++kk) {
+                    if (ATMEM)
+                        umma_f16_ts(tmem_d, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32),
+                                    idesc, (kt | kk) != 0);
+                    else
+                        umma_f16(tmem_d, smem_desc_sw128(a_addr + kk * 32),
+                                 smem_desc_sw128(b_addr + kk * 32), idesc, (kt | kk) != 0);
+                }
+                umma_commit(&empty[s]);
+            }
+            umma_commit(accum);
+        }
+    } else {
+        // ------------------------------------------------------ dequant
+        constexpr int kParts = NDQ / 4;                   // warps per column group
+        static_assert(kPackedRows % kParts == 0, "packed rows must split evenly");
+        static_assert(!ATMEM || (kPackedRows / kParts) * 4 % 16 == 0, "TMEM stores of 16 columns");
+        constexpr int kRowsPer = kPackedRows / kParts;    // packed rows per thread
+        // A-in-TMEM: a warp may only reach its lane quarter (warp % 4), so the
+        // column a thread dequantizes is the TMEM lane of that quarter
+        const int n = ATMEM ? ((warp & 3) * 32 + lane)
+                            : (((warp - kDeqWarp0) * 32 + lane) & (kTileN - 1));
+        const int part = (warp - kDeqWarp0) / 4;          // which packed rows
+        for (int kt = 0; kt < KT; ++kt) {
+            const int s = kt % a.stages, r = kt / a.stages;
+            if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            const uint32_t st = smem_u32(ring + s * a.stage_bytes);
+            // scale and zero of this column's group
+            uint32_t s2, zA;
+            {
+                uint16_t sb, zb;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sb) : "r"(st + a.s_off + 2 * n));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(st + a.z_off + 2 * n));
+                s2 = (uint32_t)sb | ((uint32_t)sb << 16);
+                // (1024 + z) in the low half and (64 + z) in the high half
+                zA = hadd2_u32((uint32_t)zb | ((uint32_t)zb << 16), 0x54006400u);
+            }
+            uint32_t wv[kRowsPer];
+#pragma unroll
+            for (int cc = 0; cc < kRowsPer; ++cc) {
+                const int c = part * kRowsPer + cc;
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wv[cc]) : "r"(st + a.p_off + (c * kTileN + n) * 4));
+            }
+            // natural k order: pair (q_2i, q_2i+1) from byte i of the word:
+            // low half 1024 + q_2i (mantissa bits 0..3), high half 64 + q_2i+1
+            // (mantissa bits 4..7); minus (1024 + z, 64 + z) is q - z exactly,
+            // times the scale is one fp16 rounding of the exact product
+            uint32_t h[kRowsPer * 4];
+#pragma unroll
+            for (int cc = 0; cc < kRowsPer; ++cc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t b = __byte_perm(wv[cc], 0, 0x4040 + 0x0101 * i);
+                    h[cc * 4 + i] =
+                        hmul2_u32(hsub2_u32(lop3_and_or(b, 0x00F0000Fu, 0x54006400u), zA), s2);
+                }
+            if (ATMEM) {
+                // A stage s: lane n, 32-bit columns a_col0 + 32 s + 4 c .. +3 (k = 8c .. 8c+7)
+                const uint32_t ta = tmem_d + ((uint32_t)((warp & 3) * 32) << 16) +
+                                    (uint32_t)(a.a_col0 + s * (kStageK / 2) + part * kRowsPer * 4);
+#pragma unroll
+                for (int c16 = 0; c16 < kRowsPer * 4; c16 += 16) {
+                    uint32_t r16[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r16[i] = h[c16 + i];
+                    tmem_st_32x32b_x16(ta + c16, r16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < kRowsPer; ++cc) {
+                    const uint32_t off = sw128_offset(n, part * kRowsPer + cc);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(st + off),
+                                 "r"(h[cc * 4]), "r"(h[cc * 4 + 1]), "r"(h[cc * 4 + 2]),
+                                 "r"(h[cc * 4 + 3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();      // the tensor cores read these stores
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aready[s]);
+        }
+        // ------------------------------------------------------ epilogue
+        if (!mbar_wait_bounded(accum, 0, a.timeout_ns))
+            report_status(a.status, W4A16_ERR_TIMEOUT);
+        tc_fence_after();
+        const int q = warp & 3;                          // TMEM lane quarter of this warp
+        const int col = n0 + q * 32 + lane;              // weight column = TMEM lane
+        const uint32_t taddr = tmem_d + ((uint32_t)(q * 32) << 16);
+        const int epart = (warp - kDeqWarp0) / 4;        // warps of one quarter split the m chunks
+        for (int mc = 32 * epart; mc < a.tile_m; mc += 32 * kParts) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr + mc, v);
+            tmem_ld_wait();
+            if (col < a.N) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int m = m0 + mc + i;
+                    if (mc + i < a.tile_m && m < a.M)
+                        a.out[(size_t)m * a.N + col] =
+                            __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem_d, a.tmem_cols);
+}
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+template <int NDQ, bool ATMEM>
+cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
+                                  const CUtensorMap &tx, const CUtensorMap &tw,
+                                  const CUtensorMap &ts, const CUtensorMap &tz,
+                                  const PrefillArgs &pa) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(prefill_tcgen05_kernel<NDQ, ATMEM>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr != cudaSuccess) return attr;
+    prefill_tcgen05_kernel<NDQ, ATMEM><<<grid, 32 * (NDQ + 2), smem, stream>>>(tx, tw, ts, tz, pa);
+    return cudaGetLastError();
+}
+
+int *status_word() {
+    int *p = nullptr;
+    return kernel_status_address(&p) == cudaSuccess ? p : nullptr;
+}
+
+}  // namespace
+
+bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group) {
+    (void)M;
+    const bool atmem = cfg.variant != W4A16_PREFILL_A_SMEM;
+    const bool warps_ok = cfg.warps_k == 0 || cfg.warps_k == 4 || cfg.warps_k == 8 ||
+                          (cfg.warps_k == 16 && !atmem);
+    return warps_ok && cfg.tile_m >= 16 && cfg.tile_m <= 256 && cfg.tile_m % 16 == 0 &&
+           group % kStageK == 0 && K % kStageK == 0 && N % 8 == 0 && (K / group) >= 1;
+}
+
+cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
+    if (!prefill_config_supported(cfg, a.M, a.N, a.K, a.group)) return cudaErrorNotSupported;
+    PrefillArgs pa;
+    pa.out = a.out;
+    pa.status = status_word();
+    if (!pa.status) return cudaErrorInvalidDevice;
+    pa.M = a.M;
+    pa.N = a.N;
+    pa.K = a.K;
+    pa.group = a.group;
+    pa.tile_m = cfg.tile_m;
+    // A operand in tensor memory unless the caller asks for shared memory
+    const bool atmem = cfg.variant != W4A16_PREFILL_A_SMEM;
+    const int ndq = cfg.warps_k == 4 || (cfg.warps_k == 16 && !atmem) ? cfg.warps_k : 8;
+    // stage: [A (dequantized W^T, 128 x 64 fp16) when in shared memory]
+    //        | B (x tile, tile_m x 64 fp16) | packed words (8 x 128) | scale row | zero row
+    const int a_bytes = atmem ? 0 : kTileN * kStageK * 2;
+    const int b_bytes = round_up(pa.tile_m, 8) * kStageK * 2;
+    pa.b_off = a_bytes;
+    pa.p_off = pa.b_off + round_up(b_bytes, 1024);
+    pa.s_off = pa.p_off + kPackedRows * kTileN * 4;
+    pa.z_off = pa.s_off + kTileN * 2;
+    pa.stage_bytes = round_up(pa.z_off + kTileN * 2, 1024);
+    pa.tx_bytes = b_bytes + kPackedRows * kTileN * 4 + 2 * kTileN * 2;
+    const int budget = 200 * 1024;
+    int stages = budget / pa.stage_bytes;
+    stages = stages > 12 ? 12 : stages;
+    // tensor memory: the accumulator (tile_m fp32 columns) and, with A in
+    // tensor memory, one 32-column A slot per stage
+    pa.a_col0 = round_up(pa.tile_m, 32);
+    if (atmem) {
+        const int max_stages = (512 - pa.a_col0) / (kStageK / 2);
+        stages = stages > max_stages ? max_stages : stages;
+    }
+    if (stages < 2) return cudaErrorNotSupported;
+    pa.stages = stages;
+    const int need = atmem ? pa.a_col0 + stages * (kStageK / 2) : pa.tile_m;
+    int cols = 32;
+    while (cols < need) cols *= 2;
+    pa.tmem_cols = cols;
+    pa.timeout_ns = 1000000000ull;
+    const size_t smem = (size_t)stages * pa.stage_bytes + (3 * stages + 1) * 8 + 16 + 1024;
+
+    CUtensorMap tx, tw, ts, tz;
+    if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, a.K, a.M, (uint64_t)a.K * 2,
+                      kStageK, pa.tile_m, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, a.K / 8,
+                      (uint64_t)a.N * 4, kTileN, kPackedRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
+                      (uint64_t)a.N * 2, kTileN, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.zeros, a.N, a.K / a.group,
+                      (uint64_t)a.N * 2, kTileN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+
+    const int mtiles = (a.M + pa.tile_m - 1) / pa.tile_m;
+    if (mtiles > 65535) return cudaErrorInvalidValue;
+    dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, 1);
+#define W4A16_PF(NDQ_, AT_) launch_prefill_kernel<NDQ_, AT_>(grid, smem, stream, tx, tw, ts, tz, pa)
+    if (atmem) return ndq == 4 ? W4A16_PF(4, true) : W4A16_PF(8, true);
+    switch (ndq) {
+    case 4: return W4A16_PF(4, false);
+    case 16: return W4A16_PF(16, false);
+    default: return W4A16_PF(8, false);
+    }
+#undef W4A16_PF
 }
 
 }  // namespace w4a16
