@@ -36,8 +36,13 @@ namespace w4a16 {
 // Optional timeline instrumentation (compiled only with -DW4A16_TRACE):
 // per CTA, clock64 offsets of: [0] entry (globaltimer), [1] smid, [2] barriers
 // ready, [3] producer done issuing, [4..11] consumer warp 0 got stage s,
-// [12] main loop done, [13] epilogue done.
+// [12] main loop done, [13] epilogue done; [14..15] compute of stages 0/1
+// done.  Across launches: g_trace_launch[i] = {globaltimer at the entry of the
+// launch's first CTA, at the producer's griddepcontrol.wait return, at the
+// leader's final store} for the i-th launch (slot from g_trace_next).
 __device__ unsigned long long g_trace[4096][16];
+__device__ unsigned long long g_trace_launch[64][4];
+__device__ unsigned int g_trace_next;
 #define W4A16_TRACE_AT(slot, v)                                                         \
     do {                                                                                 \
         const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z); \
@@ -114,6 +119,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
 
     pdl_launch_dependents();
 #ifdef W4A16_TRACE
+    __shared__ unsigned trace_slot;
+    if (threadIdx.x == 0) {
+        const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        trace_slot = cta_ == 0 ? (atomicAdd(&g_trace_next, 1u) & 63u) : 64u;
+        if (trace_slot < 64) g_trace_launch[trace_slot][0] = globaltimer_ns();
+    }
     const long long t_entry = clock64();
     if (threadIdx.x == 0) {
         unsigned smid;
@@ -176,6 +187,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 tma_load_2d(slot + a.z_off, &tm_z, &full[st], col_base, grow, pol_stream);
             }
             pdl_wait();   // x may be the previous kernel's output
+#ifdef W4A16_TRACE
+            if (trace_slot < 64) g_trace_launch[trace_slot][1] = globaltimer_ns();
+#endif
             for (int st = 0; st < first; ++st) {
                 if (st == skip) continue;
                 tma_load_2d(ring + st * a.stage_bytes + a.x_off, &tm_x, &full[st],
@@ -212,6 +226,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         }
     } else {
         // ------------------------------------------------------ consumers
+        // Under programmatic dependent launch this CTA may start while the
+        // previous kernel still runs: the consumers sleep in griddepcontrol.wait
+        // (no stage can complete before x is loaded after it anyway) instead of
+        // spinning on the stage barriers and stealing issue slots from the
+        // previous kernel's warps on the same SM.
+        pdl_wait();
         const int x0_row = g < Mc ? g : 0;         // rows past M read row 0, then zeroed
         const int x1_row = g + 8 < Mc ? g + 8 : 0;
         const bool x0_ok = g < Mc, x1_ok = g + 8 < Mc;
@@ -337,6 +357,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
             report_status(a.status, W4A16_ERR_TIMEOUT);
     }
     pdl_wait();        // out may still be in use by the previous kernel
+#ifdef W4A16_TRACE
+    if (threadIdx.x == 0 && trace_slot < 64) g_trace_launch[trace_slot][2] = globaltimer_ns();
+#endif
     for (int e = threadIdx.x; e < E; e += kThreads) {
         float v = 0.f;
         for (int q = 0; q < a.split; ++q) v += slots[q * E + e];
@@ -435,6 +458,16 @@ int *status_word() {
 #ifdef W4A16_TRACE
 extern "C" __attribute__((visibility("default"))) int w4a16_trace_read(void *host, size_t bytes) {
     return (int)cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+extern "C" __attribute__((visibility("default"))) int w4a16_trace_launches(void *host, int reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(host, g_trace_launch, sizeof(g_trace_launch));
+    if (reset) {
+        static unsigned long long init[64][4];
+        unsigned zero = 0;
+        cudaMemcpyToSymbol(g_trace_launch, init, sizeof(init));
+        cudaMemcpyToSymbol(g_trace_next, &zero, sizeof(zero));
+    }
+    return (int)e;
 }
 #endif
 
