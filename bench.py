@@ -512,9 +512,20 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cublas", action=argparse.BooleanOptionalAction, default=True)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only-shape", type=int, default=None,
+                    help="profiling aid: keep only this shape index of the workload")
+    ap.add_argument("--only-m", type=int, default=None,
+                    help="profiling aid: keep only this M of the workload")
     ap.add_argument("--ref-cols", type=int, default=256)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
+    if args.only_shape is not None or args.only_m is not None:
+        wl = dict(WORKLOADS[args.workload])
+        if args.only_shape is not None:
+            wl["shapes"] = [wl["shapes"][args.only_shape]]
+        if args.only_m is not None:
+            wl["Ms"] = [args.only_m]
+        WORKLOADS[args.workload] = wl
     rank, local, world, pg = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world, pg)

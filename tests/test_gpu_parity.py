@@ -212,6 +212,29 @@ def test_gemm_prefill_tile_widths(tile_m):
     check_gemm(x, dev_w, ref_w, 128, config=dict(path="prefill", tile_m=tile_m))
 
 
+@pytest.mark.parametrize("variant", ["tmem", "smem"])
+@pytest.mark.parametrize("warps", [4, 8, 16])
+def test_gemm_prefill_dequant_warps(warps, variant):
+    """4, 8 or 16 dequantizing warps (16, 8 or 4 packed words per thread and
+    stage), A in tensor or shared memory; K spans more stages than the ring
+    holds, so every slot is reused."""
+    K, N, M = 4096, 640, 272
+    _, dev_w, ref_w = quantized(K, N, 128, 71, True)
+    x = synth.activations(M, K, seed=72)
+    check_gemm(x, dev_w, ref_w, 128,
+               config=dict(path="prefill", warps_k=warps, variant=variant, tile_m=256))
+
+
+@pytest.mark.parametrize("K,group", [(1088, 64), (1152, 192), (576, 192), (960, 320), (1024, 512)])
+def test_gemm_prefill_group_boundaries(K, group):
+    """Stages are 128 k deep: groups of 64 (two scale rows per stage), groups
+    that start mid-stage (192, 320) and K with a half last stage (K % 128 == 64)."""
+    N, M = 264, 97
+    _, dev_w, ref_w = quantized(K, N, group, 17 + group, True)
+    x = synth.activations(M, K, seed=18 + K)
+    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=112))
+
+
 @pytest.mark.parametrize("group", [64, 256])
 def test_gemm_prefill_other_groups(group):
     K, N, M = 1024, 384, 200

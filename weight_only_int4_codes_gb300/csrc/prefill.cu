@@ -39,7 +39,9 @@ namespace {
 
 constexpr int kDeqWarp0 = 2;           // warps 2.. dequantize + run the epilogue
 constexpr int kTileN = 128;            // weight columns per CTA (UMMA M)
-constexpr int kStageK = 64;            // k per stage (one 128-byte swizzle row of fp16)
+constexpr int kChunkK = 64;            // k per 128-byte swizzle row of fp16
+constexpr int kStageK = 128;           // k per pipeline stage (two swizzle chunks)
+constexpr int kChunks = kStageK / kChunkK;
 constexpr int kPackedRows = kStageK / 8;
 
 struct PrefillArgs {
@@ -50,6 +52,8 @@ struct PrefillArgs {
     int stages;
     int stage_bytes;
     int b_off, p_off, s_off, z_off;   // offsets in a stage (A tile at 0)
+    int b_chunk_bytes;     // one 64-k chunk of the x tile (tile_m rows x 128 bytes)
+    int sz_rows;           // scale/zero rows per stage: 1, or 2 when a group boundary may fall mid-stage
     int tx_bytes;
     int tmem_cols;         // allocated columns
     int a_col0;            // A-in-TMEM: first column of the A stage ring (D uses [0, tile_m))
@@ -116,15 +120,31 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
-// 32 lanes x N consecutive 32-bit columns from registers: thread i writes lane (base + i).
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15])
-        : "memory");
+// 32 lanes x NC consecutive 32-bit columns from registers (NC = 16 or 32):
+// thread i writes lane (base + i).
+template <int NC>
+__device__ __forceinline__ void tmem_st_32x32b(uint32_t taddr, const uint32_t (&r)[NC]) {
+    static_assert(NC == 16 || NC == 32, "x16 or x32");
+    if constexpr (NC == 16) {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+            "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+            "r"(r[15])
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+            "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+            "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+            "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+            "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+            "r"(r[29]), "r"(r[30]), "r"(r[31])
+            : "memory");
+    }
 }
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -182,7 +202,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileN;
     const int m0 = blockIdx.y * a.tile_m;
-    const int KT = a.K / kStageK;
+    const int KT = (a.K + kStageK - 1) / kStageK;      // a last half stage reads zero x
 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_x);
@@ -206,48 +226,62 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     tc_fence_after();
     const uint32_t tmem_d = *tmem_slot;
 
+    // The producer and the MMA issuer are single threads whose loop bodies sit
+    // on the critical path of every stage: their ring position is kept
+    // incrementally (no division in the loop) and a stage is 128 k deep, so
+    // each loop trip feeds the tensor core for 8 MMAs.
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_w = l2_evict_first_policy();
             const uint64_t pol_x = l2_evict_last_policy();
+            int s = 0, r = 0, grow = 0, gnext = a.group;
             for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % a.stages, r = kt / a.stages;
+                const int k0 = kt * kStageK;
+                while (k0 >= gnext) { ++grow; gnext += a.group; }
                 if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1, a.timeout_ns))
                     report_status(a.status, W4A16_ERR_TIMEOUT);
                 uint8_t *st = ring + s * a.stage_bytes;
                 mbar_arrive_expect_tx(&full[s], a.tx_bytes);
-                const int k0 = kt * kStageK;
-                tma_load_2d(st + a.b_off, &tm_x, &full[s], k0, m0, pol_x);
+                // x: both 64-k chunks of the tile in one 3-D box (chunk index outermost)
+                tma_load_3d(st + a.b_off, &tm_x, &full[s], 0, m0, k0 / kChunkK, pol_x);
                 tma_load_2d(st + a.p_off, &tm_w, &full[s], n0, k0 / 8, pol_w);
-                tma_load_2d(st + a.s_off, &tm_s, &full[s], n0, k0 / a.group, pol_w);
-                tma_load_2d(st + a.z_off, &tm_z, &full[s], n0, k0 / a.group, pol_w);
+                tma_load_2d(st + a.s_off, &tm_s, &full[s], n0, grow, pol_w);
+                tma_load_2d(st + a.z_off, &tm_z, &full[s], n0, grow, pol_w);
+                if (++s == a.stages) { s = 0; ++r; }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(128, a.tile_m);
+            int s = 0, r = 0;
             for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % a.stages, r = kt / a.stages;
                 if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
                     report_status(a.status, W4A16_ERR_TIMEOUT);
                 if (!mbar_wait_bounded(&aready[s], r & 1, a.timeout_ns))
                     report_status(a.status, W4A16_ERR_TIMEOUT);
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(ring + s * a.stage_bytes);
-                const uint32_t b_addr = a_addr + a.b_off;
+                const uint64_t b_desc = smem_desc_sw128(a_addr + a.b_off);
+                const uint64_t a_desc = smem_desc_sw128(a_addr);
                 const uint32_t a_tmem = tmem_d + (uint32_t)(a.a_col0 + s * (kStageK / 2));
+                // descriptors advance in 16-byte units: 32 bytes per k16 step
+                // inside a chunk, a whole chunk between chunks
+                const uint32_t b_chunk16 = (uint32_t)a.b_chunk_bytes >> 4;
 #pragma unroll
                 for (int kk = 0; kk < kStageK / 16; ++kk) {
+                    const uint32_t c = kk / 4, w = kk % 4;
+                    const uint64_t bd = b_desc + c * b_chunk16 + w * 2;
+                    const uint32_t acc = (kt | kk) != 0;
                     if (ATMEM)
-                        umma_f16_ts(tmem_d, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32),
-                                    idesc, (kt | kk) != 0);
+                        umma_f16_ts(tmem_d, a_tmem + kk * 8, bd, idesc, acc);
                     else
-                        umma_f16(tmem_d, smem_desc_sw128(a_addr + kk * 32),
-                                 smem_desc_sw128(b_addr + kk * 32), idesc, (kt | kk) != 0);
+                        umma_f16(tmem_d, a_desc + c * (kTileN * kChunkK * 2 / 16) + w * 2, bd,
+                                 idesc, acc);
                 }
                 umma_commit(&empty[s]);
+                if (++s == a.stages) { s = 0; ++r; }
             }
             umma_commit(accum);
         }
@@ -255,73 +289,80 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         // ------------------------------------------------------ dequant
         constexpr int kParts = NDQ / 4;                   // warps per column group
         static_assert(kPackedRows % kParts == 0, "packed rows must split evenly");
-        static_assert(!ATMEM || (kPackedRows / kParts) * 4 % 16 == 0, "TMEM stores of 16 columns");
         constexpr int kRowsPer = kPackedRows / kParts;    // packed rows per thread
+        constexpr int kBlk = kRowsPer >= 8 ? 8 : 4;       // words per TMEM store
         // A-in-TMEM: a warp may only reach its lane quarter (warp % 4), so the
         // column a thread dequantizes is the TMEM lane of that quarter
         const int n = ATMEM ? ((warp & 3) * 32 + lane)
                             : (((warp - kDeqWarp0) * 32 + lane) & (kTileN - 1));
         const int part = (warp - kDeqWarp0) / 4;          // which packed rows
+        int s = 0, r = 0;
         for (int kt = 0; kt < KT; ++kt) {
-            const int s = kt % a.stages, r = kt / a.stages;
             if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
             const uint32_t st = smem_u32(ring + s * a.stage_bytes);
-            // scale and zero of this column's group
-            uint32_t s2, zA;
-            {
-                uint16_t sb, zb;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sb) : "r"(st + a.s_off + 2 * n));
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(st + a.z_off + 2 * n));
-                s2 = (uint32_t)sb | ((uint32_t)sb << 16);
-                // (1024 + z) in the low half and (64 + z) in the high half
-                zA = hadd2_u32((uint32_t)zb | ((uint32_t)zb << 16), 0x54006400u);
-            }
-            uint32_t wv[kRowsPer];
+            // the stage's scale/zero rows start at group k0 / group; k = k0 + 64
+            // is the only place inside the stage where a new group can start
+            const int row1 = ((kt * kStageK + kChunkK) % a.group) == 0 ? 1 : 0;
 #pragma unroll
-            for (int cc = 0; cc < kRowsPer; ++cc) {
-                const int c = part * kRowsPer + cc;
-                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wv[cc]) : "r"(st + a.p_off + (c * kTileN + n) * 4));
-            }
-            // natural k order: pair (q_2i, q_2i+1) from byte i of the word:
-            // low half 1024 + q_2i (mantissa bits 0..3), high half 64 + q_2i+1
-            // (mantissa bits 4..7); minus (1024 + z, 64 + z) is q - z exactly,
-            // times the scale is one fp16 rounding of the exact product
-            uint32_t h[kRowsPer * 4];
-#pragma unroll
-            for (int cc = 0; cc < kRowsPer; ++cc)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t b = __byte_perm(wv[cc], 0, 0x4040 + 0x0101 * i);
-                    h[cc * 4 + i] =
-                        hmul2_u32(hsub2_u32(lop3_and_or(b, 0x00F0000Fu, 0x54006400u), zA), s2);
+            for (int b0 = 0; b0 < kRowsPer; b0 += kBlk) {
+                const int c0 = part * kRowsPer + b0;              // first packed row of the block
+                const int zrow = c0 >= kPackedRows / 2 ? row1 : 0;
+                uint32_t s2, zA;
+                {
+                    uint16_t sb, zb;
+                    const uint32_t so = st + a.s_off + zrow * (kTileN * 2) + 2 * n;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sb) : "r"(so));
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(so + (a.z_off - a.s_off)));
+                    s2 = (uint32_t)sb | ((uint32_t)sb << 16);
+                    // (1024 + z) in the low half and (64 + z) in the high half
+                    zA = hadd2_u32((uint32_t)zb | ((uint32_t)zb << 16), 0x54006400u);
                 }
+                uint32_t wv[kBlk];
+#pragma unroll
+                for (int cc = 0; cc < kBlk; ++cc)
+                    asm volatile("ld.shared.u32 %0, [%1];"
+                                 : "=r"(wv[cc])
+                                 : "r"(st + a.p_off + ((c0 + cc) * kTileN + n) * 4));
+                // natural k order: pair (q_2i, q_2i+1) from byte i of the word:
+                // low half 1024 + q_2i (mantissa bits 0..3), high half 64 + q_2i+1
+                // (mantissa bits 4..7); minus (1024 + z, 64 + z) is q - z exactly,
+                // times the scale is one fp16 rounding of the exact product
+                uint32_t h[kBlk * 4];
+#pragma unroll
+                for (int cc = 0; cc < kBlk; ++cc)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t b = __byte_perm(wv[cc], 0, 0x4040 + 0x0101 * i);
+                        h[cc * 4 + i] =
+                            hmul2_u32(hsub2_u32(lop3_and_or(b, 0x00F0000Fu, 0x54006400u), zA), s2);
+                    }
+                if (ATMEM) {
+                    // A stage s: lane n, 32-bit columns a_col0 + 64 s + 4 c .. +3 (k = 8c .. 8c+7)
+                    const uint32_t ta = tmem_d + ((uint32_t)((warp & 3) * 32) << 16) +
+                                        (uint32_t)(a.a_col0 + s * (kStageK / 2) + c0 * 4);
+                    tmem_st_32x32b<kBlk * 4>(ta, h);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < kBlk; ++cc) {
+                        const int c = c0 + cc;
+                        const uint32_t off = (c / 8) * (kTileN * kChunkK * 2) + sw128_offset(n, c % 8);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(st + off),
+                                     "r"(h[cc * 4]), "r"(h[cc * 4 + 1]), "r"(h[cc * 4 + 2]),
+                                     "r"(h[cc * 4 + 3])
+                                     : "memory");
+                    }
+                }
+            }
             if (ATMEM) {
-                // A stage s: lane n, 32-bit columns a_col0 + 32 s + 4 c .. +3 (k = 8c .. 8c+7)
-                const uint32_t ta = tmem_d + ((uint32_t)((warp & 3) * 32) << 16) +
-                                    (uint32_t)(a.a_col0 + s * (kStageK / 2) + part * kRowsPer * 4);
-#pragma unroll
-                for (int c16 = 0; c16 < kRowsPer * 4; c16 += 16) {
-                    uint32_t r16[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) r16[i] = h[c16 + i];
-                    tmem_st_32x32b_x16(ta + c16, r16);
-                }
                 tmem_st_wait();
                 tc_fence_before();
             } else {
-#pragma unroll
-                for (int cc = 0; cc < kRowsPer; ++cc) {
-                    const uint32_t off = sw128_offset(n, part * kRowsPer + cc);
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(st + off),
-                                 "r"(h[cc * 4]), "r"(h[cc * 4 + 1]), "r"(h[cc * 4 + 2]),
-                                 "r"(h[cc * 4 + 3])
-                                 : "memory");
-                }
                 fence_proxy_async_smem();      // the tensor cores read these stores
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&aready[s]);
+            if (++s == a.stages) { s = 0; ++r; }
         }
         // ------------------------------------------------------ epilogue
         if (!mbar_wait_bounded(accum, 0, a.timeout_ns))
@@ -378,11 +419,10 @@ int *status_word() {
 
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group) {
     (void)M;
-    const bool atmem = cfg.variant != W4A16_PREFILL_A_SMEM;
     const bool warps_ok = cfg.warps_k == 0 || cfg.warps_k == 4 || cfg.warps_k == 8 ||
-                          (cfg.warps_k == 16 && !atmem);
+                          cfg.warps_k == 16;
     return warps_ok && cfg.tile_m >= 16 && cfg.tile_m <= 256 && cfg.tile_m % 16 == 0 &&
-           group % kStageK == 0 && K % kStageK == 0 && N % 8 == 0 && (K / group) >= 1;
+           group % kChunkK == 0 && K % kChunkK == 0 && N % 8 == 0 && (K / group) >= 1;
 }
 
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
@@ -398,22 +438,24 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     pa.tile_m = cfg.tile_m;
     // A operand in tensor memory unless the caller asks for shared memory
     const bool atmem = cfg.variant != W4A16_PREFILL_A_SMEM;
-    const int ndq = cfg.warps_k == 4 || (cfg.warps_k == 16 && !atmem) ? cfg.warps_k : 8;
-    // stage: [A (dequantized W^T, 128 x 64 fp16) when in shared memory]
-    //        | B (x tile, tile_m x 64 fp16) | packed words (8 x 128) | scale row | zero row
+    const int ndq = cfg.warps_k > 0 ? cfg.warps_k : 8;
+    // stage (128 k): [A (dequantized W^T, two 128 x 64 fp16 chunks) when in
+    // shared memory] | B (x tile: two tile_m x 64 fp16 chunks) | packed words
+    // (16 x 128) | scale rows | zero rows (1, or 2 when group % 128 != 0)
     const int a_bytes = atmem ? 0 : kTileN * kStageK * 2;
-    const int b_bytes = round_up(pa.tile_m, 8) * kStageK * 2;
+    pa.b_chunk_bytes = pa.tile_m * kChunkK * 2;              // tile_m % 16 == 0: 1024-aligned
+    pa.sz_rows = a.group % kStageK == 0 ? 1 : 2;
     pa.b_off = a_bytes;
-    pa.p_off = pa.b_off + round_up(b_bytes, 1024);
+    pa.p_off = pa.b_off + kChunks * pa.b_chunk_bytes;
     pa.s_off = pa.p_off + kPackedRows * kTileN * 4;
-    pa.z_off = pa.s_off + kTileN * 2;
-    pa.stage_bytes = round_up(pa.z_off + kTileN * 2, 1024);
-    pa.tx_bytes = b_bytes + kPackedRows * kTileN * 4 + 2 * kTileN * 2;
-    const int budget = 200 * 1024;
+    pa.z_off = pa.s_off + pa.sz_rows * kTileN * 2;
+    pa.stage_bytes = round_up(pa.z_off + pa.sz_rows * kTileN * 2, 1024);
+    pa.tx_bytes = kChunks * pa.b_chunk_bytes + kPackedRows * kTileN * 4 + 2 * pa.sz_rows * kTileN * 2;
+    const int budget = 224 * 1024;
     int stages = budget / pa.stage_bytes;
-    stages = stages > 12 ? 12 : stages;
+    stages = stages > 8 ? 8 : stages;
     // tensor memory: the accumulator (tile_m fp32 columns) and, with A in
-    // tensor memory, one 32-column A slot per stage
+    // tensor memory, one 64-column A slot per stage
     pa.a_col0 = round_up(pa.tile_m, 32);
     if (atmem) {
         const int max_stages = (512 - pa.a_col0) / (kStageK / 2);
@@ -428,22 +470,33 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     pa.timeout_ns = 1000000000ull;
     const size_t smem = (size_t)stages * pa.stage_bytes + (3 * stages + 1) * 8 + 16 + 1024;
 
+    // x as a 3-D view {64 k, M rows, K/64 chunks}: one box brings both 64-k
+    // chunks of a stage, each a 128B-swizzled K-major tile
+    const uint64_t x_dims[3] = {(uint64_t)kChunkK, (uint64_t)a.M, (uint64_t)(a.K / kChunkK)};
+    const uint64_t x_strides[2] = {(uint64_t)a.K * 2, (uint64_t)kChunkK * 2};
+    const uint32_t x_box[3] = {(uint32_t)kChunkK, (uint32_t)pa.tile_m, (uint32_t)kChunks};
     CUtensorMap tx, tw, ts, tz;
-    if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, a.K, a.M, (uint64_t)a.K * 2,
-                      kStageK, pa.tile_m, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, x_dims, x_strides, x_box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, a.K / 8,
                       (uint64_t)a.N * 4, kTileN, kPackedRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
-                      (uint64_t)a.N * 2, kTileN, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                      (uint64_t)a.N * 2, kTileN, pa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.zeros, a.N, a.K / a.group,
-                      (uint64_t)a.N * 2, kTileN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+                      (uint64_t)a.N * 2, kTileN, pa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     const int mtiles = (a.M + pa.tile_m - 1) / pa.tile_m;
     if (mtiles > 65535) return cudaErrorInvalidValue;
     dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, 1);
 #define W4A16_PF(NDQ_, AT_) launch_prefill_kernel<NDQ_, AT_>(grid, smem, stream, tx, tw, ts, tz, pa)
-    if (atmem) return ndq == 4 ? W4A16_PF(4, true) : W4A16_PF(8, true);
+    if (atmem) {
+        switch (ndq) {
+        case 4: return W4A16_PF(4, true);
+        case 16: return W4A16_PF(16, true);
+        default: return W4A16_PF(8, true);
+        }
+    }
     switch (ndq) {
     case 4: return W4A16_PF(4, false);
     case 16: return W4A16_PF(16, false);

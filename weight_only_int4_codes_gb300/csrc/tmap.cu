@@ -5,10 +5,10 @@
 // their full description (base address, shape, strides, box, swizzle): a
 // decode loop that calls the GEMM with the same weights and activation buffers
 // pays the encoding once.
+#include <array>
 #include <map>
 #include <mutex>
 #include <string.h>
-#include <tuple>
 
 #include "tmap.cuh"
 
@@ -35,17 +35,23 @@ EncodeFn encoder() {
     return fn;
 }
 
-using Key = std::tuple<uintptr_t, int, uint64_t, uint64_t, uint64_t, uint32_t, uint32_t, int>;
-
 }  // namespace
 
-bool make_tmap_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *base, uint64_t inner,
-                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
-                  uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+bool make_tmap(CUtensorMap *out, CUtensorMapDataType dtype, int rank, const void *base,
+               const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+               CUtensorMapSwizzle swizzle) {
+    if (rank < 1 || rank > 3) return false;
+    // cache key: every field of the description, packed into one array
+    std::array<uint64_t, 13> key{};
+    key[0] = (uintptr_t)base;
+    key[1] = ((uint64_t)dtype << 32) | ((uint64_t)rank << 8) | (uint64_t)swizzle;
+    for (int i = 0; i < rank; ++i) {
+        key[2 + i] = dims[i];
+        key[5 + i] = box[i];
+        if (i + 1 < rank) key[8 + i] = strides_bytes[i];
+    }
     static std::mutex mu;
-    static std::map<Key, CUtensorMap> cache;
-    const Key key{(uintptr_t)base, (int)dtype, inner, outer, row_stride_bytes, box_inner,
-                  box_outer, (int)swizzle};
+    static std::map<std::array<uint64_t, 13>, CUtensorMap> cache;
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
@@ -56,13 +62,16 @@ bool make_tmap_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *base,
     }
     EncodeFn fn = encoder();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {row_stride_bytes};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estride[2] = {1, 1};
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
     CUtensorMap m;
     memset(&m, 0, sizeof m);
-    const CUresult r = fn(&m, dtype, 2, const_cast<void *>(base), dims, strides, box, estride,
+    const CUresult r = fn(&m, dtype, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
@@ -71,6 +80,14 @@ bool make_tmap_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *base,
     cache[key] = m;
     *out = m;
     return true;
+}
+
+bool make_tmap_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return make_tmap(out, dtype, 2, base, dims, &row_stride_bytes, box, swizzle);
 }
 
 }  // namespace w4a16

@@ -22,7 +22,8 @@ _LIB_NAME = "libw4a16.so"
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA",
                 5: "TIMEOUT"}
 PATHS = {"auto": 0, "decode": 1, "prefill": 2}
-VARIANTS = {"auto": 0, "tma": 1, "registers": 2}
+VARIANTS = {"auto": 0, "tma": 1, "registers": 2,      # decode path
+            "tmem": 1, "smem": 2}                  # prefill path: where A lives
 FLAG_PDL = 0x1
 FLAG_TEST_TIMEOUT = 0x100
 
