@@ -37,10 +37,11 @@ namespace w4a16 {
 // per CTA, clock64 offsets of: [0] entry (globaltimer), [1] smid, [2] barriers
 // ready, [3] producer done issuing, [4..11] consumer warp 0 got stage s,
 // [12] main loop done, [13] epilogue done; [14..15] compute of stages 0/1
-// done.  Across launches: g_trace_launch[i] = {globaltimer at the entry of the
+// done; [16] consumers' griddepcontrol.wait returned; [17] CTA partial
+// written; [18] leader: every partial landed.  Across launches: g_trace_launch[i] = {globaltimer at the entry of the
 // launch's first CTA, at the producer's griddepcontrol.wait return, at the
 // leader's final store} for the i-th launch (slot from g_trace_next).
-__device__ unsigned long long g_trace[4096][16];
+__device__ unsigned long long g_trace[4096][24];
 __device__ unsigned long long g_trace_launch[64][4];
 __device__ unsigned int g_trace_next;
 #define W4A16_TRACE_AT(slot, v)                                                         \
@@ -72,6 +73,7 @@ struct TmaDecodeArgs {
     int slots_off;            // cluster reduction slots [split][Mc][BN] (leader only)
     unsigned long long timeout_ns;
     int test_skip_last;       // test hook: arm but never load the CTA's last stage
+    int w3d;                  // weights through one 3-D box per stage (N % 32 == 0)
 };
 
 // consumer lane group g reads 16-byte chunk perm8(g) of its 128-byte row
@@ -180,9 +182,12 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 if (st == skip) continue;
                 const int row = cta_row0 + st * kStageRows;
                 const int grow = row * 8 / a.group;
+                if (a.w3d)
+                    tma_load_3d(slot, &tm_w, &full[st], 0, row, col_base >> 5, pol_stream);
+                else
 #pragma unroll
-                for (int s = 0; s < BNS; ++s)
-                    tma_load_2d(slot + s * 4096, &tm_w, &full[st], col_base + 32 * s, row, pol_stream);
+                    for (int s = 0; s < BNS; ++s)
+                        tma_load_2d(slot + s * 4096, &tm_w, &full[st], col_base + 32 * s, row, pol_stream);
                 tma_load_2d(slot + a.s_off, &tm_s, &full[st], col_base, grow, pol_stream);
                 tma_load_2d(slot + a.z_off, &tm_z, &full[st], col_base, grow, pol_stream);
             }
@@ -195,22 +200,33 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 tma_load_2d(ring + st * a.stage_bytes + a.x_off, &tm_x, &full[st],
                             (cta_row0 + st * kStageRows) * 8, m_base, pol_keep);
             }
+            // steady state: the ring position and the group row advance
+            // incrementally (groups divide the 256-k stage), so the loop trip
+            // is a wait and four copy issues
+            const int gstep = kStageK / a.group;
+            int slot = first < a.stages ? first : 0, round = first < a.stages ? 0 : 1;
+            int row = cta_row0 + first * kStageRows;
+            int grow = row * 8 / a.group;
             for (int st = first; st < n_st; ++st) {
-                const int slot = st % a.stages;
-                const uint32_t parity = ((st / a.stages) - 1) & 1;
-                if (!mbar_wait_bounded(&empty[slot], parity, a.timeout_ns))
+                if (!mbar_wait_bounded(&empty[slot], (round - 1) & 1, a.timeout_ns))
                     report_status(a.status, W4A16_ERR_TIMEOUT);
                 uint8_t *sl = ring + slot * a.stage_bytes;
                 mbar_arrive_expect_tx(&full[slot], a.tx_bytes);
-                if (st == skip) continue;
-                const int row = cta_row0 + st * kStageRows;
-                const int grow = row * 8 / a.group;
+                if (st != skip) {
+                    if (a.w3d)
+                        tma_load_3d(sl, &tm_w, &full[slot], 0, row, col_base >> 5, pol_stream);
+                    else
 #pragma unroll
-                for (int s = 0; s < BNS; ++s)
-                    tma_load_2d(sl + s * 4096, &tm_w, &full[slot], col_base + 32 * s, row, pol_stream);
-                tma_load_2d(sl + a.s_off, &tm_s, &full[slot], col_base, grow, pol_stream);
-                tma_load_2d(sl + a.z_off, &tm_z, &full[slot], col_base, grow, pol_stream);
-                tma_load_2d(sl + a.x_off, &tm_x, &full[slot], row * 8, m_base, pol_keep);
+                        for (int s = 0; s < BNS; ++s)
+                            tma_load_2d(sl + s * 4096, &tm_w, &full[slot], col_base + 32 * s, row,
+                                        pol_stream);
+                    tma_load_2d(sl + a.s_off, &tm_s, &full[slot], col_base, grow, pol_stream);
+                    tma_load_2d(sl + a.z_off, &tm_z, &full[slot], col_base, grow, pol_stream);
+                    tma_load_2d(sl + a.x_off, &tm_x, &full[slot], row * 8, m_base, pol_keep);
+                }
+                row += kStageRows;
+                grow += gstep;
+                if (++slot == a.stages) { slot = 0; ++round; }
             }
 #ifdef W4A16_TRACE
             W4A16_TRACE_AT(3, clock64() - t_entry);
@@ -232,12 +248,16 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         // spinning on the stage barriers and stealing issue slots from the
         // previous kernel's warps on the same SM.
         pdl_wait();
+#ifdef W4A16_TRACE
+        if (threadIdx.x == 0) W4A16_TRACE_AT(16, clock64() - t_entry);
+#endif
         const int x0_row = g < Mc ? g : 0;         // rows past M read row 0, then zeroed
         const int x1_row = g + 8 < Mc ? g + 8 : 0;
         const bool x0_ok = g < Mc, x1_ok = g + 8 < Mc;
+        int slot = 0;
+        uint32_t phase = 0;
         for (int st = 0; st < n_st; ++st) {
-            const int slot = st % a.stages;
-            if (!mbar_wait_bounded(&full[slot], (st / a.stages) & 1, a.timeout_ns))
+            if (!mbar_wait_bounded(&full[slot], phase, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
 #ifdef W4A16_TRACE
             if (threadIdx.x == 0 && st < 8) W4A16_TRACE_AT(4 + st, clock64() - t_entry);
@@ -268,6 +288,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);   // operands are in registers
+            if (++slot == a.stages) { slot = 0; phase ^= 1; }
             GroupConsts k = make_group_consts(zraw[0], sraw[0]);
 #pragma unroll
             for (int u = 0; u < SPW; ++u) {
@@ -329,6 +350,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
             for (int w = 0; w < WK; ++w) v += red[(w * MB + m) * BN + c];
             mine[e] = v;
         }
+#ifdef W4A16_TRACE
+        if (threadIdx.x == 0) W4A16_TRACE_AT(17, clock64() - t_entry);
+#endif
         if (a.split > 1 && rank != 0) {
             fence_proxy_async_smem();              // the bulk copy reads these writes
             named_bar_sync(1, kConsumerWarps * 32);
@@ -356,6 +380,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         if (!mbar_wait_cluster_bounded(cl_done, 0, a.timeout_ns))
             report_status(a.status, W4A16_ERR_TIMEOUT);
     }
+#ifdef W4A16_TRACE
+    if (threadIdx.x == 0) W4A16_TRACE_AT(18, clock64() - t_entry);
+#endif
     pdl_wait();        // out may still be in use by the previous kernel
 #ifdef W4A16_TRACE
     if (threadIdx.x == 0 && trace_slot < 64) g_trace_launch[trace_slot][2] = globaltimer_ns();
@@ -498,8 +525,21 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     const int BN = 32 * bns;
     const int mb = 8 * nt;
     CUtensorMap tw, ts, tz, tx;
-    if (!make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, KB, (uint64_t)a.N * 4,
-                      32, kStageRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    // The weight tile of a stage is BNS strips of 32 columns x 32 packed rows
+    // (128-byte swizzled, strip s at 4096 s).  With N % 32 == 0 the packed
+    // array is also a 3-D tensor {32 columns, K/8 rows, N/32 strips} (strip
+    // stride 128 bytes) and one box brings all BNS strips: the single
+    // producer thread issues one weight copy per stage instead of BNS.
+    const bool w3d = a.N % 32 == 0;
+    const uint64_t w_dims[3] = {32, (uint64_t)KB, (uint64_t)(a.N / 32)};
+    const uint64_t w_strides[2] = {(uint64_t)a.N * 4, 128};
+    const uint32_t w_box[3] = {32, (uint32_t)kStageRows, (uint32_t)bns};
+    const bool w_ok = w3d ? make_tmap(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.packed, w_dims,
+                                      w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B)
+                          : make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, KB,
+                                         (uint64_t)a.N * 4, 32, kStageRows,
+                                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!w_ok ||
         !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
                       (uint64_t)a.N * 2, BN, L.gps, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.zeros, a.N, a.K / a.group,
@@ -527,6 +567,7 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     const bool test_timeout = (cfg.flags & W4A16_FLAG_TEST_TIMEOUT) != 0;
     da.timeout_ns = test_timeout ? 5000000ull : 1000000000ull;   // 5 ms in the test mode, else 1 s
     da.test_skip_last = test_timeout ? 1 : 0;
+    da.w3d = w3d ? 1 : 0;
     const int tiles = (a.N + BN - 1) / BN;
     const int mchunks = (a.M + 15) / 16;
     if (mchunks > 65535) return cudaErrorInvalidValue;

@@ -232,15 +232,17 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     // each loop trip feeds the tensor core for 8 MMAs.
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_w = l2_evict_first_policy();
-            const uint64_t pol_x = l2_evict_last_policy();
-            int s = 0, r = 0, grow = 0, gnext = a.group;
-            for (int kt = 0; kt < KT; ++kt) {
-                const int k0 = kt * kStageK;
-                while (k0 >= gnext) { ++grow; gnext += a.group; }
-                if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1, a.timeout_ns))
-                    report_status(a.status, W4A16_ERR_TIMEOUT);
+        // The whole warp runs the loop (its control values stay warp-uniform);
+        // lane 0 issues.
+        const uint64_t pol_w = l2_evict_first_policy();
+        const uint64_t pol_x = l2_evict_last_policy();
+        int s = 0, r = 0, grow = 0, gnext = a.group;
+        for (int kt = 0; kt < KT; ++kt) {
+            const int k0 = kt * kStageK;
+            while (k0 >= gnext) { ++grow; gnext += a.group; }
+            if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            if (lane == 0) {
                 uint8_t *st = ring + s * a.stage_bytes;
                 mbar_arrive_expect_tx(&full[s], a.tx_bytes);
                 // x: both 64-k chunks of the tile in one 3-D box (chunk index outermost)
@@ -248,43 +250,50 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                 tma_load_2d(st + a.p_off, &tm_w, &full[s], n0, k0 / 8, pol_w);
                 tma_load_2d(st + a.s_off, &tm_s, &full[s], n0, grow, pol_w);
                 tma_load_2d(st + a.z_off, &tm_z, &full[s], n0, grow, pol_w);
-                if (++s == a.stages) { s = 0; ++r; }
             }
+            __syncwarp();
+            if (++s == a.stages) { s = 0; ++r; }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16(128, a.tile_m);
-            int s = 0, r = 0;
-            for (int kt = 0; kt < KT; ++kt) {
-                if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
-                    report_status(a.status, W4A16_ERR_TIMEOUT);
-                if (!mbar_wait_bounded(&aready[s], r & 1, a.timeout_ns))
-                    report_status(a.status, W4A16_ERR_TIMEOUT);
-                tc_fence_after();
-                const uint32_t a_addr = smem_u32(ring + s * a.stage_bytes);
-                const uint64_t b_desc = smem_desc_sw128(a_addr + a.b_off);
-                const uint64_t a_desc = smem_desc_sw128(a_addr);
-                const uint32_t a_tmem = tmem_d + (uint32_t)(a.a_col0 + s * (kStageK / 2));
+        // Warp-wide loop, lane 0 issues the MMAs and the commits (a commit
+        // tracks the MMAs of the thread that issues it).
+        const uint32_t idesc = idesc_f16(128, a.tile_m);
+        const uint32_t tmem_u = __shfl_sync(0xffffffffu, tmem_d, 0);
+        const uint32_t b_chunk16 = (uint32_t)a.b_chunk_bytes >> 4;
+        const uint32_t ring_u = smem_u32(ring);
+        int s = 0, r = 0;
+        for (int kt = 0; kt < KT; ++kt) {
+            if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            if (!mbar_wait_bounded(&aready[s], r & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            tc_fence_after();
+            const uint32_t a_addr = ring_u + (uint32_t)(s * a.stage_bytes);
+            const uint64_t b_desc = smem_desc_sw128(a_addr + a.b_off);
+            const uint64_t a_desc = smem_desc_sw128(a_addr);
+            const uint32_t a_tmem = tmem_u + (uint32_t)(a.a_col0 + s * (kStageK / 2));
+            if (lane == 0) {
                 // descriptors advance in 16-byte units: 32 bytes per k16 step
                 // inside a chunk, a whole chunk between chunks
-                const uint32_t b_chunk16 = (uint32_t)a.b_chunk_bytes >> 4;
 #pragma unroll
                 for (int kk = 0; kk < kStageK / 16; ++kk) {
                     const uint32_t c = kk / 4, w = kk % 4;
                     const uint64_t bd = b_desc + c * b_chunk16 + w * 2;
                     const uint32_t acc = (kt | kk) != 0;
                     if (ATMEM)
-                        umma_f16_ts(tmem_d, a_tmem + kk * 8, bd, idesc, acc);
+                        umma_f16_ts(tmem_u, a_tmem + kk * 8, bd, idesc, acc);
                     else
-                        umma_f16(tmem_d, a_desc + c * (kTileN * kChunkK * 2 / 16) + w * 2, bd,
+                        umma_f16(tmem_u, a_desc + c * (kTileN * kChunkK * 2 / 16) + w * 2, bd,
                                  idesc, acc);
                 }
                 umma_commit(&empty[s]);
-                if (++s == a.stages) { s = 0; ++r; }
             }
-            umma_commit(accum);
+            __syncwarp();
+            if (++s == a.stages) { s = 0; ++r; }
         }
+        if (lane == 0) umma_commit(accum);
+        __syncwarp();
     } else {
         // ------------------------------------------------------ dequant
         constexpr int kParts = NDQ / 4;                   // warps per column group
