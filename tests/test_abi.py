@@ -110,7 +110,9 @@ def test_auto_path_small_m_is_decode():
         p = w4.plan(M, 4096, 4096)
         assert p["path"] == 1 and p["variant"] in (1, 2)
     # measured dispatch table rows
-    assert w4.plan(1, 4096, 4096)["variant"] == 2         # registers variant wins 4096^2
+    t = w4.plan(1, 4096, 4096)                            # TMA variant, split 8, at M <= 2
+    assert (t["variant"], t["split_k"], t["steps"]) == (1, 8, 2)
+    assert w4.plan(16, 4096, 4096)["variant"] == 2         # registers variant at M = 16
     t = w4.plan(4, 14336, 4096)
     assert (t["variant"], t["warps_n"], t["split_k"], t["steps"]) == (1, 4, 2, 8)
     assert w4.plan(1, 4092, 4096)["variant"] == 2         # N % 8 != 0: registers variant

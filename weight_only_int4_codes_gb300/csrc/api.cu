@@ -172,7 +172,9 @@ struct TableEntry {
 };
 constexpr TableEntry kDecodeTable[] = {
     // K      N      M<=   path split warps_k warps_n steps tile flags variant
-    {4096, 4096, 16, {1, 2, 8, 1, 8, 0, 0, W4A16_DECODE_REGISTERS}},
+    {4096, 4096, 2, {1, 8, 8, 4, 2, 0, 0, W4A16_DECODE_TMA}},
+    {4096, 4096, 8, {1, 2, 8, 1, 8, 0, 0, W4A16_DECODE_REGISTERS}},
+    {4096, 4096, 16, {1, 1, 8, 1, 16, 0, 0, W4A16_DECODE_REGISTERS}},
     {4096, 14336, 8, {1, 2, 8, 4, 8, 0, 0, W4A16_DECODE_TMA}},
     {4096, 14336, 16, {1, 1, 4, 1, 32, 0, 0, W4A16_DECODE_REGISTERS}},
     {14336, 4096, 8, {1, 8, 8, 4, 7, 0, 0, W4A16_DECODE_TMA}},
@@ -203,7 +205,7 @@ bool tma_variant_possible(int N, int group) {
 }
 
 // Crossover between the decode path and the tcgen05 prefill path, in rows of x
-// (measured on GB300; see the dispatch notes in the design document).
+// (measured on GB300: at M = 16 the decode kernels are still ahead).
 constexpr int kDecodeMaxM = 16;
 
 // rows of x per prefill CTA: all of M up to 256, else 256

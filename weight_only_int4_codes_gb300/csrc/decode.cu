@@ -130,21 +130,21 @@ __device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batc
         if (NT > 1) xr[NT - 1][u] = m1_ok ? ld_nc_v4(xrow1 + koff) : make_uint4(0, 0, 0, 0);
     }
     const GroupConsts k = make_group_consts(b.z, b.s);
-    float gacc[NT][2][4];
+    float gacc[NT][2][2][4];
 #pragma unroll
     for (int p = 0; p < NT; ++p)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) gacc[p][j][r] = 0.f;
+            for (int r = 0; r < 4; ++r) gacc[p][j][0][r] = gacc[p][j][1][r] = 0.f;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         uint32_t bx[NT][4];
 #pragma unroll
         for (int p = 0; p < NT; ++p) x_fragments(xr[p][u], bx[p]);
-        step_mma<NT>(gacc, b.w[u], k, bx);
+        step_mma_split<NT>(gacc, b.w[u], k, bx);
     }
-    flush_group<NT>(acc, gacc, k);
+    flush_group_split<NT>(acc, gacc, k);
 }
 
 // Grid: (ceil(N / (32*WN)), split, ceil(M / 16)); cluster (1, split, 1).

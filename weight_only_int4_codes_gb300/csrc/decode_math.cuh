@@ -74,49 +74,52 @@ __device__ __forceinline__ void x_fragments(uint4 v, uint32_t (&b)[4]) {
 }
 
 // One 32-k step of one thread: 4 words (columns c0..c0+3) x 8 k, MMAs into the
-// group accumulator gacc[p][j] (p = batch tile of 8 rows, j = column pair).
+// group accumulator gacc[p][j][kk] (p = batch tile of 8 rows, j = column pair,
+// kk = k half).  The two k halves accumulate separately, so the four MMAs of a
+// step are independent and steps that accumulate into the same registers form
+// chains only as long as the number of steps.
 template <int NT>
-__device__ __forceinline__ void step_mma(float (&gacc)[NT][2][4], uint4 w, const GroupConsts &k,
-                                         const uint32_t (&bx)[NT][4]) {
+__device__ __forceinline__ void step_mma_split(float (&gacc)[NT][2][2][4], uint4 w,
+                                               const GroupConsts &k,
+                                               const uint32_t (&bx)[NT][4]) {
     const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const uint32_t c0 = wv[2 * j], c1 = wv[2 * j + 1];
-        {   // kk = 0: nibbles (0,4) | (1,5)
-            const uint32_t a0 = hsub2_u32(lop3_and_or(c0, kMaskLo, kMagicLo), k.zA[2 * j]);
-            const uint32_t a1 = hsub2_u32(lop3_and_or(c1, kMaskLo, kMagicLo), k.zA[2 * j + 1]);
-            const uint32_t a2 = hsub2_u32(lop3_and_or(c0, kMaskHi, kMagicHi), k.zB[2 * j]);
-            const uint32_t a3 = hsub2_u32(lop3_and_or(c1, kMaskHi, kMagicHi), k.zB[2 * j + 1]);
+        const uint32_t d0 = c0 >> 8, d1 = c1 >> 8;
+        const uint32_t a0 = hsub2_u32(lop3_and_or(c0, kMaskLo, kMagicLo), k.zA[2 * j]);
+        const uint32_t a1 = hsub2_u32(lop3_and_or(c1, kMaskLo, kMagicLo), k.zA[2 * j + 1]);
+        const uint32_t a2 = hsub2_u32(lop3_and_or(c0, kMaskHi, kMagicHi), k.zB[2 * j]);
+        const uint32_t a3 = hsub2_u32(lop3_and_or(c1, kMaskHi, kMagicHi), k.zB[2 * j + 1]);
+        const uint32_t e0 = hsub2_u32(lop3_and_or(d0, kMaskLo, kMagicLo), k.zA[2 * j]);
+        const uint32_t e1 = hsub2_u32(lop3_and_or(d1, kMaskLo, kMagicLo), k.zA[2 * j + 1]);
+        const uint32_t e2 = hsub2_u32(lop3_and_or(d0, kMaskHi, kMagicHi), k.zB[2 * j]);
+        const uint32_t e3 = hsub2_u32(lop3_and_or(d1, kMaskHi, kMagicHi), k.zB[2 * j + 1]);
 #pragma unroll
-            for (int p = 0; p < NT; ++p) mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][0], bx[p][1]);
-        }
-        {   // kk = 1: nibbles (2,6) | (3,7)
-            const uint32_t d0 = c0 >> 8, d1 = c1 >> 8;
-            const uint32_t a0 = hsub2_u32(lop3_and_or(d0, kMaskLo, kMagicLo), k.zA[2 * j]);
-            const uint32_t a1 = hsub2_u32(lop3_and_or(d1, kMaskLo, kMagicLo), k.zA[2 * j + 1]);
-            const uint32_t a2 = hsub2_u32(lop3_and_or(d0, kMaskHi, kMagicHi), k.zB[2 * j]);
-            const uint32_t a3 = hsub2_u32(lop3_and_or(d1, kMaskHi, kMagicHi), k.zB[2 * j + 1]);
-#pragma unroll
-            for (int p = 0; p < NT; ++p) mma_16816(gacc[p][j], a0, a1, a2, a3, bx[p][2], bx[p][3]);
+        for (int p = 0; p < NT; ++p) {
+            mma_16816(gacc[p][j][0], a0, a1, a2, a3, bx[p][0], bx[p][1]);
+            mma_16816(gacc[p][j][1], e0, e1, e2, e3, bx[p][2], bx[p][3]);
         }
     }
 }
 
-// acc += s * gacc (the group scale, applied once per group in fp32), then gacc = 0.
+// acc += s * (gacc[..][0] + gacc[..][1]) (the group scale, applied once per
+// group in fp32), then gacc = 0.
 template <int NT>
-__device__ __forceinline__ void flush_group(float (&acc)[NT][2][4], float (&gacc)[NT][2][4],
-                                            const GroupConsts &k) {
+__device__ __forceinline__ void flush_group_split(float (&acc)[NT][2][4],
+                                                  float (&gacc)[NT][2][2][4],
+                                                  const GroupConsts &k) {
 #pragma unroll
     for (int p = 0; p < NT; ++p)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            acc[p][j][0] = fmaf(k.sc[2 * j], gacc[p][j][0], acc[p][j][0]);
-            acc[p][j][1] = fmaf(k.sc[2 * j], gacc[p][j][1], acc[p][j][1]);
-            acc[p][j][2] = fmaf(k.sc[2 * j + 1], gacc[p][j][2], acc[p][j][2]);
-            acc[p][j][3] = fmaf(k.sc[2 * j + 1], gacc[p][j][3], acc[p][j][3]);
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) gacc[p][j][r] = 0.f;
-        }
+            for (int r = 0; r < 4; ++r) {
+                acc[p][j][r] = fmaf(k.sc[2 * j + (r >> 1)], gacc[p][j][0][r] + gacc[p][j][1][r],
+                                    acc[p][j][r]);
+                gacc[p][j][0][r] = 0.f;
+                gacc[p][j][1][r] = 0.f;
+            }
 }
 
 }  // namespace w4a16

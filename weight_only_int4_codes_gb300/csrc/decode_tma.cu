@@ -290,22 +290,25 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
             if (lane == 0) mbar_arrive(&empty[slot]);   // operands are in registers
             if (++slot == a.stages) { slot = 0; phase ^= 1; }
             GroupConsts k = make_group_consts(zraw[0], sraw[0]);
+            // one group per warp-stage: the warp's steps accumulate together
+            // and the scale is applied once; otherwise once per step
+            float gs[NT][2][2][4];
+#pragma unroll
+            for (int p = 0; p < NT; ++p)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) gs[p][j][0][r] = gs[p][j][1][r] = 0.f;
 #pragma unroll
             for (int u = 0; u < SPW; ++u) {
                 if (!ONE_GROUP && u > 0) k = make_group_consts(zraw[u], sraw[u]);
                 uint32_t bx[NT][4];
 #pragma unroll
                 for (int p = 0; p < NT; ++p) x_fragments(xv[p][u], bx[p]);
-                float gs[NT][2][4];
-#pragma unroll
-                for (int p = 0; p < NT; ++p)
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) gs[p][j][r] = 0.f;
-                step_mma<NT>(gs, wv[u], k, bx);
-                flush_group<NT>(acc, gs, k);
+                step_mma_split<NT>(gs, wv[u], k, bx);
+                if (!ONE_GROUP) flush_group_split<NT>(acc, gs, k);
             }
+            if (ONE_GROUP) flush_group_split<NT>(acc, gs, k);
 #ifdef W4A16_TRACE
             if (threadIdx.x == 0 && st < 2) {
                 // make the timestamp wait for this stage's arithmetic
