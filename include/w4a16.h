@@ -91,6 +91,8 @@ typedef enum w4a16_path {
 /* Prefill kernel variants (w4a16_config.variant on the prefill path). */
 #define W4A16_PREFILL_A_TMEM 1    /* dequantized W^T operand in tensor memory (default) */
 #define W4A16_PREFILL_A_SMEM 2    /* dequantized W^T operand in shared memory */
+#define W4A16_PREFILL_PAIR 3      /* CTA pairs (cta_group::2): UMMA M = 256, each CTA
+                                     holds 128 weight columns and half of the x tile */
 
 /*
  * Launch configuration of one GEMM call.  Zero in any field means "choose
@@ -100,11 +102,11 @@ typedef struct w4a16_config {
     int path;       /* w4a16_path */
     int split_k;    /* decode: CTAs of one cluster that split K (1..8) */
     int warps_k;    /* decode (registers variant): warps per CTA that split K;
-                       prefill: dequantizing warps (4 or 8; 16 with A in shared memory) */
+                       prefill: dequantizing warps (4, 8 or 16; 4 or 8 for CTA pairs) */
     int warps_n;    /* decode: 32-column strips per CTA (TMA variant: 2 or 4) */
     int steps;      /* decode: K per warp in 32-row steps (registers variant) or
                        K per CTA in 256-row stages (TMA variant) */
-    int tile_m;     /* prefill: rows of x per CTA tile (16..256, multiple of 16) */
+    int tile_m;     /* prefill: rows of x per CTA (CTA pair) tile (16..256, multiple of 16) */
     int flags;      /* W4A16_FLAG_* */
     int variant;    /* decode: W4A16_DECODE_*; prefill: W4A16_PREFILL_* */
 } w4a16_config;

@@ -225,6 +225,29 @@ def test_gemm_prefill_dequant_warps(warps, variant):
                config=dict(path="prefill", warps_k=warps, variant=variant, tile_m=256))
 
 
+@pytest.mark.parametrize("warps", [4, 8])
+@pytest.mark.parametrize("M,tile_m", [(16, 16), (100, 48), (300, 128), (600, 256), (257, 256)])
+def test_gemm_prefill_cta_pair(M, tile_m, warps):
+    """CTA-pair kernel (cta_group::2, UMMA M = 256): each CTA holds 128 weight
+    columns and half of the x tile; N ragged against the 256-column pair tile,
+    M ragged against tile_m."""
+    K, N = 2048, 392
+    _, dev_w, ref_w = quantized(K, N, 128, 81, True)
+    x = synth.activations(M, K, seed=82 + M)
+    check_gemm(x, dev_w, ref_w, 128,
+               config=dict(path="prefill", variant="pair", tile_m=tile_m, warps_k=warps))
+
+
+@pytest.mark.parametrize("K,group", [(1088, 64), (1152, 192), (576, 192), (960, 320)])
+def test_gemm_prefill_cta_pair_groups(K, group):
+    """Groups of 64, groups starting mid-stage, a half last stage; N = 520
+    leaves the odd CTA of the last pair entirely past N."""
+    N, M = 520, 131
+    _, dev_w, ref_w = quantized(K, N, group, 17 + group, True)
+    x = synth.activations(M, K, seed=19 + K)
+    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", variant="pair", tile_m=144))
+
+
 @pytest.mark.parametrize("K,group", [(1088, 64), (1152, 192), (576, 192), (960, 320), (1024, 512)])
 def test_gemm_prefill_group_boundaries(K, group):
     """Stages are 128 k deep: groups of 64 (two scale rows per stage), groups

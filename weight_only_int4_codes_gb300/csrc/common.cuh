@@ -52,6 +52,8 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
 // Prefill path (tcgen05).  Returns cudaErrorNotSupported if unavailable.
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group);
+cudaError_t launch_prefill_pair(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
+bool prefill_pair_supported(const w4a16_config &cfg, int M, int N, int K, int group);
 
 // Hardware facts used by the planner (queried once per device, cached).
 struct DeviceInfo {

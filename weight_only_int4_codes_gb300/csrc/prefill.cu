@@ -32,17 +32,13 @@
 
 #include "common.cuh"
 #include "sm100_ptx.cuh"
+#include "prefill_tile.cuh"
+#include "tcgen05.cuh"
 #include "tmap.cuh"
 
 namespace w4a16 {
 namespace {
 
-constexpr int kDeqWarp0 = 2;           // warps 2.. dequantize + run the epilogue
-constexpr int kTileN = 128;            // weight columns per CTA (UMMA M)
-constexpr int kChunkK = 64;            // k per 128-byte swizzle row of fp16
-constexpr int kStageK = 128;           // k per pipeline stage (two swizzle chunks)
-constexpr int kChunks = kStageK / kChunkK;
-constexpr int kPackedRows = kStageK / 8;
 
 struct PrefillArgs {
     uint16_t *out;
@@ -59,124 +55,6 @@ struct PrefillArgs {
     int a_col0;            // A-in-TMEM: first column of the A stage ring (D uses [0, tile_m))
     unsigned long long timeout_ns;
 };
-
-// ------------------------------------------------------------ tcgen05 PTX
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (fp16 in, fp32 accumulate)
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (M rows = TMEM lanes, K
-// fp16 elements packed two per 32-bit column) read from tensor memory.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-// 32 lanes x NC consecutive 32-bit columns from registers (NC = 16 or 32):
-// thread i writes lane (base + i).
-template <int NC>
-__device__ __forceinline__ void tmem_st_32x32b(uint32_t taddr, const uint32_t (&r)[NC]) {
-    static_assert(NC == 16 || NC == 32, "x16 or x32");
-    if constexpr (NC == 16) {
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-            "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-            "r"(r[15])
-            : "memory");
-    } else {
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-            "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-            "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-            "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-            "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-            "r"(r[29]), "r"(r[30]), "r"(r[31])
-            : "memory");
-    }
-}
-__device__ __forceinline__ void tmem_st_wait() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes in 1024-byte groups of 8 (stride between groups 1024 bytes).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
-    d |= (uint64_t)1 << 16;                          // leading-dimension offset (unused: K fits the swizzle row)
-    d |= (uint64_t)(1024 >> 4) << 32;                // stride-dimension offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;                          // descriptor version (sm_100)
-    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 D, fp16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_f16(int umma_m, int umma_n) {
-    return (1u << 4)                                  // D format: f32
-           | (0u << 7) | (0u << 10)                   // A, B format: f16
-           | ((uint32_t)(umma_n >> 3) << 17)          // N / 8
-           | ((uint32_t)(umma_m >> 4) << 24);         // M / 16
-}
-
-// Byte offset of (row, 16-byte chunk) in a K-major 128B-swizzled tile.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
-    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
-}
 
 // NDQ: dequantizing warps (4, 8 or 16); they split the stage's 8 packed rows
 // of each column (NDQ/4 warps per column group) and, in the epilogue, the
@@ -218,8 +96,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
-        tmem_relinquish();
+        tmem_alloc<1>(smem_u32(tmem_slot), a.tmem_cols);
+        tmem_relinquish<1>();
     }
     tc_fence_before();
     __syncthreads();
@@ -282,17 +160,17 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                     const uint64_t bd = b_desc + c * b_chunk16 + w * 2;
                     const uint32_t acc = (kt | kk) != 0;
                     if (ATMEM)
-                        umma_f16_ts(tmem_u, a_tmem + kk * 8, bd, idesc, acc);
+                        umma_f16_ts<1>(tmem_u, a_tmem + kk * 8, bd, idesc, acc);
                     else
-                        umma_f16(tmem_u, a_desc + c * (kTileN * kChunkK * 2 / 16) + w * 2, bd,
+                        umma_f16_ss<1>(tmem_u, a_desc + c * (kTileN * kChunkK * 2 / 16) + w * 2, bd,
                                  idesc, acc);
                 }
-                umma_commit(&empty[s]);
+                umma_commit<1>(&empty[s]);
             }
             __syncwarp();
             if (++s == a.stages) { s = 0; ++r; }
         }
-        if (lane == 0) umma_commit(accum);
+        if (lane == 0) umma_commit<1>(accum);
         __syncwarp();
     } else {
         // ------------------------------------------------------ dequant
@@ -310,42 +188,14 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
             const uint32_t st = smem_u32(ring + s * a.stage_bytes);
-            // the stage's scale/zero rows start at group k0 / group; k = k0 + 64
-            // is the only place inside the stage where a new group can start
-            const int row1 = ((kt * kStageK + kChunkK) % a.group) == 0 ? 1 : 0;
+            // the stage's scale/zero rows start at group k0 / group
+            const int k0 = kt * kStageK;
 #pragma unroll
             for (int b0 = 0; b0 < kRowsPer; b0 += kBlk) {
                 const int c0 = part * kRowsPer + b0;              // first packed row of the block
-                const int zrow = c0 >= kPackedRows / 2 ? row1 : 0;
-                uint32_t s2, zA;
-                {
-                    uint16_t sb, zb;
-                    const uint32_t so = st + a.s_off + zrow * (kTileN * 2) + 2 * n;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sb) : "r"(so));
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(so + (a.z_off - a.s_off)));
-                    s2 = (uint32_t)sb | ((uint32_t)sb << 16);
-                    // (1024 + z) in the low half and (64 + z) in the high half
-                    zA = hadd2_u32((uint32_t)zb | ((uint32_t)zb << 16), 0x54006400u);
-                }
-                uint32_t wv[kBlk];
-#pragma unroll
-                for (int cc = 0; cc < kBlk; ++cc)
-                    asm volatile("ld.shared.u32 %0, [%1];"
-                                 : "=r"(wv[cc])
-                                 : "r"(st + a.p_off + ((c0 + cc) * kTileN + n) * 4));
-                // natural k order: pair (q_2i, q_2i+1) from byte i of the word:
-                // low half 1024 + q_2i (mantissa bits 0..3), high half 64 + q_2i+1
-                // (mantissa bits 4..7); minus (1024 + z, 64 + z) is q - z exactly,
-                // times the scale is one fp16 rounding of the exact product
                 uint32_t h[kBlk * 4];
-#pragma unroll
-                for (int cc = 0; cc < kBlk; ++cc)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t b = __byte_perm(wv[cc], 0, 0x4040 + 0x0101 * i);
-                        h[cc * 4 + i] =
-                            hmul2_u32(hsub2_u32(lop3_and_or(b, 0x00F0000Fu, 0x54006400u), zA), s2);
-                    }
+                dequant_words<kBlk>(st, a.p_off, a.s_off, a.z_off, c0, stage_zrow(k0, a.group, c0),
+                                    n, h);
                 if (ATMEM) {
                     // A stage s: lane n, 32-bit columns a_col0 + 64 s + 4 c .. +3 (k = 8c .. 8c+7)
                     const uint32_t ta = tmem_d + ((uint32_t)((warp & 3) * 32) << 16) +
@@ -381,24 +231,11 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         const int col = n0 + q * 32 + lane;              // weight column = TMEM lane
         const uint32_t taddr = tmem_d + ((uint32_t)(q * 32) << 16);
         const int epart = (warp - kDeqWarp0) / 4;        // warps of one quarter split the m chunks
-        for (int mc = 32 * epart; mc < a.tile_m; mc += 32 * kParts) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(taddr + mc, v);
-            tmem_ld_wait();
-            if (col < a.N) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int m = m0 + mc + i;
-                    if (mc + i < a.tile_m && m < a.M)
-                        a.out[(size_t)m * a.N + col] =
-                            __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
-                }
-            }
-        }
+        store_accumulator(taddr, col, m0, a.tile_m, 32 * epart, 32 * kParts, a.M, a.N, a.out);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem_d, a.tmem_cols);
+    if (warp == 1) tmem_dealloc<1>(tmem_d, a.tmem_cols);
 }
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
@@ -427,7 +264,7 @@ int *status_word() {
 }  // namespace
 
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group) {
-    (void)M;
+    if (cfg.variant == W4A16_PREFILL_PAIR) return prefill_pair_supported(cfg, M, N, K, group);
     const bool warps_ok = cfg.warps_k == 0 || cfg.warps_k == 4 || cfg.warps_k == 8 ||
                           cfg.warps_k == 16;
     return warps_ok && cfg.tile_m >= 16 && cfg.tile_m <= 256 && cfg.tile_m % 16 == 0 &&
@@ -435,6 +272,7 @@ bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int 
 }
 
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
+    if (cfg.variant == W4A16_PREFILL_PAIR) return launch_prefill_pair(a, cfg, stream);
     if (!prefill_config_supported(cfg, a.M, a.N, a.K, a.group)) return cudaErrorNotSupported;
     PrefillArgs pa;
     pa.out = a.out;
