@@ -142,9 +142,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         const uint32_t ring_u = smem_u32(ring);
         int s = 0, r = 0;
         for (int kt = 0; kt < KT; ++kt) {
-            if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
-                report_status(a.status, W4A16_ERR_TIMEOUT);
-            if (!mbar_wait_bounded(&aready[s], r & 1, a.timeout_ns))
+            // the dequant warps arrive on `aready` only after they saw the
+            // stage's copies land (`full`): one wait covers both
+            if (!mbar_spin_bounded(&aready[s], r & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
             tc_fence_after();
             const uint32_t a_addr = ring_u + (uint32_t)(s * a.stage_bytes);
