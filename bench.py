@@ -73,18 +73,34 @@ def load_peaks():
                     source="fallback")
 
 
-def source_sha():
+# The sources each workload's kernels are built from: a committed ncu summary
+# is used only while these are unchanged.
+KERNEL_SOURCES = {
+    "decode": ["api.cu", "common.cuh", "decode.cu", "decode_math.cuh", "decode_tma.cu",
+               "sm100_ptx.cuh", "tmap.cu", "tmap.cuh"],
+    "prefill": ["api.cu", "common.cuh", "prefill.cu", "prefill_pair.cu", "prefill_tile.cuh",
+                "sm100_ptx.cuh", "tcgen05.cuh", "tmap.cu", "tmap.cuh"],
+}
+
+
+def workload_kind(workload):
+    return "prefill" if workload.startswith("prefill") else "decode"
+
+
+def source_sha(kind):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_only_int4_codes_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(KERNEL_SOURCES[kind]):
+        h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    """Per-launch DRAM bytes of the workload's kernels from the committed ncu
     summary, or None when absent or taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_kernel_%s.txt" % workload)
+    kind = workload_kind(workload)
+    path = os.path.join(ROOT, "profiles", "%s_kernel_%s.txt" % (kind, workload))
     if not os.path.exists(path):
         return None
     kv = {}
@@ -92,7 +108,7 @@ def ncu_traffic(workload):
         if ":" in ln and not ln.startswith(" "):
             k, v = ln.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("kernel_source_sha") != source_sha():
+    if kv.get("kernel_source_sha") != source_sha(kind):
         return None
     try:
         return float(kv["dram_bytes_per_launch_mean"])
@@ -450,17 +466,30 @@ def run_ours(args, rank, local, world, pg):
     e2e_s = reduce_max(pg, e2e_s, dev)
     e2e_gbs = world * step_weight_bytes * e2e_steps / e2e_s / 1e9
 
-    # ---- roofline of the dominant kernel (every launch in the timed region is
-    # the decode kernel): algorithmic bytes per launch / mean launch time
+    # ---- roofline of the dominant kernel, from the timed region: every launch
+    # in it is one of the workload's GEMM kernels.  Decode shapes are bound by
+    # HBM (algorithmic bytes per launch / mean launch time); the prefill sweep
+    # by the fp16 tensor cores (fp16 and bf16 dense rates are equal on GB300).
     launches = len(calls_per_step) * args.steps
     mean_launch_s = ms * 1e-3 / launches
-    alg_bytes_launch = step_total_bytes / len(calls_per_step)
-    achieved = alg_bytes_launch / mean_launch_s / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": ncu_traffic(args.workload),
-                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
-                if peaks["source"] == "measured" else "fallback 6800 GB/s"}
+    if workload_kind(args.workload) == "prefill":
+        step_flops = sum(2.0 * M * s["K"] * s["N"] for s, M in calls_per_step)
+        achieved = step_flops / len(calls_per_step) / mean_launch_s / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1),
+                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                    "traffic": ncu_traffic(args.workload),
+                    "peak_source": (peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops_sustained: "
+                                    "a seconds-long step)") if peaks["source"] == "measured"
+                    else "fallback 1700 TFLOP/s sustained"}
+    else:
+        alg_bytes_launch = step_total_bytes / len(calls_per_step)
+        achieved = alg_bytes_launch / mean_launch_s / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "traffic": ncu_traffic(args.workload),
+                    "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+                    if peaks["source"] == "measured" else "fallback 6800 GB/s"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
