@@ -329,6 +329,11 @@ def run_ours(args, rank, local, world, pg):
     gemm_cfg = dict(pdl=not args.no_pdl)
     if args.variant != "auto":
         gemm_cfg.update(path="decode", variant=args.variant)
+    # MoE workloads: by default one grouped launch per (shape, M) covers all
+    # experts (w4a16_gemm_grouped); --no-grouped issues one call per expert
+    E = wl["experts"]
+    grouped = E > 1 and not args.no_grouped
+    group_cfg = dict(pdl=not args.no_pdl)
 
     # weights: quantize once per shape on the GPU (offline step), then R
     # byte-identical copies at distinct addresses per shape so that the
@@ -350,20 +355,46 @@ def run_ours(args, rank, local, world, pg):
             dq_copies = [wdq.clone() for _ in range(Rq)]
         xs = {}
         outs = {}
+        xg, og = {}, {}
         for M in wl["Ms"]:
             x = synth.activations(M, K, seed=synth.x_seed(wl["config"], M, shape_index=si))
             xs[M] = torch.from_numpy(x).to(dev)
             outs[M] = torch.empty((M, N), dtype=torch.float16, device=dev)
-        shapes.append(dict(K=K, N=N, copies=copies, dq=dq_copies, xs=xs, outs=outs))
+            if grouped:
+                # distinct activations per expert, stacked [E, M, K]
+                xg[M] = torch.from_numpy(np.stack([
+                    synth.activations(M, K, seed=synth.x_seed(wl["config"], M, expert=e,
+                                                              shape_index=si))
+                    for e in range(E)])).to(dev)
+                og[M] = torch.empty((E, M, N), dtype=torch.float16, device=dev)
+        shapes.append(dict(K=K, N=N, copies=copies, dq=dq_copies, xs=xs, outs=outs, xg=xg,
+                           og=og))
     torch.cuda.synchronize(dev)
 
-    calls_per_step = [(s, M) for s in shapes for M in wl["Ms"]] * wl["experts"]
-    step_weight_bytes = sum(weight_bytes(s["K"], s["N"]) for s, _ in calls_per_step)
-    step_total_bytes = sum(total_bytes(M, s["K"], s["N"]) for s, M in calls_per_step)
+    if grouped:
+        calls_per_step = [(s, M) for s in shapes for M in wl["Ms"]]
+        per_call = E                   # GEMMs (experts) per launch
+    else:
+        calls_per_step = [(s, M) for s in shapes for M in wl["Ms"]] * E
+        per_call = 1
+    step_weight_bytes = per_call * sum(weight_bytes(s["K"], s["N"]) for s, _ in calls_per_step)
+    step_total_bytes = per_call * sum(total_bytes(M, s["K"], s["N"]) for s, M in calls_per_step)
     counters = {id(s): 0 for s in shapes}
+
+    def grouped_call(s, M, api=False):
+        """One launch over E experts, each reading the next distinct weight copy."""
+        R = len(s["copies"])
+        i = counters[id(s)]
+        counters[id(s)] = (i + E) % R
+        ws = [s["copies"][(i + e) % R] for e in range(E)]
+        w4.gemm_grouped(s["xg"][M], [w[0] for w in ws], [w[1] for w in ws], [w[2] for w in ws],
+                        group=GROUP, out=s["og"][M], config=None if api else group_cfg)
 
     def one_step():
         for s, M in calls_per_step:
+            if grouped:
+                grouped_call(s, M)
+                continue
             i = counters[id(s)]
             counters[id(s)] = (i + 1) % len(s["copies"])
             w4.gemm_ex(s["xs"][M], *s["copies"][i], group=GROUP, out=s["outs"][M],
@@ -437,25 +468,43 @@ def run_ours(args, rank, local, world, pg):
                 tq = timed_replays(gq, stream, args.reps, Rq)
                 rec["cublas_fp16_us_per_call"] = round(statistics.median(tq), 3)
                 rec["speedup_vs_cublas"] = round(rec["cublas_fp16_us_per_call"] / us, 3)
+            if grouped:
+                # one grouped launch per E experts (all distinct weight copies)
+                nG = max(1, R // E)
+                gg = torch.cuda.CUDAGraph()
+                counters[id(s)] = 0
+                with torch.cuda.graph(gg, stream=stream):
+                    for _ in range(nG):
+                        grouped_call(s, M)
+                tg = statistics.median(timed_replays(gg, stream, args.reps, nG))
+                rec["grouped_us_per_%d_experts" % E] = round(tg, 3)
+                rec["grouped_weight_GBs"] = round(E * weight_bytes(K, N) / tg / 1e3, 1)
+                rec["grouped_roofline_frac"] = round(
+                    E * total_bytes(M, K, N) / (peaks["hbm_gbs"] * 1e9) / (tg * 1e-6), 4)
+                rec["grouped_speedup_vs_%d_calls" % E] = round(E * us / tg, 2)
             key = "M=%d" % M if len(shapes) == 1 else "K=%d,N=%d,M=%d" % (K, N, M)
             per_m[key] = rec
 
     # ---- end to end through the public API: x from pinned host memory and
     # the result back to pinned host memory every call; weights resident.
-    h2d = sum(2 * M * s["K"] for s, M in calls_per_step)
-    d2h = sum(2 * M * s["N"] for s, M in calls_per_step)
-    host_x = {(id(s), M): s["xs"][M].cpu().pin_memory() for s in shapes for M in wl["Ms"]}
-    host_o = {(id(s), M): torch.empty_like(s["outs"][M], device="cpu").pin_memory()
+    h2d = per_call * sum(2 * M * s["K"] for s, M in calls_per_step)
+    d2h = per_call * sum(2 * M * s["N"] for s, M in calls_per_step)
+    xkey, okey = ("xg", "og") if grouped else ("xs", "outs")
+    host_x = {(id(s), M): s[xkey][M].cpu().pin_memory() for s in shapes for M in wl["Ms"]}
+    host_o = {(id(s), M): torch.empty_like(s[okey][M], device="cpu").pin_memory()
               for s in shapes for M in wl["Ms"]}
     e2e_steps = max(3, min(args.steps, 50))
     with torch.cuda.stream(stream):
         def e2e_step():
             for s, M in calls_per_step:
-                i = counters[id(s)]
-                counters[id(s)] = (i + 1) % len(s["copies"])
-                s["xs"][M].copy_(host_x[(id(s), M)], non_blocking=True)
-                w4.gemm(s["xs"][M], *s["copies"][i], group=GROUP, out=s["outs"][M])
-                host_o[(id(s), M)].copy_(s["outs"][M], non_blocking=True)
+                s[xkey][M].copy_(host_x[(id(s), M)], non_blocking=True)
+                if grouped:
+                    grouped_call(s, M, api=True)
+                else:
+                    i = counters[id(s)]
+                    counters[id(s)] = (i + 1) % len(s["copies"])
+                    w4.gemm(s["xs"][M], *s["copies"][i], group=GROUP, out=s["outs"][M])
+                host_o[(id(s), M)].copy_(s[okey][M], non_blocking=True)
             stream.synchronize()
         e2e_step()
         barrier(pg)
@@ -513,6 +562,8 @@ def run_ours(args, rank, local, world, pg):
                              "(rotation footprint >= 3x L2)",
                        "timing": "one CUDA-graph replay of exactly `steps` steps, CUDA events",
                        "pdl": not args.no_pdl, "variant": args.variant,
+                       "launch": ("grouped: one launch per (shape, M) over %d experts" % E)
+                       if grouped else "one call per GEMM",
                        "parallelism": "replicas" if world > 1 else "1gpu"},
             "us_per_call": per_m,
             "roofline": roofline,
@@ -536,6 +587,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_square")
     ap.add_argument("--reps", type=int, default=20, help="repeats of the per-M timing graphs")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-grouped", action="store_true",
+                    help="MoE workload: one call per expert instead of one grouped launch")
     ap.add_argument("--variant", choices=["auto", "tma", "registers"], default="auto",
                     help="decode kernel variant (auto = the library's dispatch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")

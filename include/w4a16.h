@@ -155,6 +155,36 @@ W4A16_API w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed,
                            int M, int N, int K, int group, const w4a16_config *cfg,
                            cudaStream_t stream);
 
+/*
+ * Grouped GEMM: E independent products of one shape, out_e = x_e . W_e
+ * (the experts of a mixture-of-experts layer, each with its own weights and
+ * its own rows of x), in ONE kernel launch instead of E.  The pages measure
+ * MoE-expert projections among the shapes where the method wins (page "Beating
+ * FP16 with 4-bit Weights", section "Results") and name CUDA graphs and fewer
+ * launches as the next step for launch overhead (page "Triton Kernel Matches
+ * bitsandbytes", section "What's next"); this is the grouped entry that makes
+ * 64 small expert GEMMs one weight stream.
+ *   E          1 .. W4A16_MAX_EXPERTS
+ *   x, packed, scales, zeros, out
+ *              HOST arrays of E device pointers (the same layouts and
+ *              alignment rules as w4a16_gemm for each expert); the arrays are
+ *              read during the call and may be reused afterwards
+ *   M, N, K, group  the shape shared by all experts
+ *   cfg        NULL (automatic) or a decode-path configuration (registers
+ *              variant); the grouped kernel serves M <= 16, larger M runs the
+ *              experts' GEMMs one launch after another on the same stream
+ * Errors: W4A16_ERR_INVALID_ARG for E out of range or any NULL pointer,
+ * W4A16_ERR_MISALIGNED as w4a16_gemm, W4A16_ERR_UNSUPPORTED for a
+ * configuration with no kernel; nothing is enqueued on an error.
+ */
+#define W4A16_MAX_EXPERTS 64
+W4A16_API w4a16_status w4a16_gemm_grouped(int E, const uint16_t *const *x,
+                                const uint32_t *const *packed,
+                                const uint16_t *const *scales,
+                                const uint16_t *const *zeros, uint16_t *const *out,
+                                int M, int N, int K, int group, const w4a16_config *cfg,
+                                cudaStream_t stream);
+
 /* Host-only: the launch configuration w4a16_gemm_ex would use for this shape
  * with `request` (may be NULL) filled in.  Touches no GPU.  Returns the same
  * validation status the GEMM would (pointer checks excepted). */

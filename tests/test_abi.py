@@ -76,6 +76,28 @@ def test_gemm_rejects_before_touching_the_gpu(lib):
     assert lib.w4a16_gemm(8, 16, 16, 16, 16, 1, 256, 512, 128, None) == 3
 
 
+def test_grouped_rejects_before_touching_the_gpu(lib):
+    P = ctypes.c_void_p
+    good = (P * 2)(16, 32)
+    bad = (P * 2)(16, 8)          # second expert's pointer not 16-byte aligned
+    null = (P * 2)(16, None)
+    call = lambda E, t, u=good: lib.w4a16_gemm_grouped(E, t, u, u, u, u, 1, 256, 512, 128,
+                                                       None, None)
+    assert call(0, good) == 1                 # no experts
+    assert call(65, good) == 1                # above W4A16_MAX_EXPERTS
+    assert lib.w4a16_gemm_grouped(2, None, good, good, good, good, 1, 256, 512, 128,
+                                  None, None) == 1
+    assert call(2, null) == 1 and b"expert 1" in lib.w4a16_last_error()
+    assert call(2, bad) == 3 and b"expert 1" in lib.w4a16_last_error()
+    assert lib.w4a16_gemm_grouped(2, good, good, good, good, good, 1, 256, 500, 128,
+                                  None, None) == 1    # K not a multiple of the group
+    assert lib.w4a16_gemm_grouped(2, good, good, good, good, good, 0, 256, 512, 128,
+                                  None, None) == 0    # M == 0: nothing to do
+    tma = native.Config.make(dict(variant="tma"))
+    assert lib.w4a16_gemm_grouped(2, good, good, good, good, good, 1, 256, 512, 128,
+                                  ctypes.byref(tma), None) == 2
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 4096, 4096), (4, 14336, 4096),
                                    (8, 4096, 14336), (1, 768, 2048), (16, 2048, 768),
                                    (3, 260, 512), (40, 1024, 1024)])

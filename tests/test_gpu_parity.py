@@ -376,3 +376,60 @@ def test_bench_launch_config_full_size_sampled():
         torch.cuda.synchronize()
         ref = oracle.gemm(x, *ref_w, group=128)
         assert oracle.rel_err(out.cpu().numpy()[:, cols], ref) <= TOL
+
+
+# ----------------------------------------------------------- grouped (MoE) entry
+def expert_set(E, K, N, group, seed):
+    """E distinct seeded experts, quantized on the GPU; the oracle's codes
+    are checked bit-exact against them once per expert."""
+    dev, ref = [], []
+    for e in range(E):
+        _, d, r = quantized(K, N, group, seed + e, False)
+        dev.append(d)
+        ref.append(r)
+    return dev, ref
+
+
+@pytest.mark.parametrize("E,M", [(1, 1), (3, 5), (64, 1), (64, 16), (7, 9)])
+@pytest.mark.parametrize("K,N", [(2048, 768), (768, 2048), (1024, 260)])
+def test_gemm_grouped_matches_oracle_per_expert(E, M, K, N):
+    """One launch over E experts (own x, own weights, own out) equals the
+    oracle expert by expert."""
+    if E == 64 and (K, N) == (1024, 260):
+        pytest.skip("the 64-expert cases use the MoE shapes")
+    dev_w, ref_w = expert_set(E, K, N, 128, 900 + K)
+    xs = [synth.activations(M, K, seed=1000 * e + M) for e in range(E)]
+    out = w4.gemm_grouped([to_dev(x) for x in xs], [d[0] for d in dev_w], [d[1] for d in dev_w],
+                          [d[2] for d in dev_w], group=128)
+    torch.cuda.synchronize()
+    assert w4.kernel_status() == 0
+    for e in range(E):
+        ref = oracle.gemm(xs[e], *ref_w[e], group=128)
+        err = oracle.rel_err(out[e].cpu().numpy(), ref)
+        assert err <= TOL, (e, err)
+
+
+def test_gemm_grouped_equals_single_launches_bitwise():
+    """With the same explicit configuration, every expert of the grouped launch
+    is bit-identical to its own single launch (same tiles, same order)."""
+    E, M, K, N = 5, 4, 2048, 768
+    dev_w, _ = expert_set(E, K, N, 128, 77)
+    x = torch.stack([to_dev(synth.activations(M, K, seed=e)) for e in range(E)])
+    cfg = dict(path="decode", variant="registers", warps_n=1, warps_k=8, split_k=2, steps=4)
+    got = w4.gemm_grouped(x, torch.stack([d[0] for d in dev_w]), torch.stack([d[1] for d in dev_w]),
+                          torch.stack([d[2] for d in dev_w]), group=128, config=cfg)
+    for e in range(E):
+        one = w4.gemm_ex(x[e], *dev_w[e], group=128, config=cfg)
+        assert torch.equal(one, got[e]), e
+
+
+def test_gemm_grouped_prefill_sized_experts():
+    """M above the decode range: the experts run one launch after another."""
+    E, M, K, N = 2, 40, 1024, 512
+    dev_w, ref_w = expert_set(E, K, N, 128, 55)
+    xs = [synth.activations(M, K, seed=60 + e) for e in range(E)]
+    out = w4.gemm_grouped([to_dev(x) for x in xs], [d[0] for d in dev_w], [d[1] for d in dev_w],
+                          [d[2] for d in dev_w], group=128)
+    torch.cuda.synchronize()
+    for e in range(E):
+        assert oracle.rel_err(out[e].cpu().numpy(), oracle.gemm(xs[e], *ref_w[e], group=128)) <= TOL

@@ -12,8 +12,8 @@ binding is imported on first attribute access, so ``synth`` (input generation)
 can be used without the native library.
 """
 _NATIVE_NAMES = {
-    "W4A16Error", "gemm", "gemm_ex", "dequantize", "quantize_pack", "kernel_status",
-    "library_path", "load_library", "plan", "native",
+    "W4A16Error", "gemm", "gemm_ex", "gemm_grouped", "dequantize", "quantize_pack",
+    "kernel_status", "library_path", "load_library", "plan", "native",
 }
 
 

@@ -185,6 +185,29 @@ constexpr TableEntry kDecodeTable[] = {
     {768, 2048, 16, {1, 1, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
 };
 
+// Grouped launches of 64 experts (measured the same way, one grouped launch
+// per 64 distinct weight copies): registers variant, no split -- the experts
+// already give thousands of CTAs.
+constexpr TableEntry kGroupedTable[] = {
+    // K      N      M<=   path split warps_k warps_n steps tile flags variant
+    {2048, 768, 8, {1, 1, 4, 2, 16, 0, 0, W4A16_DECODE_REGISTERS}},
+    {2048, 768, 16, {1, 1, 4, 1, 16, 0, 0, W4A16_DECODE_REGISTERS}},
+    {768, 2048, 8, {1, 1, 2, 4, 12, 0, 0, W4A16_DECODE_REGISTERS}},
+    {768, 2048, 16, {1, 1, 2, 2, 12, 0, 0, W4A16_DECODE_REGISTERS}},
+};
+
+bool grouped_from_table(int M, int N, int K, int group, w4a16_config &c) {
+    if (group != 128 || c.split_k || c.warps_k || c.warps_n || c.steps) return false;
+    for (const TableEntry &e : kGroupedTable)
+        if (e.K == K && e.N == N && M <= e.m_max) {
+            const int flags = c.flags;
+            c = e.cfg;
+            c.flags = flags;
+            return true;
+        }
+    return false;
+}
+
 // Fill an all-automatic decode request from the table; false if no row fits.
 bool decode_from_table(int M, int N, int K, int group, w4a16_config &c) {
     if (group != 128 || c.variant != W4A16_DECODE_AUTO || c.split_k || c.warps_k || c.warps_n ||
@@ -347,6 +370,70 @@ w4a16_status w4a16_gemm(const uint16_t *x, const uint32_t *packed, const uint16_
                         const uint16_t *zeros, uint16_t *out, int M, int N, int K, int group,
                         cudaStream_t stream) {
     return w4a16_gemm_ex(x, packed, scales, zeros, out, M, N, K, group, nullptr, stream);
+}
+
+w4a16_status w4a16_gemm_grouped(int E, const uint16_t *const *x, const uint32_t *const *packed,
+                                const uint16_t *const *scales, const uint16_t *const *zeros,
+                                uint16_t *const *out, int M, int N, int K, int group,
+                                const w4a16_config *cfg, cudaStream_t stream) {
+    if (E < 1 || E > W4A16_MAX_EXPERTS)
+        return fail(W4A16_ERR_INVALID_ARG, "E=%d: 1..%d experts per grouped call", E,
+                    W4A16_MAX_EXPERTS);
+    if (!x || !packed || !scales || !zeros || !out)
+        return fail(W4A16_ERR_INVALID_ARG, "null pointer table");
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    for (int e = 0; e < E; ++e) {
+        if (!x[e] || !packed[e] || !scales[e] || !zeros[e] || !out[e])
+            return fail(W4A16_ERR_INVALID_ARG, "null pointer (expert %d)", e);
+        if (!aligned16(x[e]) || !aligned16(packed[e]) || !aligned16(scales[e]) ||
+            !aligned16(zeros[e]) || !aligned16(out[e]))
+            return fail(W4A16_ERR_MISALIGNED, "expert %d: x, packed, scales, zeros and out must "
+                        "be 16-byte aligned", e);
+    }
+    if (M == 0 || N == 0) return W4A16_OK;
+    if (M > kDecodeMaxM) {
+        // prefill-sized experts: one launch each (the tensor-core path is
+        // already compute-bound per expert)
+        for (int e = 0; e < E; ++e) {
+            st = w4a16_gemm_ex(x[e], packed[e], scales[e], zeros[e], out[e], M, N, K, group, cfg,
+                               stream);
+            if (st != W4A16_OK) return st;
+        }
+        return W4A16_OK;
+    }
+    w4a16_config c = cfg ? *cfg : w4a16_config{};
+    if ((c.path != W4A16_PATH_AUTO && c.path != W4A16_PATH_DECODE) ||
+        (c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_REGISTERS))
+        return fail(W4A16_ERR_UNSUPPORTED, "grouped GEMM: decode path, registers variant only");
+    c.path = W4A16_PATH_DECODE;
+    c.variant = W4A16_DECODE_REGISTERS;
+    // measured rows for the expert shapes; otherwise the E experts' column
+    // tiles fill the GPU together: plan as one GEMM with E * N columns
+    if (E == W4A16_MAX_EXPERTS) grouped_from_table(M, N, K, group, c);
+    plan_decode(M, N * E, K, group, device_info().sm_count, c);
+    if (!decode_config_supported(c, M) || c.steps % decode_steps_per_batch(group) != 0 ||
+        (long long)c.warps_k * c.steps * 4 * c.split_k < K / 8)
+        return fail(W4A16_ERR_UNSUPPORTED, "grouped decode configuration not available "
+                    "(split_k=%d warps_k=%d warps_n=%d steps=%d)",
+                    c.split_k, c.warps_k, c.warps_n, c.steps);
+    GroupedGemmArgs a;
+    a.E = E;
+    for (int e = 0; e < E; ++e) {
+        a.x[e] = x[e];
+        a.packed[e] = packed[e];
+        a.scales[e] = scales[e];
+        a.zeros[e] = zeros[e];
+        a.out[e] = out[e];
+    }
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.group = group;
+    cudaError_t err = launch_decode_grouped(a, c, stream);
+    if (err == cudaErrorNotSupported)
+        return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
+    return err == cudaSuccess ? W4A16_OK : cuda_fail(err, "grouped gemm launch");
 }
 
 w4a16_status w4a16_get_kernel_status(cudaStream_t stream) {

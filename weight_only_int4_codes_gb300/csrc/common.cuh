@@ -30,6 +30,19 @@ struct GemmArgs {
     int M, N, K, group;
 };
 
+// A grouped launch: E GEMMs of one shape (MoE experts), each with its own
+// x, weights and out.  The pointer tables travel in the kernel parameters.
+constexpr int kMaxExperts = W4A16_MAX_EXPERTS;
+struct GroupedGemmArgs {
+    int E;
+    const uint16_t *x[kMaxExperts];
+    const uint32_t *packed[kMaxExperts];
+    const uint16_t *scales[kMaxExperts];
+    const uint16_t *zeros[kMaxExperts];
+    uint16_t *out[kMaxExperts];
+    int M, N, K, group;
+};
+
 // Each returns cudaSuccess or the launch error; they never synchronize.
 cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group,
                                  uint32_t *packed, uint16_t *scales, uint16_t *zeros,
@@ -40,6 +53,9 @@ cudaError_t launch_dequantize(const uint32_t *packed, const uint16_t *scales,
 // Decode path: cfg already fully resolved (split_k, warps_k, warps_n, steps > 0).
 // Returns cudaErrorNotSupported for a configuration with no compiled kernel.
 cudaError_t launch_decode(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
+// Grouped decode (registers variant, M <= 16): one launch over all E GEMMs.
+cudaError_t launch_decode_grouped(const GroupedGemmArgs &a, const w4a16_config &cfg,
+                                  cudaStream_t stream);
 bool decode_config_supported(const w4a16_config &cfg, int M);
 int decode_steps_per_batch(int group);
 // Resident CTAs per SM of the decode kernel that `cfg` selects (occupancy

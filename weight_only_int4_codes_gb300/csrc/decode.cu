@@ -147,18 +147,33 @@ __device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batc
     flush_group_split<NT>(acc, gacc, k);
 }
 
-// Grid: (ceil(N / (32*WN)), split, ceil(M / 16)); cluster (1, split, 1).
+// The operands of one GEMM of a launch (one expert of a grouped launch).
+struct Operands {
+    const uint16_t *x;
+    const uint32_t *packed;
+    const uint16_t *scales;
+    const uint16_t *zeros;
+    uint16_t *out;
+};
+
+// Up to kMaxExperts weight sets and activations of one grouped launch, passed
+// by value in the kernel's parameter block (nothing is allocated per call).
+struct ExpertTable {
+    Operands e[kMaxExperts];
+};
+
+// One CTA's share of one GEMM: column tile blockIdx.x, K slice blockIdx.y,
+// 16-row chunk `mchunk` of x.
 // Block: 32*WN*WK threads; dynamic shared memory (WK + 1) * 16 * 32*WN floats.
 template <int NT, int WN, int WK, int U>
-__global__ void __launch_bounds__(32 * WN * WK)
-decode_kernel(const DecodeArgs a)
+__device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands &o, int mchunk)
 {
     extern __shared__ float smem[];
     constexpr int BN = 32 * WN;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wn = warp % WN, wk = warp / WN;
     const int g = lane >> 2, t = lane & 3;
-    const int m_base = blockIdx.z * 16;
+    const int m_base = mchunk * 16;
     const int Mc = min(16, a.M - m_base);
     const int col0 = blockIdx.x * BN + wn * 32 + 4 * g;
     const bool col_ok = col0 < a.N;                 // N % 4 == 0: all 4 columns valid
@@ -170,9 +185,9 @@ decode_kernel(const DecodeArgs a)
 
     const uint64_t pol = evict_first_policy();
     const size_t wstride = (size_t)4 * a.N;         // one step = 4 packed rows
-    const uint32_t *wptr = a.packed + (size_t)(row0 + t) * a.N + col0;
-    const uint16_t *sptr = a.scales + col0;
-    const uint16_t *zptr = a.zeros + col0;
+    const uint32_t *wptr = o.packed + (size_t)(row0 + t) * a.N + col0;
+    const uint16_t *sptr = o.scales + col0;
+    const uint16_t *zptr = o.zeros + col0;
     // group row of batch b: (8 * (row0 + 4*U*b)) / group
     const int rows_per_group = a.group >> 3;
 
@@ -186,8 +201,8 @@ decode_kernel(const DecodeArgs a)
 
     const int m0 = g, m1 = 8 + g;
     const bool m0_ok = m0 < Mc, m1_ok = m1 < Mc;
-    const uint16_t *xrow0 = a.x + (size_t)(m_base + (m0_ok ? m0 : 0)) * a.K;
-    const uint16_t *xrow1 = a.x + (size_t)(m_base + (m1_ok ? m1 : 0)) * a.K;
+    const uint16_t *xrow0 = o.x + (size_t)(m_base + (m0_ok ? m0 : 0)) * a.K;
+    const uint16_t *xrow1 = o.x + (size_t)(m_base + (m1_ok ? m1 : 0)) * a.K;
 
     Batch<U> ba, bb;
     if (nbatch > 0) {
@@ -242,7 +257,7 @@ decode_kernel(const DecodeArgs a)
         if (a.split == 1) {
             const int col = blockIdx.x * BN + c;
             if (col < a.N)
-                a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
+                o.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
         } else {
             part[e] = v;
         }
@@ -262,9 +277,29 @@ decode_kernel(const DecodeArgs a)
         const int m = e / BN, c = e - m * BN;
         const int col = blockIdx.x * BN + c;
         if (col < a.N)
-            a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
+            o.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
     }
     cluster.sync();   // keep this CTA's shared memory alive until all peers have read it
+}
+
+// Grid: (ceil(N / (32*WN)), split, ceil(M / 16)); cluster (1, split, 1).
+template <int NT, int WN, int WK, int U>
+__global__ void __launch_bounds__(32 * WN * WK)
+decode_kernel(const DecodeArgs a)
+{
+    const Operands o{a.x, a.packed, a.scales, a.zeros, a.out};
+    decode_tile<NT, WN, WK, U>(a, o, blockIdx.z);
+}
+
+// Grouped launch of E GEMMs of one shape (MoE experts): grid z = E * ceil(M / 16),
+// expert e = z / mchunks.  Same tiles, same arithmetic, one launch.
+template <int NT, int WN, int WK, int U>
+__global__ void __launch_bounds__(32 * WN * WK)
+decode_grouped_kernel(const DecodeArgs a, const ExpertTable tab)
+{
+    const int mchunks = (a.M + 15) >> 4;
+    const int e = blockIdx.z / mchunks;
+    decode_tile<NT, WN, WK, U>(a, tab.e[e], blockIdx.z - e * mchunks);
 }
 
 template <int NT, int WN, int WK, int U>
@@ -293,6 +328,45 @@ cudaError_t launch_one(const DecodeArgs &da, int strips, int mchunks, bool pdl,
     lc.attrs = attrs;
     lc.numAttrs = na;
     return cudaLaunchKernelEx(&lc, decode_kernel<NT, WN, WK, U>, da);
+}
+
+template <int NT, int WN, int WK, int U>
+cudaError_t launch_grouped_one(const DecodeArgs &da, const ExpertTable &tab, int strips, int zdim,
+                               bool pdl, cudaStream_t stream) {
+    constexpr int BN = 32 * WN;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(strips, da.split, zdim);
+    lc.blockDim = dim3(32 * WN * WK, 1, 1);
+    lc.dynamicSmemBytes = (size_t)(WK + 1) * 16 * BN * sizeof(float);
+    lc.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (da.split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = da.split;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    lc.attrs = attrs;
+    lc.numAttrs = na;
+    return cudaLaunchKernelEx(&lc, decode_grouped_kernel<NT, WN, WK, U>, da, tab);
+}
+
+template <int NT, int U>
+cudaError_t launch_grouped_shape(const DecodeArgs &da, const ExpertTable &tab, int wn, int wk,
+                                 int strips, int zdim, bool pdl, cudaStream_t s) {
+    if (wn == 1 && wk == 4) return launch_grouped_one<NT, 1, 4, U>(da, tab, strips, zdim, pdl, s);
+    if (wn == 1 && wk == 8) return launch_grouped_one<NT, 1, 8, U>(da, tab, strips, zdim, pdl, s);
+    if (wn == 2 && wk == 4) return launch_grouped_one<NT, 2, 4, U>(da, tab, strips, zdim, pdl, s);
+    if (wn == 4 && wk == 2) return launch_grouped_one<NT, 4, 2, U>(da, tab, strips, zdim, pdl, s);
+    if (wn == 2 && wk == 2) return launch_grouped_one<NT, 2, 2, U>(da, tab, strips, zdim, pdl, s);
+    return cudaErrorNotSupported;
 }
 
 template <int NT, int U>
@@ -400,6 +474,38 @@ cudaError_t launch_decode(const GemmArgs &a, const w4a16_config &cfg, cudaStream
         return nt2 ? launch_shape<2, 1>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream)
                    : launch_shape<1, 1>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream);
     }
+}
+
+cudaError_t launch_decode_grouped(const GroupedGemmArgs &a, const w4a16_config &cfg,
+                                  cudaStream_t stream) {
+    if (!decode_config_supported(cfg, a.M) || a.E < 1 || a.E > kMaxExperts || a.M > 16)
+        return cudaErrorNotSupported;
+    const int U = steps_per_batch(a.group);
+    if (cfg.steps % U != 0) return cudaErrorNotSupported;
+    DecodeArgs da = {};
+    da.M = a.M;
+    da.N = a.N;
+    da.K = a.K;
+    da.group = a.group;
+    da.steps = cfg.steps;
+    da.rows_per_cta = cfg.warps_k * cfg.steps * 4;
+    da.split = cfg.split_k;
+    if ((long long)da.rows_per_cta * da.split < a.K / 8) return cudaErrorInvalidValue;
+    ExpertTable tab = {};
+    for (int e = 0; e < a.E; ++e)
+        tab.e[e] = Operands{a.x[e], a.packed[e], a.scales[e], a.zeros[e], a.out[e]};
+    const int strips = (a.N + 32 * cfg.warps_n - 1) / (32 * cfg.warps_n);
+    const int zdim = a.E;                    // M <= 16: one 16-row chunk per expert
+    const bool pdl = (cfg.flags & W4A16_FLAG_PDL) != 0;
+    const bool nt2 = a.M > 8;
+#define W4A16_GROUPED(NT_, U_) \
+    launch_grouped_shape<NT_, U_>(da, tab, cfg.warps_n, cfg.warps_k, strips, zdim, pdl, stream)
+    switch (U) {
+    case 4: return nt2 ? W4A16_GROUPED(2, 4) : W4A16_GROUPED(1, 4);
+    case 2: return nt2 ? W4A16_GROUPED(2, 2) : W4A16_GROUPED(1, 2);
+    default: return nt2 ? W4A16_GROUPED(2, 1) : W4A16_GROUPED(1, 1);
+    }
+#undef W4A16_GROUPED
 }
 
 int decode_steps_per_batch(int group) { return steps_per_batch(group); }

@@ -87,6 +87,7 @@ def load_library():
             "w4a16_gemm": [P, P, P, P, P, I, I, I, I, P],
             "w4a16_gemm_ex": [P, P, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_plan": [I, I, I, I, ctypes.POINTER(Config), ctypes.POINTER(Config)],
+            "w4a16_gemm_grouped": [I, P, P, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_get_kernel_status": [P],
             "w4a16_last_error": [],
             "w4a16_version": [],
@@ -175,6 +176,46 @@ def gemm(x, packed, scales, zeros, group: int = 128, out=None, stream=None):
         _dev(x, "x", torch.float16), _dev(packed, "packed", torch.int32),
         _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
         _dev(out, "out", torch.float16), M, N, K, group, _stream_handle(stream)))
+    return out
+
+
+MAX_EXPERTS = 64
+
+
+def _experts(t, name, dtype):
+    """A stacked tensor [E, ...] or a sequence of E tensors -> list of device pointers."""
+    if isinstance(t, torch.Tensor):
+        return [_dev(t[e], name, dtype) for e in range(t.shape[0])]
+    return [_dev(v, name, dtype) for v in t]
+
+
+def gemm_grouped(xs, packed, scales, zeros, group: int = 128, out=None, config=None,
+                 stream=None):
+    """E expert GEMMs of one shape in one launch: out[e] = xs[e] @ dequant(packed[e], ...).
+    Each argument is a stacked tensor with a leading expert dimension or a
+    sequence of per-expert tensors; ``out`` likewise (allocated stacked if None
+    and the experts' slices stay 16-byte aligned, else as a list)."""
+    E = xs.shape[0] if isinstance(xs, torch.Tensor) else len(xs)
+    x0 = xs[0]
+    M, K = x0.shape
+    N = packed[0].shape[1]
+    if out is None:
+        # stacked when every expert's slice stays 16-byte aligned, else one
+        # tensor per expert
+        if (M * N) % 8 == 0:
+            out = torch.empty((E, M, N), dtype=torch.float16, device=x0.device)
+        else:
+            out = [torch.empty((M, N), dtype=torch.float16, device=x0.device) for _ in range(E)]
+    ptrs = [_experts(xs, "x", torch.float16), _experts(packed, "packed", torch.int32),
+            _experts(scales, "scales", torch.float16), _experts(zeros, "zeros", torch.float16),
+            _experts(out, "out", torch.float16)]
+    if any(len(p) != E for p in ptrs):
+        raise ValueError("every argument needs %d experts" % E)
+    tables = [(ctypes.c_void_p * E)(*p) for p in ptrs]
+    cfg = Config.make(config)
+    _check(load_library().w4a16_gemm_grouped(
+        E, *[ctypes.cast(t, ctypes.c_void_p) for t in tables], M, N, K, group,
+        ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
     return out
 
 
