@@ -433,3 +433,56 @@ def test_gemm_grouped_prefill_sized_experts():
     torch.cuda.synchronize()
     for e in range(E):
         assert oracle.rel_err(out[e].cpu().numpy(), oracle.gemm(xs[e], *ref_w[e], group=128)) <= TOL
+
+
+# ----------------------------------------------- dependent calls (PDL chains)
+@pytest.mark.parametrize("variant", ["registers", "tma"])
+@pytest.mark.parametrize("M", [1, 16])
+def test_pdl_chain_reads_the_previous_output(variant, M):
+    """A chain of square GEMMs where every call's x is the previous call's out,
+    launched with programmatic dependent launch inside one CUDA graph: each
+    call may start before its predecessor ends, and must still read the
+    finished output (griddepcontrol.wait before touching x, no stale cache).
+    Compared with the same chain launched without PDL, bit for bit, and the
+    first link with the oracle."""
+    K = N = 1024
+    L = 12
+    ws = []
+    for i in range(L):
+        # std 0.03: x stays O(1) from link to link (sqrt(1024) * 0.03 ~ 1)
+        W = (synth.weight(K, N, seed=700 + i) * np.float16(1.5)).astype(np.float16)
+        ws.append(w4.quantize_pack(to_dev(W), 128))
+        if i == 0:
+            ref_w0 = oracle.quantize_pack(W, 128)
+    x0 = to_dev(synth.activations(M, K, seed=5))
+    cfg = dict(path="decode", variant=variant)
+    bufs = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _ in range(L)]
+
+    def chain(pdl):
+        stream = torch.cuda.Stream()
+        c = dict(cfg, pdl=pdl)
+        with torch.cuda.stream(stream):
+            w4.gemm_ex(x0, *ws[0], out=bufs[0], config=c)       # warm-up, outside capture
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                x = x0
+                for i in range(L):
+                    w4.gemm_ex(x, *ws[i], out=bufs[i], config=c)
+                    x = bufs[i]
+            for b in bufs:
+                b.fill_(float("nan"))
+            g.replay()
+            stream.synchronize()
+        return [b.clone() for b in bufs]
+
+    plain = chain(False)
+    assert w4.kernel_status() == 0
+    ref0 = oracle.gemm(x0.cpu().numpy(), *ref_w0, group=128)
+    assert oracle.rel_err(plain[0].cpu().numpy(), ref0) <= TOL
+    for rep in range(3):
+        dep = chain(True)
+        assert w4.kernel_status() == 0
+        for i in range(L):
+            assert torch.equal(dep[i], plain[i]), (rep, i)
+    assert torch.isfinite(plain[-1].float()).all()
