@@ -66,7 +66,7 @@ template <int NDQ, bool ATMEM>
 __global__ void __launch_bounds__(32 * (NDQ + 2), 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
-                       const PrefillArgs a)
+                       const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
@@ -87,6 +87,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_s);
         prefetch_tmap(&tm_z);
+        prefetch_tmap(&tm_o);
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&aready[i], NDQ);
@@ -228,10 +229,19 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             report_status(a.status, W4A16_ERR_TIMEOUT);
         tc_fence_after();
         const int q = warp & 3;                          // TMEM lane quarter of this warp
-        const int col = n0 + q * 32 + lane;              // weight column = TMEM lane
         const uint32_t taddr = tmem_d + ((uint32_t)(q * 32) << 16);
         const int epart = (warp - kDeqWarp0) / 4;        // warps of one quarter split the m chunks
-        store_accumulator(taddr, col, m0, a.tile_m, 32 * epart, 32 * kParts, a.M, a.N, a.out);
+        // every copy has landed and every MMA has read its operands: the ring
+        // holds the fp16 output tile [tile_m][128], stored by one TMA copy
+        // (rows past M and columns past N are clipped by the tensor map)
+        stage_accumulator(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart, 32 * kParts);
+        fence_proxy_async_smem();
+        named_bar_sync(1, NDQ * 32);
+        if (warp == kDeqWarp0 && lane == 0) {
+            tma_store_2d(&tm_o, ring, n0, m0);
+            bulk_commit();
+            bulk_wait_all();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -244,7 +254,7 @@ template <int NDQ, bool ATMEM>
 cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                   const CUtensorMap &tx, const CUtensorMap &tw,
                                   const CUtensorMap &ts, const CUtensorMap &tz,
-                                  const PrefillArgs &pa) {
+                                  const CUtensorMap &to, const PrefillArgs &pa) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
@@ -252,7 +262,8 @@ cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr != cudaSuccess) return attr;
-    prefill_tcgen05_kernel<NDQ, ATMEM><<<grid, 32 * (NDQ + 2), smem, stream>>>(tx, tw, ts, tz, pa);
+    prefill_tcgen05_kernel<NDQ, ATMEM><<<grid, 32 * (NDQ + 2), smem, stream>>>(tx, tw, ts, tz, to,
+                                                                              pa);
     return cudaGetLastError();
 }
 
@@ -322,9 +333,11 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     const uint64_t x_dims[3] = {(uint64_t)kChunkK, (uint64_t)a.M, (uint64_t)(a.K / kChunkK)};
     const uint64_t x_strides[2] = {(uint64_t)a.K * 2, (uint64_t)kChunkK * 2};
     const uint32_t x_box[3] = {(uint32_t)kChunkK, (uint32_t)pa.tile_m, (uint32_t)kChunks};
-    CUtensorMap tx, tw, ts, tz;
+    CUtensorMap tx, tw, ts, tz, to;
     if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, x_dims, x_strides, x_box,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.out, a.N, a.M, (uint64_t)a.N * 2,
+                      kTileN, pa.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, a.K / 8,
                       (uint64_t)a.N * 4, kTileN, kPackedRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
@@ -336,7 +349,8 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     const int mtiles = (a.M + pa.tile_m - 1) / pa.tile_m;
     if (mtiles > 65535) return cudaErrorInvalidValue;
     dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, 1);
-#define W4A16_PF(NDQ_, AT_) launch_prefill_kernel<NDQ_, AT_>(grid, smem, stream, tx, tw, ts, tz, pa)
+#define W4A16_PF(NDQ_, AT_) \
+    launch_prefill_kernel<NDQ_, AT_>(grid, smem, stream, tx, tw, ts, tz, to, pa)
     if (atmem) {
         switch (ndq) {
         case 4: return W4A16_PF(4, true);

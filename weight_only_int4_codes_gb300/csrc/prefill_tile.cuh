@@ -83,4 +83,26 @@ __device__ __forceinline__ void store_accumulator(uint32_t taddr, int col, int m
     }
 }
 
+// Staged epilogue of one warp: its 32 TMEM lanes (weight columns n = lane
+// base + lane, one per thread) for the accumulator columns mc = first, first +
+// step, ... (rows of x) become an fp16 tile [tile_m][128] in shared memory at
+// `tile` (one 256-byte row per row of x), ready for one TMA store.  A warp's
+// 2-byte stores for one row cover 64 contiguous bytes.
+__device__ __forceinline__ void stage_accumulator(uint32_t taddr, uint32_t tile, int n, int tile_m,
+                                                  int first, int step) {
+    for (int mc = first; mc < tile_m; mc += step) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + mc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (mc + i < tile_m) {
+                const uint16_t h = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(tile + ((mc + i) * kTileN + n) * 2),
+                             "h"(h)
+                             : "memory");
+            }
+    }
+}
+
 }  // namespace w4a16
