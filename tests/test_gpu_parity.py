@@ -248,14 +248,17 @@ def test_gemm_prefill_cta_pair_groups(K, group):
     check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", variant="pair", tile_m=144))
 
 
+@pytest.mark.parametrize("tile_m", [112, 256])
 @pytest.mark.parametrize("K,group", [(1088, 64), (1152, 192), (576, 192), (960, 320), (1024, 512)])
-def test_gemm_prefill_group_boundaries(K, group):
+def test_gemm_prefill_group_boundaries(K, group, tile_m):
     """Stages are 128 k deep: groups of 64 (two scale rows per stage), groups
-    that start mid-stage (192, 320) and K with a half last stage (K % 128 == 64)."""
-    N, M = 264, 97
+    that start mid-stage (192, 320) and K with a half last stage (K % 128 == 64);
+    tile_m = 112 runs the one-ring kernel, 256 the split-ring kernel (x in
+    64-k chunks, so an odd chunk count ends in half a stage)."""
+    N, M = 264, 297
     _, dev_w, ref_w = quantized(K, N, group, 17 + group, True)
     x = synth.activations(M, K, seed=18 + K)
-    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=112))
+    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=tile_m))
 
 
 @pytest.mark.parametrize("group", [64, 256])

@@ -248,6 +248,222 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     if (warp == 1) tmem_dealloc<1>(tmem_d, a.tmem_cols);
 }
 
+// ---------------------------------------------------------------------------
+// Split-ring kernel (the default, A in tensor memory).  The x tile and the
+// weights travel in separate rings so that each is refilled as soon as its
+// own consumer is done with it:
+//   x ring      xs slots of one 64-k chunk of the x tile (tile_m x 128 bytes,
+//               128B-swizzled); filled by warp 0, freed by the MMAs' commit;
+//   weight ring ws slots of one 128-k stage (16 x 128 packed words, scale and
+//               zero rows); filled by warp 2, freed by the dequantizing warps
+//               as soon as they have the words in registers;
+//   A slots     as tensor-memory slots of one dequantized 128-k stage
+//               (64 columns); written by the dequantizing warps, freed by the
+//               MMAs' commit.
+// With one ring per stage the x slot of a stage could only be refilled after
+// its MMAs, so at tile_m = 256 (73 KB per stage, three stages) the copies ran
+// about two stages ahead -- less than their latency.  Here x is refilled in
+// 32 KB chunks (six in flight) and the weights run further ahead on their own.
+// Warps: 0 x producer, 1 tensor-memory owner and MMA issuer, 2 weight
+// producer, 3.. dequantization and epilogue.
+constexpr int kSplitDeq0 = 3;
+constexpr int kSplitMinTileM = 192;     // measured crossover (128: one ring is faster)
+
+struct SplitArgs {
+    int *status;
+    int M, N, K, group;
+    int tile_m;
+    int xs, ws, as;            // slots of the x ring, the weight ring, the A ring
+    int x_chunk_bytes;         // tile_m * 128
+    int w_off;                 // offset of the weight ring (after the x ring)
+    int w_stage_bytes;
+    int s_off, z_off;          // scale / zero rows inside a weight stage (packed at 0)
+    int sz_rows;
+    int w_tx;                  // bytes one weight stage's copies deliver
+    int tmem_cols, a_col0;
+    unsigned long long timeout_ns;
+};
+
+template <int NDQ>
+__global__ void __launch_bounds__(32 * (NDQ + 3), 1)
+prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
+                     const __grid_constant__ CUtensorMap tm_o, const SplitArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *wring = ring + a.w_off;
+    uint64_t *xfull = reinterpret_cast<uint64_t *>(wring + a.ws * a.w_stage_bytes);
+    uint64_t *xempty = xfull + a.xs;
+    uint64_t *wfull = xempty + a.xs;
+    uint64_t *wempty = wfull + a.ws;
+    uint64_t *aready = wempty + a.ws;
+    uint64_t *aempty = aready + a.as;
+    uint64_t *accum = aempty + a.as;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTileN;
+    const int m0 = blockIdx.y * a.tile_m;
+    const int KT = (a.K + kStageK - 1) / kStageK;      // 128-k stages (a last half stage reads zeros)
+    const int KC = a.K / kChunkK;                      // 64-k x chunks
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_s);
+        prefetch_tmap(&tm_z);
+        prefetch_tmap(&tm_o);
+        for (int i = 0; i < a.xs; ++i) {
+            mbar_init(&xfull[i], 1);
+            mbar_init(&xempty[i], 1);
+        }
+        for (int i = 0; i < a.ws; ++i) {
+            mbar_init(&wfull[i], 1);
+            mbar_init(&wempty[i], NDQ);
+        }
+        for (int i = 0; i < a.as; ++i) {
+            mbar_init(&aready[i], NDQ);
+            mbar_init(&aempty[i], 1);
+        }
+        mbar_init(accum, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_u32(tmem_slot), a.tmem_cols);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ x producer (lane 0 issues)
+        const uint64_t pol_x = l2_evict_last_policy();
+        int s = 0, r = 0;
+        for (int c = 0; c < KC; ++c) {
+            if (r > 0 && !mbar_spin_bounded(&xempty[s], (r - 1) & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&xfull[s], (uint32_t)a.x_chunk_bytes);
+                tma_load_2d(ring + s * a.x_chunk_bytes, &tm_x, &xfull[s], c * kChunkK, m0, pol_x);
+            }
+            __syncwarp();
+            if (++s == a.xs) { s = 0; ++r; }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ weight producer
+        const uint64_t pol_w = l2_evict_first_policy();
+        int s = 0, r = 0, grow = 0, gnext = a.group;
+        for (int kt = 0; kt < KT; ++kt) {
+            const int k0 = kt * kStageK;
+            while (k0 >= gnext) { ++grow; gnext += a.group; }
+            if (r > 0 && !mbar_wait_bounded(&wempty[s], (r - 1) & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            if (lane == 0) {
+                uint8_t *st = wring + s * a.w_stage_bytes;
+                mbar_arrive_expect_tx(&wfull[s], (uint32_t)a.w_tx);
+                tma_load_2d(st, &tm_w, &wfull[s], n0, k0 / 8, pol_w);
+                tma_load_2d(st + a.s_off, &tm_s, &wfull[s], n0, grow, pol_w);
+                tma_load_2d(st + a.z_off, &tm_z, &wfull[s], n0, grow, pol_w);
+            }
+            __syncwarp();
+            if (++s == a.ws) { s = 0; ++r; }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (lane 0 issues)
+        const uint32_t idesc = idesc_f16(128, a.tile_m);
+        const uint32_t tmem_u = __shfl_sync(0xffffffffu, tmem_d, 0);
+        const uint32_t ring_u = smem_u32(ring);
+        int sa = 0, ra = 0, sx = 0, rx = 0;
+        for (int kt = 0; kt < KT; ++kt) {
+            if (!mbar_spin_bounded(&aready[sa], ra & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            const uint32_t a_tmem = tmem_u + (uint32_t)(a.a_col0 + sa * (kStageK / 2));
+#pragma unroll
+            for (int h = 0; h < kChunks; ++h) {
+                if (kt * kChunks + h >= KC) break;            // half last stage
+                if (!mbar_spin_bounded(&xfull[sx], rx & 1, a.timeout_ns))
+                    report_status(a.status, W4A16_ERR_TIMEOUT);
+                tc_fence_after();
+                const uint64_t b_desc = smem_desc_sw128(ring_u + (uint32_t)(sx * a.x_chunk_bytes));
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < kChunkK / 16; ++kk)
+                        umma_f16_ts<1>(tmem_u, a_tmem + h * (kChunkK / 2) + kk * 8, b_desc + kk * 2,
+                                       idesc, (kt | h | kk) != 0);
+                    umma_commit<1>(&xempty[sx]);
+                }
+                __syncwarp();
+                if (++sx == a.xs) { sx = 0; ++rx; }
+            }
+            if (lane == 0) umma_commit<1>(&aempty[sa]);
+            __syncwarp();
+            if (++sa == a.as) { sa = 0; ++ra; }
+        }
+        if (lane == 0) umma_commit<1>(accum);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ dequant
+        constexpr int kParts = NDQ / 4;                   // warps per lane quarter
+        static_assert(kPackedRows % kParts == 0, "packed rows must split evenly");
+        constexpr int kRowsPer = kPackedRows / kParts;    // packed rows per thread
+        constexpr int kBlk = kRowsPer >= 8 ? 8 : 4;       // words per TMEM store
+        // a warp may only reach its lane quarter (warp % 4): the column a
+        // thread dequantizes is the TMEM lane of that quarter
+        const int n = (warp & 3) * 32 + lane;
+        const int part = (warp - kSplitDeq0) / 4;
+        const uint32_t lane_base = tmem_d + ((uint32_t)((warp & 3) * 32) << 16);
+        int sw = 0, rw = 0, sa = 0, ra = 0;
+        for (int kt = 0; kt < KT; ++kt) {
+            if (!mbar_wait_bounded(&wfull[sw], rw & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            // the A slot is free once the MMAs that read it last have completed
+            if (ra > 0 && !mbar_wait_bounded(&aempty[sa], (ra - 1) & 1, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            tc_fence_after();
+            const uint32_t st = smem_u32(wring + sw * a.w_stage_bytes);
+            const int k0 = kt * kStageK;
+#pragma unroll
+            for (int b0 = 0; b0 < kRowsPer; b0 += kBlk) {
+                const int c0 = part * kRowsPer + b0;
+                uint32_t h[kBlk * 4];
+                dequant_words<kBlk>(st, 0, a.s_off, a.z_off, c0, stage_zrow(k0, a.group, c0), n, h);
+                tmem_st_32x32b<kBlk * 4>(lane_base + (uint32_t)(a.a_col0 + sa * (kStageK / 2) + c0 * 4),
+                                         h);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&wempty[sw]);     // the words are in registers (and stored)
+                mbar_arrive(&aready[sa]);
+            }
+            if (++sw == a.ws) { sw = 0; ++rw; }
+            if (++sa == a.as) { sa = 0; ++ra; }
+        }
+        // ------------------------------------------------ epilogue
+        if (!mbar_wait_bounded(accum, 0, a.timeout_ns))
+            report_status(a.status, W4A16_ERR_TIMEOUT);
+        tc_fence_after();
+        // every copy has landed and every MMA has read its operands: the x
+        // ring holds the fp16 output tile [tile_m][128] for one TMA store
+        stage_accumulator(lane_base, smem_u32(ring), n, a.tile_m, 32 * part, 32 * kParts);
+        fence_proxy_async_smem();
+        named_bar_sync(1, NDQ * 32);
+        if (warp == kSplitDeq0 && lane == 0) {
+            tma_store_2d(&tm_o, ring, n0, m0);
+            bulk_commit();
+            bulk_wait_all();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc<1>(tmem_d, a.tmem_cols);
+}
+
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 template <int NDQ, bool ATMEM>
@@ -267,6 +483,22 @@ cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
     return cudaGetLastError();
 }
 
+template <int NDQ>
+cudaError_t launch_split_kernel(dim3 grid, size_t smem, cudaStream_t stream,
+                                const CUtensorMap &tx, const CUtensorMap &tw,
+                                const CUtensorMap &ts, const CUtensorMap &tz,
+                                const CUtensorMap &to, const SplitArgs &sa) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(prefill_split_kernel<NDQ>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr != cudaSuccess) return attr;
+    prefill_split_kernel<NDQ><<<grid, 32 * (NDQ + 3), smem, stream>>>(tx, tw, ts, tz, to, sa);
+    return cudaGetLastError();
+}
+
 int *status_word() {
     int *p = nullptr;
     return kernel_status_address(&p) == cudaSuccess ? p : nullptr;
@@ -282,9 +514,78 @@ bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int 
            group % kChunkK == 0 && K % kChunkK == 0 && N % 8 == 0 && (K / group) >= 1;
 }
 
+// Default variant (A in tensor memory): the split-ring kernel.
+cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
+    SplitArgs sa;
+    sa.status = status_word();
+    if (!sa.status) return cudaErrorInvalidDevice;
+    sa.M = a.M;
+    sa.N = a.N;
+    sa.K = a.K;
+    sa.group = a.group;
+    sa.tile_m = cfg.tile_m;
+    const int ndq = cfg.warps_k > 0 ? cfg.warps_k : 8;
+    sa.sz_rows = a.group % kStageK == 0 ? 1 : 2;
+    sa.x_chunk_bytes = sa.tile_m * kChunkK * 2;                // tile_m % 16 == 0: 1024-aligned
+    sa.s_off = kPackedRows * kTileN * 4;
+    sa.z_off = sa.s_off + sa.sz_rows * kTileN * 2;
+    sa.w_stage_bytes = round_up(sa.z_off + sa.sz_rows * kTileN * 2, 1024);
+    sa.w_tx = kPackedRows * kTileN * 4 + 2 * sa.sz_rows * kTileN * 2;
+    // tensor memory: the accumulator (tile_m fp32 columns) and the A slots
+    sa.a_col0 = round_up(sa.tile_m, 32);
+    sa.as = (512 - sa.a_col0) / (kStageK / 2);
+    if (sa.as > 4) sa.as = 4;
+    if (sa.as < 2) return cudaErrorNotSupported;
+    int cols = 32;
+    while (cols < sa.a_col0 + sa.as * (kStageK / 2)) cols *= 2;
+    sa.tmem_cols = cols;
+    // shared memory: the weight ring (4 stages when x leaves room, else 3),
+    // then as many x chunks as fit (at most 16)
+    const int budget = 224 * 1024;
+    sa.ws = 4;
+    int xs = (budget - sa.ws * sa.w_stage_bytes) / sa.x_chunk_bytes;
+    if (xs < 6) {
+        sa.ws = 3;
+        xs = (budget - sa.ws * sa.w_stage_bytes) / sa.x_chunk_bytes;
+    }
+    sa.xs = xs > 16 ? 16 : xs;
+    if (sa.xs < 2) return cudaErrorNotSupported;
+    sa.w_off = sa.xs * sa.x_chunk_bytes;
+    sa.timeout_ns = 1000000000ull;
+    const size_t smem = (size_t)sa.w_off + (size_t)sa.ws * sa.w_stage_bytes +
+                        (2 * sa.xs + 2 * sa.ws + 2 * sa.as + 1) * 8 + 16 + 1024;
+
+    CUtensorMap tx, tw, ts, tz, to;
+    if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, a.K, a.M, (uint64_t)a.K * 2,
+                      kChunkK, sa.tile_m, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.out, a.N, a.M, (uint64_t)a.N * 2,
+                      kTileN, sa.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, a.K / 8,
+                      (uint64_t)a.N * 4, kTileN, kPackedRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
+                      (uint64_t)a.N * 2, kTileN, sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.zeros, a.N, a.K / a.group,
+                      (uint64_t)a.N * 2, kTileN, sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const int mtiles = (a.M + sa.tile_m - 1) / sa.tile_m;
+    if (mtiles > 65535) return cudaErrorInvalidValue;
+    dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, 1);
+    switch (ndq) {
+    case 4: return launch_split_kernel<4>(grid, smem, stream, tx, tw, ts, tz, to, sa);
+    case 16: return launch_split_kernel<16>(grid, smem, stream, tx, tw, ts, tz, to, sa);
+    default: return launch_split_kernel<8>(grid, smem, stream, tx, tw, ts, tz, to, sa);
+    }
+}
+
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
     if (cfg.variant == W4A16_PREFILL_PAIR) return launch_prefill_pair(a, cfg, stream);
     if (!prefill_config_supported(cfg, a.M, a.N, a.K, a.group)) return cudaErrorNotSupported;
+    // Wide tiles: the split-ring kernel (its x ring runs far enough ahead to
+    // cover the copy latency at 1024+ MMA cycles per stage).  Narrower tiles
+    // are bound by the per-stage control path instead, where one ring (one
+    // wait and one commit per stage) is cheaper.
+    if (cfg.variant != W4A16_PREFILL_A_SMEM && cfg.tile_m >= kSplitMinTileM)
+        return launch_prefill_split(a, cfg, stream);
     PrefillArgs pa;
     pa.out = a.out;
     pa.status = status_word();
