@@ -232,7 +232,15 @@ bool tma_variant_possible(int N, int group) {
 constexpr int kDecodeMaxM = 16;
 
 // rows of x per prefill CTA: all of M up to 256, else 256
-int default_tile_m(int M) { return M >= 256 ? 256 : ((M + 15) / 16) * 16; }
+// Rows of x per prefill CTA (measured on GB300): 256 from M = 256 up; below,
+// all of M in one tile -- except that for M <= 64 with fewer 128-column tiles
+// than SMs, a 128-row tile (one CTA per SM) beats narrow tiles two to an SM.
+int default_tile_m(int M, int N) {
+    if (M >= 256) return 256;
+    const int rounded = ((M + 15) / 16) * 16;
+    if (rounded <= 64 && (N + 127) / 128 < device_info().sm_count) return 128;
+    return rounded;
+}
 
 w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
                        w4a16_config &c) {
@@ -244,7 +252,7 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
         if (M > kDecodeMaxM) {
             w4a16_config pc = c;
             pc.path = W4A16_PATH_PREFILL;
-            if (pc.tile_m <= 0) pc.tile_m = default_tile_m(M);
+            if (pc.tile_m <= 0) pc.tile_m = default_tile_m(M, N);
             if (prefill_config_supported(pc, M, N, K, group)) c.path = W4A16_PATH_PREFILL;
         }
     }
@@ -272,7 +280,7 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
             return fail(W4A16_ERR_INVALID_ARG, "unknown decode variant %d", c.variant);
         }
     } else if (c.path == W4A16_PATH_PREFILL) {
-        if (c.tile_m <= 0) c.tile_m = default_tile_m(M);
+        if (c.tile_m <= 0) c.tile_m = default_tile_m(M, N);
         // measured: 8 dequantizing warps at every tile width (with 4, M = 32..64
         // on K=8192 N=28672 ran 25% slower)
         if (c.warps_k <= 0) c.warps_k = 8;

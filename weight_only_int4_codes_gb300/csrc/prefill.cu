@@ -267,6 +267,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 // Warps: 0 x producer, 1 tensor-memory owner and MMA issuer, 2 weight
 // producer, 3.. dequantization and epilogue.
 constexpr int kSplitDeq0 = 3;
+constexpr int kTwoPerSmMaxTileM = 64;   // one-ring kernel: two CTAs per SM up to this tile
 constexpr int kSplitMinTileM = 192;     // measured crossover (128: one ring is faster)
 
 struct SplitArgs {
@@ -610,14 +611,20 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     pa.z_off = pa.s_off + pa.sz_rows * kTileN * 2;
     pa.stage_bytes = round_up(pa.z_off + pa.sz_rows * kTileN * 2, 1024);
     pa.tx_bytes = kChunks * pa.b_chunk_bytes + kPackedRows * kTileN * 4 + 2 * pa.sz_rows * kTileN * 2;
-    const int budget = 224 * 1024;
+    // Narrow tiles (up to 64 rows of x) are bound by the per-stage control
+    // path, not by the tensor core: two CTAs share an SM (half of its shared
+    // memory and of its tensor memory each), which doubles the stages in
+    // flight per SM.  Wider tiles take the whole SM.
+    const bool two_per_sm = atmem && pa.tile_m <= kTwoPerSmMaxTileM;
+    const int budget = two_per_sm ? 104 * 1024 : 224 * 1024;
+    const int tmem_max = two_per_sm ? 256 : 512;
     int stages = budget / pa.stage_bytes;
     stages = stages > 8 ? 8 : stages;
     // tensor memory: the accumulator (tile_m fp32 columns) and, with A in
     // tensor memory, one 64-column A slot per stage
     pa.a_col0 = round_up(pa.tile_m, 32);
     if (atmem) {
-        const int max_stages = (512 - pa.a_col0) / (kStageK / 2);
+        const int max_stages = (tmem_max - pa.a_col0) / (kStageK / 2);
         stages = stages > max_stages ? max_stages : stages;
     }
     if (stages < 2) return cudaErrorNotSupported;
