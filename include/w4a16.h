@@ -101,7 +101,9 @@ typedef enum w4a16_path {
 typedef struct w4a16_config {
     int path;       /* w4a16_path */
     int split_k;    /* decode: CTAs of one cluster that split K (1..8) */
-    int warps_k;    /* decode (registers variant): warps per CTA that split K;
+    int warps_k;    /* decode, registers variant: warps per CTA that split K;
+                       decode, TMA variant: consumer warps per CTA (4, 8 or 16;
+                       4 lets three CTAs share an SM);
                        prefill: dequantizing warps (4, 8 or 16; 4 or 8 for CTA pairs) */
     int warps_n;    /* decode: 32-column strips per CTA (TMA variant: 2 or 4) */
     int steps;      /* decode: K per warp in 32-row steps (registers variant) or

@@ -136,7 +136,7 @@ def test_auto_path_small_m_is_decode():
     assert (t["variant"], t["split_k"], t["steps"]) == (1, 8, 2)
     assert w4.plan(16, 4096, 4096)["variant"] == 2         # registers variant at M = 16
     t = w4.plan(4, 14336, 4096)
-    assert (t["variant"], t["warps_n"], t["split_k"], t["steps"]) == (1, 4, 2, 8)
+    assert (t["variant"], t["warps_n"], t["warps_k"], t["split_k"], t["steps"]) == (1, 2, 4, 2, 8)
     assert w4.plan(1, 4092, 4096)["variant"] == 2         # N % 8 != 0: registers variant
     assert w4.plan(1, 4096, 4096, 512)["variant"] == 2    # group 512: registers variant
     # off-table shapes take the TMA planner when the format allows it

@@ -172,15 +172,14 @@ struct TableEntry {
 };
 constexpr TableEntry kDecodeTable[] = {
     // K      N      M<=   path split warps_k warps_n steps tile flags variant
-    {4096, 4096, 2, {1, 8, 8, 4, 2, 0, 0, W4A16_DECODE_TMA}},
+    {4096, 4096, 4, {1, 8, 4, 2, 2, 0, 0, W4A16_DECODE_TMA}},
     {4096, 4096, 8, {1, 2, 8, 1, 8, 0, 0, W4A16_DECODE_REGISTERS}},
     {4096, 4096, 16, {1, 1, 8, 1, 16, 0, 0, W4A16_DECODE_REGISTERS}},
-    {4096, 14336, 8, {1, 2, 8, 4, 8, 0, 0, W4A16_DECODE_TMA}},
-    {4096, 14336, 16, {1, 1, 4, 1, 32, 0, 0, W4A16_DECODE_REGISTERS}},
+    {4096, 14336, 16, {1, 2, 4, 2, 8, 0, 0, W4A16_DECODE_TMA}},
     {14336, 4096, 8, {1, 8, 8, 4, 7, 0, 0, W4A16_DECODE_TMA}},
-    {14336, 4096, 16, {1, 4, 8, 2, 14, 0, 0, W4A16_DECODE_TMA}},
-    {2048, 768, 4, {1, 8, 8, 2, 1, 0, 0, W4A16_DECODE_TMA}},
-    {2048, 768, 8, {1, 2, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+    {14336, 4096, 16, {1, 6, 4, 2, 10, 0, 0, W4A16_DECODE_TMA}},
+    {2048, 768, 2, {1, 8, 8, 2, 1, 0, 0, W4A16_DECODE_TMA}},
+    {2048, 768, 8, {1, 8, 2, 2, 4, 0, 0, W4A16_DECODE_REGISTERS}},
     {2048, 768, 16, {1, 4, 4, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
     {768, 2048, 16, {1, 1, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
 };

@@ -57,7 +57,9 @@ namespace {
 
 constexpr int kStageRows = 32;                 // packed rows per stage
 constexpr int kStageK = 8 * kStageRows;        // 256 k per stage
-constexpr int kSmemBudget = 108 * 1024;        // ring + slots per CTA (about half an SM)
+// ring + slots per CTA: about half an SM with 8 or 16 consumer warps, about a
+// third with 4 (three small CTAs per SM: two of one GEMM and one of the next)
+constexpr int smem_budget(int cw) { return cw == 4 ? 72 * 1024 : 108 * 1024; }
 constexpr int kSmemMax = 220 * 1024;           // opt-in limit set on the kernels
 
 struct TmaDecodeArgs {
@@ -83,7 +85,7 @@ __device__ __forceinline__ int perm8(int g) { return (g >> 1) + ((g & 1) << 2); 
 // quantization group (group >= 32 * steps per warp), so the group constants
 // are formed once per stage and the step loop has no branches.
 template <int NT, int BNS, int CW, bool ONE_GROUP>
-__global__ void __launch_bounds__(32 * (CW + 1), CW == 8 ? 2 : 1)
+__global__ void __launch_bounds__(32 * (CW + 1), CW == 4 ? 3 : (CW == 8 ? 2 : 1))
 decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_x,
                   const TmaDecodeArgs a)
@@ -425,7 +427,7 @@ Layout layout_for(int group, int bns, int nt, int n_st, int split, int cw) {
     L.tx_bytes = bns * 4096 + 2 * sz + kStageK * mb * 2;
     // [split][MB][BN] CTA partials, then [WK][MB][BN] warp partials (fp32)
     const int slots_bytes = (split + cw / bns) * mb * BN * 4;
-    int ns = (kSmemBudget - slots_bytes) / L.stage_bytes;
+    int ns = (smem_budget(cw) - slots_bytes) / L.stage_bytes;
     ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
     if (n_st > 0 && ns > n_st) ns = n_st < 2 ? 2 : n_st;
     L.stages = ns;
@@ -501,15 +503,20 @@ extern "C" __attribute__((visibility("default"))) int w4a16_trace_launches(void 
 }
 #endif
 
+int consumer_warps(const w4a16_config &cfg) {
+    return cfg.warps_k == 16 ? 16 : (cfg.warps_k == 4 ? 4 : 8);
+}
+
 int decode_tma_smem_bytes(const w4a16_config &cfg, int M, int group) {
-    const int cw = cfg.warps_k == 16 ? 16 : 8;
+    const int cw = consumer_warps(cfg);
     return layout_for(group, cfg.warps_n, M > 8 ? 2 : 1, cfg.steps, cfg.split_k, cw).smem_bytes;
 }
 
 bool decode_tma_supported(const w4a16_config &cfg, int group) {
     const bool g_ok = group == 32 || group == 64 || group == 128 || group == 256;
     return g_ok && (cfg.warps_n == 2 || cfg.warps_n == 4) &&
-           (cfg.warps_k == 0 || cfg.warps_k == 8 || cfg.warps_k == 16) && cfg.split_k >= 1 &&
+           (cfg.warps_k == 0 || cfg.warps_k == 4 || cfg.warps_k == 8 || cfg.warps_k == 16) &&
+           cfg.split_k >= 1 &&
            cfg.split_k <= 8 && cfg.steps >= 1;
 }
 
@@ -522,7 +529,7 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     const int KB = a.K / 8;
     const int rows_per_cta = cfg.steps * kStageRows;
     if ((long long)rows_per_cta * cfg.split_k < KB) return cudaErrorInvalidValue;
-    const int cw = cfg.warps_k == 16 ? 16 : 8;   // consumer warps per CTA
+    const int cw = consumer_warps(cfg);           // consumer warps per CTA
     const Layout L = layout_for(a.group, bns, nt, cfg.steps, cfg.split_k, cw);
     if (L.smem_bytes > kSmemMax) return cudaErrorNotSupported;
     const int BN = 32 * bns;
@@ -586,6 +593,10 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     if (cw == 8) {
         if (nt == 1) return bns == 4 ? W4A16_TMA_LAUNCH(1, 4, 8) : W4A16_TMA_LAUNCH(1, 2, 8);
         return bns == 4 ? W4A16_TMA_LAUNCH(2, 4, 8) : W4A16_TMA_LAUNCH(2, 2, 8);
+    }
+    if (cw == 4) {
+        if (nt == 1) return bns == 4 ? W4A16_TMA_LAUNCH(1, 4, 4) : W4A16_TMA_LAUNCH(1, 2, 4);
+        return bns == 4 ? W4A16_TMA_LAUNCH(2, 4, 4) : W4A16_TMA_LAUNCH(2, 2, 4);
     }
     if (nt == 1) return bns == 4 ? W4A16_TMA_LAUNCH(1, 4, 16) : W4A16_TMA_LAUNCH(1, 2, 16);
     return bns == 4 ? W4A16_TMA_LAUNCH(2, 4, 16) : W4A16_TMA_LAUNCH(2, 2, 16);
