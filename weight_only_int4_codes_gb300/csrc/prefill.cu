@@ -8,26 +8,31 @@
 // section "Results": once M grows into prefill the unpack must hide under the
 // MMA).
 //
-// Roles are swapped so that one kernel serves every M from 16 up:
+// Roles are swapped so that one kernel family serves every M from 16 up:
 //   D[n, m] (TMEM: 128 lanes = weight columns n, tile_m columns = rows m of x)
-//     += A[n, k] (dequantized W^T, K-major, 128B-swizzled, in shared memory)
+//     += A[n, k] (dequantized W^T, in tensor memory -- or, variant 2, in
+//                 128B-swizzled shared memory)
 //      * B[k, m] (x tile, K-major = x row-major, TMA-loaded 128B-swizzled).
 //   UMMA shape M = 128 (weight columns), N = tile_m (16..256, rows of x), K = 16.
-// Each weight is dequantized once per tile_m rows of x.
+// Each weight is dequantized once per tile_m rows of x; with A in tensor
+// memory the dequantized weight never touches shared memory, which would
+// otherwise become the bottleneck (the MMA re-reads its shared operands).
 //
-// Warp roles: warp 0 issues TMA (x tile, packed words, scale and zero rows)
-// into a ring of stages; warp 1 allocates tensor memory and its elected lane
-// issues the MMAs and commits them to mbarriers; the 4 or 8 warps after them
-// dequantize each stage's 8 x 128 packed words into the A operand (a thread
-// owns one weight column -- one tensor-memory lane -- and 8 or 4 of its
-// words) and, at the end, read the accumulator out of tensor memory and store
-// fp16 results.  By default A lives in tensor memory (tcgen05.st, read by the
-// MMA as [a_tmem]): the dequantized weight then never touches shared memory,
-// which otherwise becomes the bottleneck (the MMA re-reads both operands from
-// it).  An A-in-shared-memory variant (one 16-byte 128B-swizzled store per
-// word, 4/8/16 dequantizing warps) is kept for comparison.  Every wait is
-// bounded in wall time; a wait that gives up records W4A16_ERR_TIMEOUT and the
-// kernel still frees its tensor memory before it exits.
+// Two kernels, chosen by tile width (launch_prefill):
+//   * prefill_split_kernel (tiles of 192+ rows): x, weights and A each on
+//     their own ring (see its comment) so that the wide x tile is refilled in
+//     64-k chunks as soon as the MMAs release them;
+//   * prefill_tcgen05_kernel (narrower tiles, and the A-in-shared-memory
+//     variant): one ring of 128-k stages carrying the x chunks, the packed
+//     words and the scale/zero rows -- one wait and one commit per stage,
+//     cheaper when a stage holds few MMA cycles.  Tiles of up to 64 rows use
+//     half an SM, so two CTAs (two issuers) share it.
+// In both, the 4, 8 or 16 dequantizing warps own one weight column (one TMEM
+// lane) per thread and split the stage's 16 packed rows; at the end they read
+// the accumulator out of tensor memory, stage the fp16 tile in the drained
+// ring and store it with one TMA copy.  Every wait is bounded in wall time; a
+// wait that gives up records W4A16_ERR_TIMEOUT and the kernel still frees its
+// tensor memory before it exits.
 #include <mutex>
 
 #include "common.cuh"
@@ -56,7 +61,7 @@ struct PrefillArgs {
     unsigned long long timeout_ns;
 };
 
-// NDQ: dequantizing warps (4, 8 or 16); they split the stage's 8 packed rows
+// NDQ: dequantizing warps (4, 8 or 16); they split the stage's 16 packed rows
 // of each column (NDQ/4 warps per column group) and, in the epilogue, the
 // accumulator's columns.
 // ATMEM: the dequantized A operand lives in tensor memory (written with
