@@ -2,6 +2,7 @@
 // launch planning (dispatch), error reporting.  Every compute step runs in the
 // kernels of quant.cu, decode.cu and prefill.cu.
 #include <mutex>
+#include <set>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string>
@@ -294,6 +295,19 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
 }
 
 }  // namespace
+
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::set<std::pair<int, const void *>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({dev, kernel})) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({dev, kernel});
+    return e;
+}
 
 const DeviceInfo &device_info() {
     static DeviceInfo info;

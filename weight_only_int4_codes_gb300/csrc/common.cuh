@@ -71,6 +71,11 @@ bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int 
 cudaError_t launch_prefill_pair(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool prefill_pair_supported(const w4a16_config &cfg, int M, int N, int K, int group);
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (device, kernel): the attribute belongs to the device's
+// context, so a process that drives several GPUs sets it on each.
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
+
 // Hardware facts used by the planner (queried once per device, cached).
 struct DeviceInfo {
     int sm_count;

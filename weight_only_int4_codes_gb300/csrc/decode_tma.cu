@@ -440,12 +440,8 @@ template <int NT, int BNS, int CW, bool OG>
 cudaError_t launch_tma(const CUtensorMap &w, const CUtensorMap &s, const CUtensorMap &z,
                        const CUtensorMap &x, const TmaDecodeArgs &da, int tiles, int mchunks,
                        int smem, bool pdl, cudaStream_t stream) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_tma_kernel<NT, BNS, CW, OG>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    });
+    const cudaError_t attr_err =
+        ensure_dynamic_smem((const void *)decode_tma_kernel<NT, BNS, CW, OG>, kSmemMax);
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(tiles, da.split, mchunks);

@@ -477,12 +477,8 @@ cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                   const CUtensorMap &tx, const CUtensorMap &tw,
                                   const CUtensorMap &ts, const CUtensorMap &tz,
                                   const CUtensorMap &to, const PrefillArgs &pa) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(prefill_tcgen05_kernel<NDQ, ATMEM>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
+    const cudaError_t attr =
+        ensure_dynamic_smem((const void *)prefill_tcgen05_kernel<NDQ, ATMEM>, 227 * 1024);
     if (attr != cudaSuccess) return attr;
     prefill_tcgen05_kernel<NDQ, ATMEM><<<grid, 32 * (NDQ + 2), smem, stream>>>(tx, tw, ts, tz, to,
                                                                               pa);
@@ -494,12 +490,8 @@ cudaError_t launch_split_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                 const CUtensorMap &tx, const CUtensorMap &tw,
                                 const CUtensorMap &ts, const CUtensorMap &tz,
                                 const CUtensorMap &to, const SplitArgs &sa) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(prefill_split_kernel<NDQ>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
+    const cudaError_t attr =
+        ensure_dynamic_smem((const void *)prefill_split_kernel<NDQ>, 227 * 1024);
     if (attr != cudaSuccess) return attr;
     prefill_split_kernel<NDQ><<<grid, 32 * (NDQ + 3), smem, stream>>>(tx, tw, ts, tz, to, sa);
     return cudaGetLastError();

@@ -224,12 +224,8 @@ template <int NDQ>
 cudaError_t launch_pair_kernel(dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap &tx,
                                const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tz,
                                const PairArgs &pa) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(prefill_pair_kernel<NDQ>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
+    const cudaError_t attr =
+        ensure_dynamic_smem((const void *)prefill_pair_kernel<NDQ>, 227 * 1024);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = grid;
