@@ -299,19 +299,53 @@ def test_gemm_random_encodings():
         check_gemm(x, dev_w, (packed, scales, zeros), 128)
 
 
-def test_one_hot_is_exact():
-    """x = e_k: a single nonzero product, so out equals the dequantized row bit-exactly."""
+@pytest.mark.parametrize("M,config", [
+    (1, None), (16, None),
+    (1, dict(path="decode", variant="registers")), (16, dict(path="decode", variant="registers")),
+    (1, dict(path="decode", variant="tma", warps_k=4)), (16, dict(path="decode", variant="tma", warps_k=4)),
+    (9, dict(path="decode", variant="tma", warps_k=16)),
+    (64, dict(path="prefill", tile_m=64)), (128, dict(path="prefill", tile_m=128)),
+    (300, dict(path="prefill", tile_m=256)), (300, dict(path="prefill", variant="smem", tile_m=128)),
+    (300, dict(path="prefill", variant="pair", tile_m=256)),
+])
+def test_one_hot_is_exact(M, config):
+    """x = e_k: a single nonzero product, so out equals the dequantized row
+    bit-exactly -- on every kernel (decode variants, the tcgen05 kernels)."""
     K, N = 1024, 768
     W = synth.weight(K, N, seed=61, outliers=True)
     dev_w, ref_w = quantize_both(W, 128)
     wdq = oracle.dequant(*ref_w, group=128).view(np.uint16)
     ks = np.array([0, 1, 7, 8, 127, 128, 500, 1023, 640, 64, 333, 900, 17, 256, 1000, 2])
-    for M in (1, 16):
-        x = np.zeros((M, K), dtype=np.float16)
-        x[np.arange(M), ks[:M]] = 1.0
-        out = w4.gemm(to_dev(x), *dev_w, group=128)
+    if M > len(ks):
+        ks = np.random.Generator(np.random.PCG64(M)).integers(0, K, M)
+    x = np.zeros((M, K), dtype=np.float16)
+    x[np.arange(M), ks[:M]] = 1.0
+    out = w4.gemm_ex(to_dev(x), *dev_w, group=128, config=config)
+    torch.cuda.synchronize()
+    assert w4.kernel_status() == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), wdq[ks[:M]])
+
+
+@pytest.mark.parametrize("config", [dict(path="prefill", tile_m=256),
+                                    dict(path="prefill", variant="pair", tile_m=256),
+                                    dict(path="prefill", tile_m=64)])
+def test_prefill_zero_input_dirty_output_determinism(config):
+    """The tcgen05 kernels overwrite every output element (NaN-filled out),
+    give exact zeros for x = 0 and are bitwise run-to-run reproducible."""
+    K, N, M = 2048, 1024, 300
+    W = synth.weight(K, N, seed=73)
+    dev_w, _ = quantize_both(W, 128)
+    x = to_dev(synth.activations(M, K, seed=74))
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    w4.gemm_ex(torch.zeros_like(x), *dev_w, group=128, out=out, config=config)
+    torch.cuda.synchronize()
+    assert not out.isnan().any() and (out == 0).all()
+    first = w4.gemm_ex(x, *dev_w, group=128, config=config).clone()
+    for _ in range(3):
+        out.fill_(float("nan"))
+        w4.gemm_ex(x, *dev_w, group=128, out=out, config=config)
         torch.cuda.synchronize()
-        assert np.array_equal(out.cpu().numpy().view(np.uint16), wdq[ks[:M]])
+        assert torch.equal(out.view(torch.int16), first.view(torch.int16))
 
 
 def test_zero_input_and_dirty_output_and_determinism():
