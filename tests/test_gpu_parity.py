@@ -261,6 +261,20 @@ def test_gemm_prefill_group_boundaries(K, group, tile_m):
     check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=tile_m))
 
 
+@pytest.mark.parametrize("warps", [4, 8])
+@pytest.mark.parametrize("K,group", [(64, 64), (192, 64), (1088, 64), (1152, 192)])
+def test_gemm_prefill_persistent_tiles(K, group, warps):
+    """The split-ring kernel is persistent (one CTA per SM): 21 x 8 = 168
+    output tiles, more than there are SMs, so some CTAs run two tiles and the
+    rings, the A slots and the accumulator carry over a tile boundary.  K from
+    one half stage (64) and fewer stages than the ring holds (192) up to
+    several ring turns with a half last stage; N and M ragged."""
+    N, M = 2600, 1999
+    _, dev_w, ref_w = quantized(K, N, group, 23 + K, True)
+    x = synth.activations(M, K, seed=29 + K)
+    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=256, warps_k=warps))
+
+
 @pytest.mark.parametrize("group", [64, 256])
 def test_gemm_prefill_other_groups(group):
     K, N, M = 1024, 384, 200

@@ -254,21 +254,28 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 }
 
 // ---------------------------------------------------------------------------
-// Split-ring kernel (the default, A in tensor memory).  The x tile and the
-// weights travel in separate rings so that each is refilled as soon as its
-// own consumer is done with it:
-//   x ring      xs slots of one 64-k chunk of the x tile (tile_m x 128 bytes,
-//               128B-swizzled); filled by warp 0, freed by the MMAs' commit;
-//   weight ring ws slots of one 128-k stage (16 x 128 packed words, scale and
-//               zero rows); filled by warp 2, freed by the dequantizing warps
-//               as soon as they have the words in registers;
-//   A slots     as tensor-memory slots of one dequantized 128-k stage
-//               (64 columns); written by the dequantizing warps, freed by the
-//               MMAs' commit.
-// With one ring per stage the x slot of a stage could only be refilled after
-// its MMAs, so at tile_m = 256 (73 KB per stage, three stages) the copies ran
-// about two stages ahead -- less than their latency.  Here x is refilled in
-// 32 KB chunks (six in flight) and the weights run further ahead on their own.
+// Split-ring kernel (the default for wide tiles, A in tensor memory).  It is
+// persistent: one CTA per SM walks the output tiles t = blockIdx.x, +gridDim.x,
+// ... (weight-column tile fastest), and its rings run on across tile
+// boundaries, so the next tile's copies and dequantization overlap the
+// current tile's last MMAs and epilogue.  The weights travel on their own
+// ring, apart from the x tile:
+//   stage slots  xs slots, each holding one 128-k x tile (two 64-k chunks,
+//                128B-swizzled, one 3-D TMA box) in shared memory AND one
+//                dequantized 128-k A stage (64 columns) in tensor memory;
+//                filled by warp 0 (x) and the dequantizing warps (A), freed
+//                by ONE commit of the stage's MMAs;
+//   weight ring  ws slots of one 128-k stage (16 x 128 packed words, scale
+//                and zero rows); filled by warp 2, freed by the dequantizing
+//                warps as soon as they have the words in registers.
+// The single issuing thread is the pace-setter at tile_m = 256 (a
+// tcgen05.mma issue costs tens of cycles, a commit about a hundred): per
+// stage it waits on two barriers, issues 8 MMAs and one commit.
+// The accumulator (tile_m fp32 columns) has one buffer: at the end of a tile
+// the dequantizing warps drain it into registers (fp16 pairs), free it for
+// the next tile's MMAs, and then write the fp16 tile to global memory with
+// 4-byte stores while the next tile's first stages, already dequantized,
+// run on the tensor cores.
 // Warps: 0 x producer, 1 tensor-memory owner and MMA issuer, 2 weight
 // producer, 3.. dequantization and epilogue.
 constexpr int kSplitDeq0 = 3;
@@ -277,11 +284,14 @@ constexpr int kSplitMinTileM = 192;     // measured crossover (128: one ring is 
 
 struct SplitArgs {
     int *status;
+    uint16_t *out;
     int M, N, K, group;
     int tile_m;
-    int xs, ws, as;            // slots of the x ring, the weight ring, the A ring
+    int n_tiles, tiles;        // weight-column tiles, all output tiles
+    int xs, ws;                // stage slots (x in shared + A in tensor memory), weight slots
+    int x_stage_bytes;         // two 64-k chunks of the x tile: tile_m * 256
     int x_chunk_bytes;         // tile_m * 128
-    int w_off;                 // offset of the weight ring (after the x ring)
+    int w_off;                 // offset of the weight ring (after the x slots)
     int w_stage_bytes;
     int s_off, z_off;          // scale / zero rows inside a weight stage (packed at 0)
     int sz_rows;
@@ -290,50 +300,119 @@ struct SplitArgs {
     unsigned long long timeout_ns;
 };
 
+// Write 16 fp16 pairs of one thread -- column n (its TMEM lane), rows
+// r0 + 2j and r0 + 2j + 1 -- as 4-byte words: even and odd lanes swap halves
+// so that each holds two adjacent columns of one row.
+__device__ __forceinline__ void store_pairs(const uint32_t (&hc)[16], int r0, int lane, int col,
+                                            bool col_ok, int m0, int tile_m, int M, int N,
+                                            uint16_t *out) {
+    const bool odd = lane & 1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t mine = hc[j];
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+        const uint32_t w = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
+        const int r = r0 + 2 * j + (odd ? 1 : 0);
+        if (col_ok && r < tile_m && m0 + r < M)
+            *reinterpret_cast<uint32_t *>(out + (size_t)(m0 + r) * N + col) = w;
+    }
+}
+
+__device__ __forceinline__ void pack_chunk(const uint32_t (&v)[32], uint32_t (&hc)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const __half2 p = __floats2half2_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        hc[j] = *reinterpret_cast<const uint32_t *>(&p);
+    }
+}
+
+// Epilogue of one dequantizing warp for the tile at (m0, n0): its lane quarter
+// of the accumulator, columns 32 * part, + 32 * (NDQ / 4), ...  With 8 or 16
+// warps the thread's share (at most 64 pairs) is held in registers and the
+// accumulator is freed before any store; with 4 warps it is written chunk by
+// chunk and freed after.
+template <int NDQ>
+__device__ __forceinline__ void split_epilogue(uint32_t lane_base, int lane, int n, int part,
+                                               int m0, int n0, uint64_t *accum_full,
+                                               uint64_t *accum_empty, uint32_t parity,
+                                               const SplitArgs &a) {
+    constexpr int kStep = 32 * (NDQ / 4);
+    constexpr int kCh = 256 / kStep;          // chunks of 32 columns per thread (tile_m <= 256)
+    if (!mbar_wait_bounded(accum_full, parity, a.timeout_ns))
+        report_status(a.status, W4A16_ERR_TIMEOUT);
+    tc_fence_after();
+    const int col = n0 + (n & ~1);
+    const bool col_ok = col < a.N;
+    const int first = 32 * part;
+    if constexpr (kCh <= 4) {
+        uint32_t h[kCh][16];
+#pragma unroll
+        for (int c = 0; c < kCh; ++c) {
+            // columns first + c * kStep < 256: inside the allocation even
+            // where they lie past tile_m (those rows are never stored)
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(lane_base + (uint32_t)(first + c * kStep), v);
+            tmem_ld_wait();
+            pack_chunk(v, h[c]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accum_empty);
+#pragma unroll
+        for (int c = 0; c < kCh; ++c)
+            store_pairs(h[c], first + c * kStep, lane, col, col_ok, m0, a.tile_m, a.M, a.N, a.out);
+    } else {
+        for (int c = 0; c < kCh; ++c) {
+            uint32_t v[32], hc[16];
+            tmem_ld_32x32b_x32(lane_base + (uint32_t)(first + c * kStep), v);
+            tmem_ld_wait();
+            pack_chunk(v, hc);
+            store_pairs(hc, first + c * kStep, lane, col, col_ok, m0, a.tile_m, a.M, a.N, a.out);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accum_empty);
+    }
+}
+
 template <int NDQ>
 __global__ void __launch_bounds__(32 * (NDQ + 3), 1)
 prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
-                     const __grid_constant__ CUtensorMap tm_o, const SplitArgs a)
+                     const SplitArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *wring = ring + a.w_off;
     uint64_t *xfull = reinterpret_cast<uint64_t *>(wring + a.ws * a.w_stage_bytes);
-    uint64_t *xempty = xfull + a.xs;
-    uint64_t *wfull = xempty + a.xs;
+    uint64_t *aready = xfull + a.xs;      // the stage's A slot is written
+    uint64_t *sempty = aready + a.xs;     // the stage's MMAs completed: x slot and A slot free
+    uint64_t *wfull = sempty + a.xs;
     uint64_t *wempty = wfull + a.ws;
-    uint64_t *aready = wempty + a.ws;
-    uint64_t *aempty = aready + a.as;
-    uint64_t *accum = aempty + a.as;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+    uint64_t *accum_full = wempty + a.ws;
+    uint64_t *accum_empty = accum_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum_empty + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileN;
-    const int m0 = blockIdx.y * a.tile_m;
     const int KT = (a.K + kStageK - 1) / kStageK;      // 128-k stages (a last half stage reads zeros)
-    const int KC = a.K / kChunkK;                      // 64-k x chunks
 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_x);
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_s);
         prefetch_tmap(&tm_z);
-        prefetch_tmap(&tm_o);
         for (int i = 0; i < a.xs; ++i) {
             mbar_init(&xfull[i], 1);
-            mbar_init(&xempty[i], 1);
+            mbar_init(&aready[i], NDQ);
+            mbar_init(&sempty[i], 1);
         }
         for (int i = 0; i < a.ws; ++i) {
             mbar_init(&wfull[i], 1);
             mbar_init(&wempty[i], NDQ);
         }
-        for (int i = 0; i < a.as; ++i) {
-            mbar_init(&aready[i], NDQ);
-            mbar_init(&aempty[i], 1);
-        }
-        mbar_init(accum, 1);
+        mbar_init(accum_full, 1);
+        mbar_init(accum_empty, NDQ);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -349,70 +428,81 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         // ------------------------------------------------ x producer (lane 0 issues)
         const uint64_t pol_x = l2_evict_last_policy();
         int s = 0, r = 0;
-        for (int c = 0; c < KC; ++c) {
-            if (r > 0 && !mbar_spin_bounded(&xempty[s], (r - 1) & 1, a.timeout_ns))
-                report_status(a.status, W4A16_ERR_TIMEOUT);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&xfull[s], (uint32_t)a.x_chunk_bytes);
-                tma_load_2d(ring + s * a.x_chunk_bytes, &tm_x, &xfull[s], c * kChunkK, m0, pol_x);
+        for (int t = blockIdx.x; t < a.tiles; t += gridDim.x) {
+            const int m0 = (t / a.n_tiles) * a.tile_m;
+            for (int kt = 0; kt < KT; ++kt) {
+                if (r > 0 && !mbar_spin_bounded(&sempty[s], (r - 1) & 1, a.timeout_ns))
+                    report_status(a.status, W4A16_ERR_TIMEOUT);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&xfull[s], (uint32_t)a.x_stage_bytes);
+                    // both 64-k chunks in one 3-D box (chunk index outermost)
+                    tma_load_3d(ring + s * a.x_stage_bytes, &tm_x, &xfull[s], 0, m0, kt * kChunks,
+                                pol_x);
+                }
+                __syncwarp();
+                if (++s == a.xs) { s = 0; ++r; }
             }
-            __syncwarp();
-            if (++s == a.xs) { s = 0; ++r; }
         }
     } else if (warp == 2) {
         // ------------------------------------------------ weight producer
         const uint64_t pol_w = l2_evict_first_policy();
-        int s = 0, r = 0, grow = 0, gnext = a.group;
-        for (int kt = 0; kt < KT; ++kt) {
-            const int k0 = kt * kStageK;
-            while (k0 >= gnext) { ++grow; gnext += a.group; }
-            if (r > 0 && !mbar_wait_bounded(&wempty[s], (r - 1) & 1, a.timeout_ns))
-                report_status(a.status, W4A16_ERR_TIMEOUT);
-            if (lane == 0) {
-                uint8_t *st = wring + s * a.w_stage_bytes;
-                mbar_arrive_expect_tx(&wfull[s], (uint32_t)a.w_tx);
-                tma_load_2d(st, &tm_w, &wfull[s], n0, k0 / 8, pol_w);
-                tma_load_2d(st + a.s_off, &tm_s, &wfull[s], n0, grow, pol_w);
-                tma_load_2d(st + a.z_off, &tm_z, &wfull[s], n0, grow, pol_w);
+        int s = 0, r = 0;
+        for (int t = blockIdx.x; t < a.tiles; t += gridDim.x) {
+            const int n0 = (t % a.n_tiles) * kTileN;
+            int grow = 0, gnext = a.group;
+            for (int kt = 0; kt < KT; ++kt) {
+                const int k0 = kt * kStageK;
+                while (k0 >= gnext) { ++grow; gnext += a.group; }
+                if (r > 0 && !mbar_wait_bounded(&wempty[s], (r - 1) & 1, a.timeout_ns))
+                    report_status(a.status, W4A16_ERR_TIMEOUT);
+                if (lane == 0) {
+                    uint8_t *st = wring + s * a.w_stage_bytes;
+                    mbar_arrive_expect_tx(&wfull[s], (uint32_t)a.w_tx);
+                    tma_load_2d(st, &tm_w, &wfull[s], n0, k0 / 8, pol_w);
+                    tma_load_2d(st + a.s_off, &tm_s, &wfull[s], n0, grow, pol_w);
+                    tma_load_2d(st + a.z_off, &tm_z, &wfull[s], n0, grow, pol_w);
+                }
+                __syncwarp();
+                if (++s == a.ws) { s = 0; ++r; }
             }
-            __syncwarp();
-            if (++s == a.ws) { s = 0; ++r; }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (lane 0 issues)
         const uint32_t idesc = idesc_f16(128, a.tile_m);
         const uint32_t tmem_u = __shfl_sync(0xffffffffu, tmem_d, 0);
         const uint32_t ring_u = smem_u32(ring);
-        int sa = 0, ra = 0, sx = 0, rx = 0;
-        for (int kt = 0; kt < KT; ++kt) {
-            if (!mbar_spin_bounded(&aready[sa], ra & 1, a.timeout_ns))
+        const uint32_t chunk16 = (uint32_t)a.x_chunk_bytes >> 4;
+        int s = 0, r = 0, it = 0;
+        for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
+            // the epilogue of the previous tile has read the accumulator out
+            if (it > 0 && !mbar_spin_bounded(accum_empty, (it - 1) & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
-            const uint32_t a_tmem = tmem_u + (uint32_t)(a.a_col0 + sa * (kStageK / 2));
-#pragma unroll
-            for (int h = 0; h < kChunks; ++h) {
-                if (kt * kChunks + h >= KC) break;            // half last stage
-                if (!mbar_spin_bounded(&xfull[sx], rx & 1, a.timeout_ns))
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_spin_bounded(&aready[s], r & 1, a.timeout_ns))
+                    report_status(a.status, W4A16_ERR_TIMEOUT);
+                if (!mbar_spin_bounded(&xfull[s], r & 1, a.timeout_ns))
                     report_status(a.status, W4A16_ERR_TIMEOUT);
                 tc_fence_after();
-                const uint64_t b_desc = smem_desc_sw128(ring_u + (uint32_t)(sx * a.x_chunk_bytes));
+                const uint64_t b_desc = smem_desc_sw128(ring_u + (uint32_t)(s * a.x_stage_bytes));
+                const uint32_t a_tmem = tmem_u + (uint32_t)(a.a_col0 + s * (kStageK / 2));
                 if (lane == 0) {
+                    // descriptors advance in 16-byte units: 32 bytes per k16
+                    // step inside a chunk, a whole chunk between chunks
 #pragma unroll
-                    for (int kk = 0; kk < kChunkK / 16; ++kk)
-                        umma_f16_ts<1>(tmem_u, a_tmem + h * (kChunkK / 2) + kk * 8, b_desc + kk * 2,
-                                       idesc, (kt | h | kk) != 0);
-                    umma_commit<1>(&xempty[sx]);
+                    for (int kk = 0; kk < kStageK / 16; ++kk)
+                        umma_f16_ts<1>(tmem_u, a_tmem + kk * 8,
+                                       b_desc + (kk / 4) * chunk16 + (kk % 4) * 2, idesc,
+                                       (kt | kk) != 0);
+                    umma_commit<1>(&sempty[s]);
                 }
                 __syncwarp();
-                if (++sx == a.xs) { sx = 0; ++rx; }
+                if (++s == a.xs) { s = 0; ++r; }
             }
-            if (lane == 0) umma_commit<1>(&aempty[sa]);
+            if (lane == 0) umma_commit<1>(accum_full);
             __syncwarp();
-            if (++sa == a.as) { sa = 0; ++ra; }
         }
-        if (lane == 0) umma_commit<1>(accum);
-        __syncwarp();
     } else {
-        // ------------------------------------------------ dequant
+        // ------------------------------------------------ dequant + epilogue
         constexpr int kParts = NDQ / 4;                   // warps per lane quarter
         static_assert(kPackedRows % kParts == 0, "packed rows must split evenly");
         constexpr int kRowsPer = kPackedRows / kParts;    // packed rows per thread
@@ -422,12 +512,16 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         const int n = (warp & 3) * 32 + lane;
         const int part = (warp - kSplitDeq0) / 4;
         const uint32_t lane_base = tmem_d + ((uint32_t)((warp & 3) * 32) << 16);
-        int sw = 0, rw = 0, sa = 0, ra = 0;
-        for (int kt = 0; kt < KT; ++kt) {
+        // the previous tile's epilogue comes before the dequantization of
+        // this tile's stage `ep_at`: the first one whose A slot is freed by
+        // the previous tile's last MMAs (earlier stages overlap those MMAs)
+        const int ep_at = (a.xs - 1 < KT - 1) ? a.xs - 1 : KT - 1;
+        int sw = 0, rw = 0, s = 0, r = 0, it = 0, pm0 = 0, pn0 = 0;
+        auto stage = [&](int kt) {
             if (!mbar_wait_bounded(&wfull[sw], rw & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
             // the A slot is free once the MMAs that read it last have completed
-            if (ra > 0 && !mbar_wait_bounded(&aempty[sa], (ra - 1) & 1, a.timeout_ns))
+            if (r > 0 && !mbar_wait_bounded(&sempty[s], (r - 1) & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
             tc_fence_after();
             const uint32_t st = smem_u32(wring + sw * a.w_stage_bytes);
@@ -437,33 +531,33 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                 const int c0 = part * kRowsPer + b0;
                 uint32_t h[kBlk * 4];
                 dequant_words<kBlk>(st, 0, a.s_off, a.z_off, c0, stage_zrow(k0, a.group, c0), n, h);
-                tmem_st_32x32b<kBlk * 4>(lane_base + (uint32_t)(a.a_col0 + sa * (kStageK / 2) + c0 * 4),
-                                         h);
+                tmem_st_32x32b<kBlk * 4>(
+                    lane_base + (uint32_t)(a.a_col0 + s * (kStageK / 2) + c0 * 4), h);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&wempty[sw]);     // the words are in registers (and stored)
-                mbar_arrive(&aready[sa]);
+                mbar_arrive(&aready[s]);
             }
             if (++sw == a.ws) { sw = 0; ++rw; }
-            if (++sa == a.as) { sa = 0; ++ra; }
+            if (++s == a.xs) { s = 0; ++r; }
+        };
+        for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
+            int kt = 0;
+            if (it > 0) {
+                for (; kt < ep_at; ++kt) stage(kt);
+                split_epilogue<NDQ>(lane_base, lane, n, part, pm0, pn0, accum_full, accum_empty,
+                                    (uint32_t)((it - 1) & 1), a);
+            }
+            for (; kt < KT; ++kt) stage(kt);
+            pm0 = (t / a.n_tiles) * a.tile_m;
+            pn0 = (t % a.n_tiles) * kTileN;
         }
-        // ------------------------------------------------ epilogue
-        if (!mbar_wait_bounded(accum, 0, a.timeout_ns))
-            report_status(a.status, W4A16_ERR_TIMEOUT);
-        tc_fence_after();
-        // every copy has landed and every MMA has read its operands: the x
-        // ring holds the fp16 output tile [tile_m][128] for one TMA store
-        stage_accumulator(lane_base, smem_u32(ring), n, a.tile_m, 32 * part, 32 * kParts);
-        fence_proxy_async_smem();
-        named_bar_sync(1, NDQ * 32);
-        if (warp == kSplitDeq0 && lane == 0) {
-            tma_store_2d(&tm_o, ring, n0, m0);
-            bulk_commit();
-            bulk_wait_all();
-        }
+        if (it > 0)
+            split_epilogue<NDQ>(lane_base, lane, n, part, pm0, pn0, accum_full, accum_empty,
+                                (uint32_t)((it - 1) & 1), a);
     }
     tc_fence_before();
     __syncthreads();
@@ -488,12 +582,11 @@ cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
 template <int NDQ>
 cudaError_t launch_split_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                 const CUtensorMap &tx, const CUtensorMap &tw,
-                                const CUtensorMap &ts, const CUtensorMap &tz,
-                                const CUtensorMap &to, const SplitArgs &sa) {
+                                const CUtensorMap &ts, const CUtensorMap &tz, const SplitArgs &sa) {
     const cudaError_t attr =
         ensure_dynamic_smem((const void *)prefill_split_kernel<NDQ>, 227 * 1024);
     if (attr != cudaSuccess) return attr;
-    prefill_split_kernel<NDQ><<<grid, 32 * (NDQ + 3), smem, stream>>>(tx, tw, ts, tz, to, sa);
+    prefill_split_kernel<NDQ><<<grid, 32 * (NDQ + 3), smem, stream>>>(tx, tw, ts, tz, sa);
     return cudaGetLastError();
 }
 
@@ -512,7 +605,7 @@ bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int 
            group % kChunkK == 0 && K % kChunkK == 0 && N % 8 == 0 && (K / group) >= 1;
 }
 
-// Default variant (A in tensor memory): the split-ring kernel.
+// Default variant (A in tensor memory) for wide tiles: the split-ring kernel.
 cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
     SplitArgs sa;
     sa.status = status_word();
@@ -522,42 +615,41 @@ cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cud
     sa.K = a.K;
     sa.group = a.group;
     sa.tile_m = cfg.tile_m;
+    sa.out = a.out;
+    sa.n_tiles = (a.N + kTileN - 1) / kTileN;
     const int ndq = cfg.warps_k > 0 ? cfg.warps_k : 8;
     sa.sz_rows = a.group % kStageK == 0 ? 1 : 2;
     sa.x_chunk_bytes = sa.tile_m * kChunkK * 2;                // tile_m % 16 == 0: 1024-aligned
+    sa.x_stage_bytes = kChunks * sa.x_chunk_bytes;
     sa.s_off = kPackedRows * kTileN * 4;
     sa.z_off = sa.s_off + sa.sz_rows * kTileN * 2;
     sa.w_stage_bytes = round_up(sa.z_off + sa.sz_rows * kTileN * 2, 1024);
     sa.w_tx = kPackedRows * kTileN * 4 + 2 * sa.sz_rows * kTileN * 2;
-    // tensor memory: the accumulator (tile_m fp32 columns) and the A slots
-    sa.a_col0 = round_up(sa.tile_m, 32);
-    sa.as = (512 - sa.a_col0) / (kStageK / 2);
-    if (sa.as > 4) sa.as = 4;
-    if (sa.as < 2) return cudaErrorNotSupported;
-    int cols = 32;
-    while (cols < sa.a_col0 + sa.as * (kStageK / 2)) cols *= 2;
-    sa.tmem_cols = cols;
-    // shared memory: the weight ring (4 stages when x leaves room, else 3),
-    // then as many x chunks as fit (at most 16)
+    sa.ws = 3;
+    // stage slots: as many x tiles as shared memory holds next to the weight
+    // ring, and no more A stages than tensor memory holds next to the
+    // accumulator (tile_m fp32 columns)
     const int budget = 224 * 1024;
-    sa.ws = 4;
-    int xs = (budget - sa.ws * sa.w_stage_bytes) / sa.x_chunk_bytes;
-    if (xs < 6) {
-        sa.ws = 3;
-        xs = (budget - sa.ws * sa.w_stage_bytes) / sa.x_chunk_bytes;
-    }
-    sa.xs = xs > 16 ? 16 : xs;
+    int xs = (budget - sa.ws * sa.w_stage_bytes) / sa.x_stage_bytes;
+    sa.a_col0 = round_up(sa.tile_m, 32);
+    const int a_max = (512 - sa.a_col0) / (kStageK / 2);
+    xs = xs > a_max ? a_max : xs;
+    sa.xs = xs > 8 ? 8 : xs;
     if (sa.xs < 2) return cudaErrorNotSupported;
-    sa.w_off = sa.xs * sa.x_chunk_bytes;
+    int cols = 32;
+    while (cols < sa.a_col0 + sa.xs * (kStageK / 2)) cols *= 2;
+    sa.tmem_cols = cols;
+    sa.w_off = sa.xs * sa.x_stage_bytes;
     sa.timeout_ns = 1000000000ull;
     const size_t smem = (size_t)sa.w_off + (size_t)sa.ws * sa.w_stage_bytes +
-                        (2 * sa.xs + 2 * sa.ws + 2 * sa.as + 1) * 8 + 16 + 1024;
+                        (3 * sa.xs + 2 * sa.ws + 2) * 8 + 16 + 1024;
 
-    CUtensorMap tx, tw, ts, tz, to;
-    if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, a.K, a.M, (uint64_t)a.K * 2,
-                      kChunkK, sa.tile_m, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_2d(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.out, a.N, a.M, (uint64_t)a.N * 2,
-                      kTileN, sa.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    const uint64_t x_dims[3] = {(uint64_t)kChunkK, (uint64_t)a.M, (uint64_t)(a.K / kChunkK)};
+    const uint64_t x_strides[2] = {(uint64_t)a.K * 2, (uint64_t)kChunkK * 2};
+    const uint32_t x_box[3] = {(uint32_t)kChunkK, (uint32_t)sa.tile_m, (uint32_t)kChunks};
+    CUtensorMap tx, tw, ts, tz;
+    if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, x_dims, x_strides, x_box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, a.K / 8,
                       (uint64_t)a.N * 4, kTileN, kPackedRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
@@ -565,13 +657,16 @@ cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cud
         !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.zeros, a.N, a.K / a.group,
                       (uint64_t)a.N * 2, kTileN, sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    const int mtiles = (a.M + sa.tile_m - 1) / sa.tile_m;
-    if (mtiles > 65535) return cudaErrorInvalidValue;
-    dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, 1);
+    // persistent: one CTA per SM (at most one per tile)
+    const long long tiles = (long long)sa.n_tiles * ((a.M + sa.tile_m - 1) / sa.tile_m);
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    sa.tiles = (int)tiles;
+    const int sms = device_info().sm_count;
+    dim3 grid(sa.tiles < sms ? sa.tiles : sms, 1, 1);
     switch (ndq) {
-    case 4: return launch_split_kernel<4>(grid, smem, stream, tx, tw, ts, tz, to, sa);
-    case 16: return launch_split_kernel<16>(grid, smem, stream, tx, tw, ts, tz, to, sa);
-    default: return launch_split_kernel<8>(grid, smem, stream, tx, tw, ts, tz, to, sa);
+    case 4: return launch_split_kernel<4>(grid, smem, stream, tx, tw, ts, tz, sa);
+    case 16: return launch_split_kernel<16>(grid, smem, stream, tx, tw, ts, tz, sa);
+    default: return launch_split_kernel<8>(grid, smem, stream, tx, tw, ts, tz, sa);
     }
 }
 
