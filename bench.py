@@ -11,9 +11,11 @@ bracketed by CUDA events on the capture stream.
 
 Printed: one JSON line (rank 0).  `value` is the weight-stream bandwidth of
 the whole job (packed words + scales + zeros of every call, all ranks) over the
-timed region; per-M microseconds per call, roofline fractions, a cuBLAS fp16
-reference (torch.matmul on the dequantized weight, same rotation) and the fp64
-oracle on the host cores (`cpu_baseline`) ride along.
+timed region; per-M microseconds per call (CUDA graph, and eager launches one
+by one), GB/s in three conventions (packed + scales + zeros; packed words
+only; every algorithmic byte), roofline fractions, a cuBLAS fp16 reference
+(torch.matmul on the dequantized weight, same rotation) and the fp64 oracle on
+the host cores (`cpu_baseline`) ride along.
 
 --impl reference times the fp64 CPU oracle instead (the reference arm).
 Multi-GPU (torchrun): every rank runs the same step on its own GPU with its own
@@ -312,6 +314,27 @@ def timed_replays(graph, stream, reps, calls_per_replay):
     return out
 
 
+def timed_eager(calls, stream, reps):
+    """Microseconds per call of `reps` rounds of the `calls` issued one by one
+    (no graph), each round bracketed by events on `stream`."""
+    import torch
+    out = []
+    with torch.cuda.stream(stream):
+        for c in calls:                      # warm
+            c()
+        stream.synchronize()
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for c in calls:
+                c()
+            b.record(stream)
+            b.synchronize()
+            out.append(a.elapsed_time(b) * 1e3 / len(calls))
+    return out
+
+
 def run_ours(args, rank, local, world, pg):
     import numpy as np
     import torch
@@ -451,8 +474,15 @@ def run_ours(args, rank, local, world, pg):
             ts = timed_replays(g, stream, args.reps, R)
             us = statistics.median(ts)
             K, N = s["K"], s["N"]
+            calls = [lambda i=i: w4.gemm_ex(s["xs"][M], *s["copies"][i], group=GROUP,
+                                            out=s["outs"][M], config=gemm_cfg)
+                     for i in range(R)]
+            us_eager = statistics.median(timed_eager(calls, stream, args.reps))
             rec = {"us_per_call": round(us, 3),
+                   "us_per_call_eager": round(us_eager, 3),
                    "weight_GBs": round(weight_bytes(K, N) / us / 1e3, 1),
+                   "packed_GBs": round(K * N // 2 / us / 1e3, 1),
+                   "total_GBs": round(total_bytes(M, K, N) / us / 1e3, 1),
                    "roofline_frac": round(max(total_bytes(M, K, N) / (peaks["hbm_gbs"] * 1e9),
                                               2.0 * M * N * K / (peaks["bf16_tflops"] * 1e12))
                                           / (us * 1e-6), 4)}

@@ -19,20 +19,23 @@
 // otherwise become the bottleneck (the MMA re-reads its shared operands).
 //
 // Two kernels, chosen by tile width (launch_prefill):
-//   * prefill_split_kernel (tiles of 192+ rows): x, weights and A each on
-//     their own ring (see its comment) so that the wide x tile is refilled in
-//     64-k chunks as soon as the MMAs release them;
+//   * prefill_split_kernel (tiles of 192+ rows): persistent, one CTA per SM;
+//     a stage slot holds the x tile and the dequantized A stage, freed by one
+//     commit, while the weights travel on a ring of their own (see its
+//     comment); the epilogue drains the accumulator into registers and stores
+//     from there while the next tile's MMAs run;
 //   * prefill_tcgen05_kernel (narrower tiles, and the A-in-shared-memory
-//     variant): one ring of 128-k stages carrying the x chunks, the packed
-//     words and the scale/zero rows -- one wait and one commit per stage,
-//     cheaper when a stage holds few MMA cycles.  Tiles of up to 64 rows use
-//     half an SM, so two CTAs (two issuers) share it.
+//     variant): one CTA per tile, one ring of 128-k stages carrying the x
+//     chunks, the packed words and the scale/zero rows -- one wait and one
+//     commit per stage, cheaper when a stage holds few MMA cycles.  Tiles of
+//     up to 64 rows use half an SM, so two CTAs (two issuers) share it; at the
+//     end the accumulator is staged as an fp16 tile in the drained ring and
+//     stored with one TMA copy.
 // In both, the 4, 8 or 16 dequantizing warps own one weight column (one TMEM
-// lane) per thread and split the stage's 16 packed rows; at the end they read
-// the accumulator out of tensor memory, stage the fp16 tile in the drained
-// ring and store it with one TMA copy.  Every wait is bounded in wall time; a
-// wait that gives up records W4A16_ERR_TIMEOUT and the kernel still frees its
-// tensor memory before it exits.
+// lane) per thread and split the stage's 16 packed rows, and run the
+// epilogue.  Every wait is bounded in wall time; a wait that gives up records
+// W4A16_ERR_TIMEOUT and the kernel still frees its tensor memory before it
+// exits.
 #include <mutex>
 
 #include "common.cuh"
