@@ -275,6 +275,16 @@ def test_gemm_prefill_persistent_tiles(K, group, warps):
     check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=256, warps_k=warps))
 
 
+def test_gemm_prefill_tile_groups():
+    """K = 8192: a 256-row x tile is 4 MB, so the tile order groups 8 of the 11
+    x row tiles and then the last 3 (a short last group); 15 x 11 = 165 tiles,
+    more than there are SMs."""
+    K, N, M = 8192, 1800, 2600
+    _, dev_w, ref_w = quantized(K, N, 128, 37, True)
+    x = synth.activations(M, K, seed=38)
+    check_gemm(x, dev_w, ref_w, 128, config=dict(path="prefill", tile_m=256))
+
+
 @pytest.mark.parametrize("group", [64, 256])
 def test_gemm_prefill_other_groups(group):
     K, N, M = 1024, 384, 200

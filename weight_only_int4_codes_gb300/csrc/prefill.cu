@@ -291,6 +291,7 @@ struct SplitArgs {
     int M, N, K, group;
     int tile_m;
     int n_tiles, tiles;        // weight-column tiles, all output tiles
+    int m_tiles, gm;           // x row tiles; row tiles per group of the tile order
     int xs, ws;                // stage slots (x in shared + A in tensor memory), weight slots
     int x_stage_bytes;         // two 64-k chunks of the x tile: tile_m * 256
     int x_chunk_bytes;         // tile_m * 128
@@ -302,6 +303,23 @@ struct SplitArgs {
     int tmem_cols, a_col0;
     unsigned long long timeout_ns;
 };
+
+// Output tile t of the persistent walk.  Tiles go in groups of `gm` x row
+// tiles: within a group the row tile runs fastest and the weight-column tile
+// slowest, so the CTAs resident at one time share a few weight tiles (read
+// from DRAM once, then from L2 by the group's other row tiles) and the group's
+// x rows stay in L2 while the group sweeps every weight column.  Without the
+// grouping the whole weight matrix would pass through L2 once per x row tile.
+__device__ __forceinline__ void split_tile(const SplitArgs &a, int t, int &m0, int &n0) {
+    const int per_group = a.gm * a.n_tiles;
+    const int g = t / per_group;
+    const int r = t - g * per_group;
+    const int left = a.m_tiles - g * a.gm;
+    const int gm = left < a.gm ? left : a.gm;
+    const int n = r / gm;
+    m0 = (g * a.gm + (r - n * gm)) * a.tile_m;
+    n0 = n * kTileN;
+}
 
 // Write 16 fp16 pairs of one thread -- column n (its TMEM lane), rows
 // r0 + 2j and r0 + 2j + 1 -- as 4-byte words: even and odd lanes swap halves
@@ -432,7 +450,8 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         const uint64_t pol_x = l2_evict_last_policy();
         int s = 0, r = 0;
         for (int t = blockIdx.x; t < a.tiles; t += gridDim.x) {
-            const int m0 = (t / a.n_tiles) * a.tile_m;
+            int m0, n0;
+            split_tile(a, t, m0, n0);
             for (int kt = 0; kt < KT; ++kt) {
                 if (r > 0 && !mbar_spin_bounded(&sempty[s], (r - 1) & 1, a.timeout_ns))
                     report_status(a.status, W4A16_ERR_TIMEOUT);
@@ -451,7 +470,8 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         const uint64_t pol_w = l2_evict_first_policy();
         int s = 0, r = 0;
         for (int t = blockIdx.x; t < a.tiles; t += gridDim.x) {
-            const int n0 = (t % a.n_tiles) * kTileN;
+            int m0, n0;
+            split_tile(a, t, m0, n0);
             int grow = 0, gnext = a.group;
             for (int kt = 0; kt < KT; ++kt) {
                 const int k0 = kt * kStageK;
@@ -555,8 +575,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                                     (uint32_t)((it - 1) & 1), a);
             }
             for (; kt < KT; ++kt) stage(kt);
-            pm0 = (t / a.n_tiles) * a.tile_m;
-            pn0 = (t % a.n_tiles) * kTileN;
+            split_tile(a, t, pm0, pn0);
         }
         if (it > 0)
             split_epilogue<NDQ>(lane_base, lane, n, part, pm0, pn0, accum_full, accum_empty,
@@ -661,7 +680,14 @@ cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cud
                       (uint64_t)a.N * 2, kTileN, sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     // persistent: one CTA per SM (at most one per tile)
-    const long long tiles = (long long)sa.n_tiles * ((a.M + sa.tile_m - 1) / sa.tile_m);
+    sa.m_tiles = (a.M + sa.tile_m - 1) / sa.tile_m;
+    // row tiles per group of the tile order: as many as keep the group's x
+    // rows (tile_m x K fp16 each) within 32 MB, a quarter of the L2
+    const long long x_tile_bytes = (long long)sa.tile_m * a.K * 2;
+    long long gm = (32ll << 20) / x_tile_bytes;
+    gm = gm < 1 ? 1 : (gm > sa.m_tiles ? sa.m_tiles : gm);
+    sa.gm = (int)gm;
+    const long long tiles = (long long)sa.n_tiles * sa.m_tiles;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     sa.tiles = (int)tiles;
     const int sms = device_info().sm_count;

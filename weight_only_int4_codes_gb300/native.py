@@ -45,6 +45,20 @@ class Config(ctypes.Structure):
             return None
         if isinstance(cfg, Config):
             return cfg
+        try:
+            key = tuple(sorted(cfg.items()))
+            hit = _cfg_cache.get(key)
+        except (AttributeError, TypeError):
+            key, hit = None, None
+        if hit is not None:
+            return hit
+        c = cls._build(cfg)
+        if key is not None and len(_cfg_cache) < 256:
+            _cfg_cache[key] = c
+        return c
+
+    @classmethod
+    def _build(cls, cfg):
         c = cls()
         for k, v in dict(cfg).items():
             if k == "path" and isinstance(v, str):
@@ -63,6 +77,7 @@ class Config(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+_cfg_cache = {}       # config dict items -> Config (read-only once built)
 
 
 def library_path() -> str:
@@ -101,19 +116,32 @@ def load_library():
         return lib
 
 
+def _lib_fast():
+    lib = _lib
+    return lib if lib is not None else load_library()
+
+
 def _check(status: int):
     if status != 0:
         msg = load_library().w4a16_last_error().decode(errors="replace")
         raise W4A16Error(status, msg)
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
 
 
 def _dev(t: torch.Tensor, name: str, dtype) -> int:
+    # fast path first: the per-call host cost matters at decode sizes
+    if type(t) is torch.Tensor and t.dtype is dtype and t.is_cuda and t.is_contiguous():
+        return t.data_ptr()
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
     if not t.is_cuda:
@@ -158,7 +186,7 @@ def gemm_ex(x, packed, scales, zeros, group: int = 128, out=None, config=None, s
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     cfg = Config.make(config)
-    _check(load_library().w4a16_gemm_ex(
+    _check(_lib_fast().w4a16_gemm_ex(
         _dev(x, "x", torch.float16), _dev(packed, "packed", torch.int32),
         _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
         _dev(out, "out", torch.float16), M, N, K, group,
@@ -172,7 +200,7 @@ def gemm(x, packed, scales, zeros, group: int = 128, out=None, stream=None):
     N = packed.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
-    _check(load_library().w4a16_gemm(
+    _check(_lib_fast().w4a16_gemm(
         _dev(x, "x", torch.float16), _dev(packed, "packed", torch.int32),
         _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
         _dev(out, "out", torch.float16), M, N, K, group, _stream_handle(stream)))
