@@ -100,7 +100,10 @@ typedef enum w4a16_path {
  */
 typedef struct w4a16_config {
     int path;       /* w4a16_path */
-    int split_k;    /* decode: CTAs of one cluster that split K (1..8) */
+    int split_k;    /* decode: CTAs of one cluster that split K (1..8);
+                       prefill: the same for the one-ring kernel (1..8; its
+                       CTAs' fp32 partials are summed in rank order by the
+                       cluster's first CTA; not with CTA pairs) */
     int warps_k;    /* decode, registers variant: warps per CTA that split K;
                        decode, TMA variant: consumer warps per CTA (4, 8 or 16;
                        4 lets three CTAs share an SM);

@@ -127,6 +127,15 @@ def test_plan_respects_requests():
     assert e.value.status == 2
 
 
+def test_prefill_split_k_requests():
+    p = w4.plan(64, 4096, 4096, 128, path="prefill", tile_m=64, split_k=4)
+    assert (p["path"], p["split_k"], p["tile_m"]) == (2, 4, 64)
+    for bad in (dict(split_k=9), dict(split_k=2, variant="pair")):
+        with pytest.raises(native.W4A16Error) as e:
+            w4.plan(64, 4096, 4096, 128, path="prefill", tile_m=64, **bad)
+        assert e.value.status == 2
+
+
 def test_auto_path_small_m_is_decode():
     for M in (1, 2, 4, 8, 16):
         p = w4.plan(M, 4096, 4096)

@@ -248,14 +248,14 @@ def test_gemm_prefill_cta_pair_groups(K, group):
     check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", variant="pair", tile_m=144))
 
 
-@pytest.mark.parametrize("tile_m", [112, 256])
+@pytest.mark.parametrize("tile_m,N", [(112, 264), (256, 264), (112, 7000)])
 @pytest.mark.parametrize("K,group", [(1088, 64), (1152, 192), (576, 192), (960, 320), (1024, 512)])
-def test_gemm_prefill_group_boundaries(K, group, tile_m):
+def test_gemm_prefill_group_boundaries(K, group, tile_m, N):
     """Stages are 128 k deep: groups of 64 (two scale rows per stage), groups
-    that start mid-stage (192, 320) and K with a half last stage (K % 128 == 64);
-    tile_m = 112 runs the one-ring kernel, 256 the split-ring kernel (x in
-    64-k chunks, so an odd chunk count ends in half a stage)."""
-    N, M = 264, 297
+    that start mid-stage (192, 320) and K with a half last stage (K % 128 == 64).
+    tile_m = 112 runs the one-ring kernel (N = 7000: 55 x 3 tiles, more than
+    there are SMs), 256 the persistent split-ring kernel."""
+    M = 297
     _, dev_w, ref_w = quantized(K, N, group, 17 + group, True)
     x = synth.activations(M, K, seed=18 + K)
     check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=tile_m))
@@ -273,6 +273,51 @@ def test_gemm_prefill_persistent_tiles(K, group, warps):
     _, dev_w, ref_w = quantized(K, N, group, 23 + K, True)
     x = synth.activations(M, K, seed=29 + K)
     check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=256, warps_k=warps))
+
+
+@pytest.mark.parametrize("split", [2, 3, 4, 8])
+@pytest.mark.parametrize("tile_m", [32, 64, 128])
+def test_gemm_prefill_split_k(split, tile_m):
+    """One-ring kernel with split-K across a cluster: each CTA takes a run of
+    the 17 stages (K = 2112 ends in half a stage), the first CTA sums the
+    others' fp32 partials in rank order; M and N ragged."""
+    K, N, M = 2112, 392, 100
+    cfg = dict(path="prefill", tile_m=tile_m, split_k=split)
+    try:
+        w4.plan(M, N, K, 64, **cfg)
+    except w4.native.W4A16Error as e:
+        # the leader's fp32 partial slots (64 KB each at tile_m = 128) leave
+        # no room for a ring of two stages from four CTAs on
+        assert e.status == 2 and tile_m == 128 and split >= 4
+        return
+    _, dev_w, ref_w = quantized(K, N, 64, 61, True)
+    x = synth.activations(M, K, seed=62)
+    out = check_gemm(x, dev_w, ref_w, 64, config=cfg)
+    again = w4.gemm_ex(to_dev(x), *dev_w, group=64, config=cfg)
+    torch.cuda.synchronize()
+    assert torch.equal(out, again)          # fixed summation order: bitwise reproducible
+
+
+@pytest.mark.parametrize("K,group,split", [(1088, 64, 3), (1152, 192, 2), (576, 192, 4),
+                                           (960, 320, 3), (256, 128, 4)])
+def test_gemm_prefill_split_k_groups(K, group, split):
+    """Split-K ranges that start inside a group (192, 320), groups of 64, and
+    more CTAs asked for than there are stages (K = 256: two stages, two CTAs)."""
+    N, M = 264, 45
+    _, dev_w, ref_w = quantized(K, N, group, 71 + group, True)
+    x = synth.activations(M, K, seed=73 + K)
+    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", tile_m=48, split_k=split))
+
+
+@pytest.mark.parametrize("tile_m", [16, 32, 64, 128])
+def test_gemm_prefill_one_ring_many_tiles(tile_m):
+    """The one-ring kernel with more output tiles than SMs (32 column tiles x
+    6..44 row tiles), two CTAs per SM up to 64 rows; K ends in half a stage, N
+    and M ragged."""
+    K, N, M = 576, 4000, 700
+    _, dev_w, ref_w = quantized(K, N, 64, 83, True)
+    x = synth.activations(M, K, seed=84)
+    check_gemm(x, dev_w, ref_w, 64, config=dict(path="prefill", tile_m=tile_m))
 
 
 def test_gemm_prefill_tile_groups():

@@ -282,12 +282,10 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
     } else if (c.path == W4A16_PATH_PREFILL) {
         if (c.tile_m <= 0) c.tile_m = default_tile_m(M, N);
         if (c.variant <= 0) c.variant = W4A16_PREFILL_A_TMEM;
-        // measured: 8 dequantizing warps for the narrower one-ring tiles (with
-        // 4, M = 32..64 on K=8192 N=28672 ran 25% slower); 4 for the wide
-        // split-ring tiles, as fast or faster and drawing less power, so the
-        // clock sits higher under the power cap
-        if (c.warps_k <= 0)
-            c.warps_k = (c.variant == W4A16_PREFILL_A_TMEM && c.tile_m >= 192) ? 4 : 8;
+        // measured: 4 dequantizing warps, on both kernels -- 1-3% ahead of 8
+        // at M = 32..4096 on both prefill shapes; fewer busy warps also draw
+        // less power, so the clock sits higher under the power cap
+        if (c.warps_k <= 0) c.warps_k = 4;
         if (!prefill_config_supported(c, M, N, K, group))
             return fail(W4A16_ERR_UNSUPPORTED, "prefill path not available for M=%d N=%d K=%d "
                         "group=%d tile_m=%d", M, N, K, group, c.tile_m);

@@ -61,6 +61,10 @@ struct PrefillArgs {
     int tx_bytes;
     int tmem_cols;         // allocated columns
     int a_col0;            // A-in-TMEM: first column of the A stage ring (D uses [0, tile_m))
+    int split;             // CTAs per cluster along K (gridDim.z); 1 = no split
+    int kt_per;            // 128-k stages per CTA of a split cluster
+    int red_off;           // leader: fp32 partial slots [split - 1][tile_m][128] (after the ring)
+    int bar_off;           // mbarriers
     unsigned long long timeout_ns;
 };
 
@@ -70,7 +74,9 @@ struct PrefillArgs {
 // ATMEM: the dequantized A operand lives in tensor memory (written with
 // tcgen05.st, read by the MMA as [a_tmem]) instead of shared memory; the
 // stage then carries only x, the packed words and the scale/zero rows.
-template <int NDQ, bool ATMEM>
+// SPLIT: split-K across a cluster along z (a separate instantiation, so that
+// the kernel without it carries none of its code).
+template <int NDQ, bool ATMEM, bool SPLIT>
 __global__ void __launch_bounds__(32 * (NDQ + 2), 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
@@ -79,16 +85,21 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + a.stages * a.stage_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + a.bar_off);
     uint64_t *aready = full + a.stages;      // dequantized A tile written
     uint64_t *empty = aready + a.stages;     // MMAs of the stage completed
     uint64_t *accum = empty + a.stages;      // all MMAs of the tile completed
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+    uint64_t *cl_done = accum + 1;           // split leader: the other CTAs' partials landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cl_done + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileN;
     const int m0 = blockIdx.y * a.tile_m;
     const int KT = (a.K + kStageK - 1) / kStageK;      // a last half stage reads zero x
+    // split-K: this CTA's stages [kt0, kt1) (the host makes every range non-empty)
+    const int kt0 = SPLIT ? (int)blockIdx.z * a.kt_per : 0;
+    const int kt1 = SPLIT ? (kt0 + a.kt_per < KT ? kt0 + a.kt_per : KT) : KT;
+    const int rank = SPLIT ? (int)cluster_ctarank() : 0;
 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_x);
@@ -102,6 +113,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             mbar_init(&empty[i], 1);
         }
         mbar_init(accum, 1);
+        mbar_init(cl_done, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -112,6 +124,14 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_d = *tmem_slot;
+    if constexpr (SPLIT) {
+        // the leader expects the other CTAs' partials as bulk-copy bytes; the
+        // first half of a split cluster barrier then publishes every CTA's
+        // barriers before any CTA signals another
+        if (rank == 0 && threadIdx.x == 0)
+            mbar_arrive_expect_tx(cl_done, (uint32_t)((a.split - 1) * a.tile_m * kTileN * 4));
+        cluster_arrive();
+    }
 
     // The producer and the MMA issuer are single threads whose loop bodies sit
     // on the critical path of every stage: their ring position is kept
@@ -124,7 +144,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         const uint64_t pol_w = l2_evict_first_policy();
         const uint64_t pol_x = l2_evict_last_policy();
         int s = 0, r = 0, grow = 0, gnext = a.group;
-        for (int kt = 0; kt < KT; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
             const int k0 = kt * kStageK;
             while (k0 >= gnext) { ++grow; gnext += a.group; }
             if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1, a.timeout_ns))
@@ -150,7 +170,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         const uint32_t b_chunk16 = (uint32_t)a.b_chunk_bytes >> 4;
         const uint32_t ring_u = smem_u32(ring);
         int s = 0, r = 0;
-        for (int kt = 0; kt < KT; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
             // the dequant warps arrive on `aready` only after they saw the
             // stage's copies land (`full`): one wait covers both
             if (!mbar_spin_bounded(&aready[s], r & 1, a.timeout_ns))
@@ -167,7 +187,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                 for (int kk = 0; kk < kStageK / 16; ++kk) {
                     const uint32_t c = kk / 4, w = kk % 4;
                     const uint64_t bd = b_desc + c * b_chunk16 + w * 2;
-                    const uint32_t acc = (kt | kk) != 0;
+                    const uint32_t acc = (kt != kt0) || (kk != 0);
                     if (ATMEM)
                         umma_f16_ts<1>(tmem_u, a_tmem + kk * 8, bd, idesc, acc);
                     else
@@ -193,7 +213,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                             : (((warp - kDeqWarp0) * 32 + lane) & (kTileN - 1));
         const int part = (warp - kDeqWarp0) / 4;          // which packed rows
         int s = 0, r = 0;
-        for (int kt = 0; kt < KT; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
             if (!mbar_wait_bounded(&full[s], r & 1, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
             const uint32_t st = smem_u32(ring + s * a.stage_bytes);
@@ -239,18 +259,50 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         const int q = warp & 3;                          // TMEM lane quarter of this warp
         const uint32_t taddr = tmem_d + ((uint32_t)(q * 32) << 16);
         const int epart = (warp - kDeqWarp0) / 4;        // warps of one quarter split the m chunks
-        // every copy has landed and every MMA has read its operands: the ring
-        // holds the fp16 output tile [tile_m][128], stored by one TMA copy
-        // (rows past M and columns past N are clipped by the tensor map)
-        stage_accumulator(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart, 32 * kParts);
-        fence_proxy_async_smem();
-        named_bar_sync(1, NDQ * 32);
-        if (warp == kDeqWarp0 && lane == 0) {
-            tma_store_2d(&tm_o, ring, n0, m0);
-            bulk_commit();
-            bulk_wait_all();
+        if (SPLIT && rank != 0) {
+            // split-K, not the leader: the fp32 partial tile [tile_m][128]
+            // goes into the drained ring, then with one bulk copy into slot
+            // rank - 1 of the leader's shared memory (completing bytes on the
+            // leader's cl_done); the CTA exits once the copy has read it
+            stage_partial_f32(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart,
+                              32 * kParts);
+            fence_proxy_async_smem();                    // the bulk copy reads these writes
+            named_bar_sync(1, NDQ * 32);
+            if (warp == kDeqWarp0 && lane == 0) {
+                cluster_wait();                          // the leader's barrier is initialized
+                const uint32_t bytes = (uint32_t)(a.tile_m * kTileN * 4);
+                bulk_copy_to_cluster(
+                    map_to_rank(smem_u32(ring + a.red_off) + (uint32_t)(rank - 1) * bytes, 0), ring,
+                    bytes, map_to_rank(smem_u32(cl_done), 0));
+                bulk_commit();
+                bulk_wait_read();
+            }
+        } else {
+            if (SPLIT && !mbar_wait_cluster_bounded(cl_done, 0, a.timeout_ns))
+                report_status(a.status, W4A16_ERR_TIMEOUT);
+            // every copy has landed and every MMA has read its operands: the
+            // ring holds the fp16 output tile [tile_m][128] -- this CTA's
+            // accumulator plus the other CTAs' partials in rank order -- stored
+            // by one TMA copy (rows past M and columns past N are clipped by
+            // the tensor map)
+            if constexpr (SPLIT)
+                stage_accumulator(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart,
+                                  32 * kParts, smem_u32(ring + a.red_off), a.split - 1);
+            else
+                stage_accumulator(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart,
+                                  32 * kParts);
+            fence_proxy_async_smem();
+            named_bar_sync(1, NDQ * 32);
+            if (warp == kDeqWarp0 && lane == 0) {
+                tma_store_2d(&tm_o, ring, n0, m0);
+                bulk_commit();
+                bulk_wait_all();
+            }
         }
     }
+    // every thread completes the split cluster barrier once (the non-leader's
+    // copying thread already has)
+    if (SPLIT && !(rank != 0 && warp == kDeqWarp0 && lane == 0)) cluster_wait();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc<1>(tmem_d, a.tmem_cols);
@@ -284,6 +336,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 constexpr int kSplitDeq0 = 3;
 constexpr int kTwoPerSmMaxTileM = 64;   // one-ring kernel: two CTAs per SM up to this tile
 constexpr int kSplitMinTileM = 192;     // measured crossover (128: one ring is faster)
+constexpr int kMaxPrefillSplit = 8;     // one-ring kernel: split-K cluster size (portable limit)
+constexpr int kMaxWeightSlots = 16;     // split-ring kernel: weight ring depth cap
 
 struct SplitArgs {
     int *status;
@@ -593,12 +647,35 @@ cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                   const CUtensorMap &tx, const CUtensorMap &tw,
                                   const CUtensorMap &ts, const CUtensorMap &tz,
                                   const CUtensorMap &to, const PrefillArgs &pa) {
+    if (pa.split <= 1) {
+        const cudaError_t attr = ensure_dynamic_smem(
+            (const void *)prefill_tcgen05_kernel<NDQ, ATMEM, false>, 227 * 1024);
+        if (attr != cudaSuccess) return attr;
+        prefill_tcgen05_kernel<NDQ, ATMEM, false><<<grid, 32 * (NDQ + 2), smem, stream>>>(
+            tx, tw, ts, tz, to, pa);
+        return cudaGetLastError();
+    }
+    if constexpr (!ATMEM) {
+        return cudaErrorNotSupported;     // split-K is built for A in tensor memory only
+    } else {
     const cudaError_t attr =
-        ensure_dynamic_smem((const void *)prefill_tcgen05_kernel<NDQ, ATMEM>, 227 * 1024);
+        ensure_dynamic_smem((const void *)prefill_tcgen05_kernel<NDQ, ATMEM, true>, 227 * 1024);
     if (attr != cudaSuccess) return attr;
-    prefill_tcgen05_kernel<NDQ, ATMEM><<<grid, 32 * (NDQ + 2), smem, stream>>>(tx, tw, ts, tz, to,
-                                                                              pa);
-    return cudaGetLastError();
+    // split-K: the CTAs of one output tile form a cluster along z
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(32 * (NDQ + 2), 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr1[1];
+    attr1[0].id = cudaLaunchAttributeClusterDimension;
+    attr1[0].val.clusterDim.x = 1;
+    attr1[0].val.clusterDim.y = 1;
+    attr1[0].val.clusterDim.z = (unsigned)pa.split;
+    lc.attrs = attr1;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, prefill_tcgen05_kernel<NDQ, ATMEM, true>, tx, tw, ts, tz, to, pa);
+    }
 }
 
 template <int NDQ>
@@ -617,14 +694,86 @@ int *status_word() {
     return kernel_status_address(&p) == cudaSuccess ? p : nullptr;
 }
 
+// Shared-memory and tensor-memory layout of the one-ring kernel for `cfg`
+// (tile_m, variant, split_k) and K; false when it does not fit.
+bool ring_layout(const w4a16_config &cfg, int K, int group, PrefillArgs &pa) {
+    pa.tile_m = cfg.tile_m;
+    // A operand in tensor memory unless the caller asks for shared memory
+    const bool atmem = cfg.variant != W4A16_PREFILL_A_SMEM;
+    // stage (128 k): [A (dequantized W^T, two 128 x 64 fp16 chunks) when in
+    // shared memory] | B (x tile: two tile_m x 64 fp16 chunks) | packed words
+    // (16 x 128) | scale rows | zero rows (1, or 2 when group % 128 != 0)
+    const int a_bytes = atmem ? 0 : kTileN * kStageK * 2;
+    pa.b_chunk_bytes = pa.tile_m * kChunkK * 2;              // tile_m % 16 == 0: 1024-aligned
+    pa.sz_rows = group % kStageK == 0 ? 1 : 2;
+    pa.b_off = a_bytes;
+    pa.p_off = pa.b_off + kChunks * pa.b_chunk_bytes;
+    pa.s_off = pa.p_off + kPackedRows * kTileN * 4;
+    pa.z_off = pa.s_off + pa.sz_rows * kTileN * 2;
+    pa.stage_bytes = round_up(pa.z_off + pa.sz_rows * kTileN * 2, 1024);
+    pa.tx_bytes = kChunks * pa.b_chunk_bytes + kPackedRows * kTileN * 4 + 2 * pa.sz_rows * kTileN * 2;
+    // split-K across a cluster of `split` CTAs along z, each with kt_per of
+    // the 128-k stages (every CTA gets at least one); the leader keeps the
+    // others' fp32 partials [split - 1][tile_m][128] after its ring
+    const int KT = (K + kStageK - 1) / kStageK;
+    int split = cfg.split_k > 1 ? cfg.split_k : 1;
+    if (split > kMaxPrefillSplit) return false;
+    pa.kt_per = (KT + split - 1) / split;
+    split = (KT + pa.kt_per - 1) / pa.kt_per;
+    pa.split = split;
+    const int red_bytes = (split - 1) * pa.tile_m * kTileN * 4;
+    pa.a_col0 = round_up(pa.tile_m, 32);
+    // Narrow tiles (up to 64 rows of x) are bound by the per-stage control
+    // path, not by the tensor core: two CTAs share an SM (half of its shared
+    // memory and of its tensor memory each), which doubles the stages in
+    // flight per SM -- unless a split leader's partial slots leave that half
+    // room for fewer than two stages.  Wider tiles take the whole SM.
+    auto ring_stages = [&](bool two_per_sm) {
+        const int budget = two_per_sm ? 104 * 1024 : 224 * 1024;
+        const int tmem_max = two_per_sm ? 256 : 512;
+        int st = (budget - red_bytes) / pa.stage_bytes;
+        st = st > 8 ? 8 : st;
+        // tensor memory: the accumulator (tile_m fp32 columns) and, with A in
+        // tensor memory, one 64-column A slot per stage
+        if (atmem) {
+            const int max_stages = (tmem_max - pa.a_col0) / (kStageK / 2);
+            st = st > max_stages ? max_stages : st;
+        }
+        return st;
+    };
+    int stages = ring_stages(atmem && pa.tile_m <= kTwoPerSmMaxTileM);
+    if (stages < 2) stages = ring_stages(false);
+    if (stages < 2) return false;
+    pa.stages = stages;
+    const int need = atmem ? pa.a_col0 + stages * (kStageK / 2) : pa.tile_m;
+    int cols = 32;
+    while (cols < need) cols *= 2;
+    pa.tmem_cols = cols;
+    // a split partner stages its fp32 partial in its drained ring
+    if (split > 1 && stages * pa.stage_bytes < pa.tile_m * kTileN * 4) return false;
+    pa.red_off = stages * pa.stage_bytes;
+    pa.bar_off = pa.red_off + red_bytes;
+    return true;
+}
+
 }  // namespace
 
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group) {
-    if (cfg.variant == W4A16_PREFILL_PAIR) return prefill_pair_supported(cfg, M, N, K, group);
+    if (cfg.split_k < 0 || cfg.split_k > kMaxPrefillSplit) return false;
+    if (cfg.split_k > 1 && cfg.variant == W4A16_PREFILL_A_SMEM) return false;
+    if (cfg.variant == W4A16_PREFILL_PAIR)
+        return cfg.split_k <= 1 && prefill_pair_supported(cfg, M, N, K, group);
     const bool warps_ok = cfg.warps_k == 0 || cfg.warps_k == 4 || cfg.warps_k == 8 ||
                           cfg.warps_k == 16;
-    return warps_ok && cfg.tile_m >= 16 && cfg.tile_m <= 256 && cfg.tile_m % 16 == 0 &&
-           group % kChunkK == 0 && K % kChunkK == 0 && N % 8 == 0 && (K / group) >= 1;
+    if (!(warps_ok && cfg.tile_m >= 16 && cfg.tile_m <= 256 && cfg.tile_m % 16 == 0 &&
+          group % kChunkK == 0 && K % kChunkK == 0 && N % 8 == 0 && (K / group) >= 1))
+        return false;
+    // the one-ring kernel (narrow tiles, A in shared memory, or split-K) must
+    // fit its ring and a split leader's partial slots
+    const bool one_ring = cfg.variant == W4A16_PREFILL_A_SMEM || cfg.split_k > 1 ||
+                          cfg.tile_m < kSplitMinTileM;
+    PrefillArgs pa;
+    return !one_ring || ring_layout(cfg, K, group, pa);
 }
 
 // Default variant (A in tensor memory) for wide tiles: the split-ring kernel.
@@ -647,17 +796,20 @@ cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cud
     sa.z_off = sa.s_off + sa.sz_rows * kTileN * 2;
     sa.w_stage_bytes = round_up(sa.z_off + sa.sz_rows * kTileN * 2, 1024);
     sa.w_tx = kPackedRows * kTileN * 4 + 2 * sa.sz_rows * kTileN * 2;
-    sa.ws = 3;
-    // stage slots: as many x tiles as shared memory holds next to the weight
-    // ring, and no more A stages than tensor memory holds next to the
-    // accumulator (tile_m fp32 columns)
+    // stage slots: as many x tiles as shared memory holds next to a weight
+    // ring of three, and no more A stages than tensor memory holds next to
+    // the accumulator (tile_m fp32 columns); then the weight ring takes what
+    // shared memory is left (deep for narrow tiles, whose small x slots leave
+    // room to keep more weight bytes in flight)
     const int budget = 224 * 1024;
-    int xs = (budget - sa.ws * sa.w_stage_bytes) / sa.x_stage_bytes;
+    int xs = (budget - 3 * sa.w_stage_bytes) / sa.x_stage_bytes;
     sa.a_col0 = round_up(sa.tile_m, 32);
     const int a_max = (512 - sa.a_col0) / (kStageK / 2);
     xs = xs > a_max ? a_max : xs;
     sa.xs = xs > 8 ? 8 : xs;
     if (sa.xs < 2) return cudaErrorNotSupported;
+    int ws = (budget - sa.xs * sa.x_stage_bytes) / sa.w_stage_bytes;
+    sa.ws = ws > kMaxWeightSlots ? kMaxWeightSlots : ws;
     int cols = 32;
     while (cols < sa.a_col0 + sa.xs * (kStageK / 2)) cols *= 2;
     sa.tmem_cols = cols;
@@ -705,10 +857,13 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     // Wide tiles: the split-ring kernel (its x ring runs far enough ahead to
     // cover the copy latency at 1024+ MMA cycles per stage).  Narrower tiles
     // are bound by the per-stage control path instead, where one ring (one
-    // wait and one commit per stage) is cheaper.
-    if (cfg.variant != W4A16_PREFILL_A_SMEM && cfg.tile_m >= kSplitMinTileM)
+    // wait and one commit per stage) is cheaper (measured: 11-13% faster at
+    // M = 32..128, K=4096 N=14336, than the split-ring kernel with a deep
+    // weight ring); split-K runs on the one-ring kernel too.
+    if (cfg.variant != W4A16_PREFILL_A_SMEM && cfg.split_k <= 1 && cfg.tile_m >= kSplitMinTileM)
         return launch_prefill_split(a, cfg, stream);
     PrefillArgs pa;
+    if (!ring_layout(cfg, a.K, a.group, pa)) return cudaErrorNotSupported;
     pa.out = a.out;
     pa.status = status_word();
     if (!pa.status) return cudaErrorInvalidDevice;
@@ -716,46 +871,11 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     pa.N = a.N;
     pa.K = a.K;
     pa.group = a.group;
-    pa.tile_m = cfg.tile_m;
-    // A operand in tensor memory unless the caller asks for shared memory
+    pa.timeout_ns = 1000000000ull;
     const bool atmem = cfg.variant != W4A16_PREFILL_A_SMEM;
     const int ndq = cfg.warps_k > 0 ? cfg.warps_k : 8;
-    // stage (128 k): [A (dequantized W^T, two 128 x 64 fp16 chunks) when in
-    // shared memory] | B (x tile: two tile_m x 64 fp16 chunks) | packed words
-    // (16 x 128) | scale rows | zero rows (1, or 2 when group % 128 != 0)
-    const int a_bytes = atmem ? 0 : kTileN * kStageK * 2;
-    pa.b_chunk_bytes = pa.tile_m * kChunkK * 2;              // tile_m % 16 == 0: 1024-aligned
-    pa.sz_rows = a.group % kStageK == 0 ? 1 : 2;
-    pa.b_off = a_bytes;
-    pa.p_off = pa.b_off + kChunks * pa.b_chunk_bytes;
-    pa.s_off = pa.p_off + kPackedRows * kTileN * 4;
-    pa.z_off = pa.s_off + pa.sz_rows * kTileN * 2;
-    pa.stage_bytes = round_up(pa.z_off + pa.sz_rows * kTileN * 2, 1024);
-    pa.tx_bytes = kChunks * pa.b_chunk_bytes + kPackedRows * kTileN * 4 + 2 * pa.sz_rows * kTileN * 2;
-    // Narrow tiles (up to 64 rows of x) are bound by the per-stage control
-    // path, not by the tensor core: two CTAs share an SM (half of its shared
-    // memory and of its tensor memory each), which doubles the stages in
-    // flight per SM.  Wider tiles take the whole SM.
-    const bool two_per_sm = atmem && pa.tile_m <= kTwoPerSmMaxTileM;
-    const int budget = two_per_sm ? 104 * 1024 : 224 * 1024;
-    const int tmem_max = two_per_sm ? 256 : 512;
-    int stages = budget / pa.stage_bytes;
-    stages = stages > 8 ? 8 : stages;
-    // tensor memory: the accumulator (tile_m fp32 columns) and, with A in
-    // tensor memory, one 64-column A slot per stage
-    pa.a_col0 = round_up(pa.tile_m, 32);
-    if (atmem) {
-        const int max_stages = (tmem_max - pa.a_col0) / (kStageK / 2);
-        stages = stages > max_stages ? max_stages : stages;
-    }
-    if (stages < 2) return cudaErrorNotSupported;
-    pa.stages = stages;
-    const int need = atmem ? pa.a_col0 + stages * (kStageK / 2) : pa.tile_m;
-    int cols = 32;
-    while (cols < need) cols *= 2;
-    pa.tmem_cols = cols;
-    pa.timeout_ns = 1000000000ull;
-    const size_t smem = (size_t)stages * pa.stage_bytes + (3 * stages + 1) * 8 + 16 + 1024;
+    const size_t smem = (size_t)pa.bar_off + (3 * pa.stages + 2) * 8 + 16 + 1024;
+    const int split = pa.split;
 
     // x as a 3-D view {64 k, M rows, K/64 chunks}: one box brings both 64-k
     // chunks of a stage, each a 128B-swizzled K-major tile
@@ -777,7 +897,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
 
     const int mtiles = (a.M + pa.tile_m - 1) / pa.tile_m;
     if (mtiles > 65535) return cudaErrorInvalidValue;
-    dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, 1);
+    dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, split);
 #define W4A16_PF(NDQ_, AT_) \
     launch_prefill_kernel<NDQ_, AT_>(grid, smem, stream, tx, tw, ts, tz, to, pa)
     if (atmem) {

@@ -86,10 +86,15 @@ __device__ __forceinline__ void store_accumulator(uint32_t taddr, int col, int m
 // Staged epilogue of one warp: its 32 TMEM lanes (weight columns n = lane
 // base + lane, one per thread) for the accumulator columns mc = first, first +
 // step, ... (rows of x) become an fp16 tile [tile_m][128] in shared memory at
-// `tile` (one 256-byte row per row of x), ready for one TMA store.  A warp's
-// 2-byte stores for one row cover 64 contiguous bytes.
+// `tile` (one 256-byte row per row of x), ready for one TMA store.  With
+// nred > 0 the fp32 partial tiles [tile_m][128] at red, red + tile_m * 512,
+// ... (the other CTAs of a split-K cluster, in rank order) are added to the
+// accumulator first, before the one rounding to fp16.  A warp's stores for
+// one row cover 64 contiguous bytes.
 __device__ __forceinline__ void stage_accumulator(uint32_t taddr, uint32_t tile, int n, int tile_m,
-                                                  int first, int step) {
+                                                  int first, int step, uint32_t red = 0,
+                                                  int nred = 0) {
+    const uint32_t slot = (uint32_t)tile_m * kTileN * 4;
     for (int mc = first; mc < tile_m; mc += step) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + mc, v);
@@ -97,11 +102,35 @@ __device__ __forceinline__ void stage_accumulator(uint32_t taddr, uint32_t tile,
 #pragma unroll
         for (int i = 0; i < 32; ++i)
             if (mc + i < tile_m) {
-                const uint16_t h = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+                float acc = __uint_as_float(v[i]);
+                const uint32_t e = (uint32_t)((mc + i) * kTileN + n) * 4;
+                for (int q = 0; q < nred; ++q) {
+                    float p;
+                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(p) : "r"(red + q * slot + e));
+                    acc += p;
+                }
+                const uint16_t h = __half_as_ushort(__float2half_rn(acc));
                 asm volatile("st.shared.u16 [%0], %1;" ::"r"(tile + ((mc + i) * kTileN + n) * 2),
                              "h"(h)
                              : "memory");
             }
+    }
+}
+
+// The fp32 partial of one warp's accumulator share (as above) as a tile
+// [tile_m][128] of floats at `tile`, for a split-K cluster's leader.
+__device__ __forceinline__ void stage_partial_f32(uint32_t taddr, uint32_t tile, int n, int tile_m,
+                                                  int first, int step) {
+    for (int mc = first; mc < tile_m; mc += step) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + mc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (mc + i < tile_m)
+                asm volatile("st.shared.b32 [%0], %1;" ::"r"(tile + ((mc + i) * kTileN + n) * 4),
+                             "r"(v[i])
+                             : "memory");
     }
 }
 
