@@ -214,9 +214,10 @@ def barrier(pg):
 
 
 # --------------------------------------------------------------- CPU oracle
-def oracle_calls(wl, cols):
+def oracle_calls(wl, cols, rows=None):
     """Inputs of one sampled step for the fp64 oracle: the first `cols` columns
-    of every weight (quantized once, offline) and the step's activations."""
+    of every weight (quantized once, offline) and the step's activations (their
+    first `rows` rows when given)."""
     import oracle
     from weight_only_int4_codes_gb300 import synth
     calls = []
@@ -227,6 +228,8 @@ def oracle_calls(wl, cols):
         qw = oracle.quantize_pack(W, GROUP)
         for M in wl["Ms"]:
             x = synth.activations(M, K, seed=synth.x_seed(wl["config"], M, shape_index=si))
+            if rows is not None:
+                x = x[:rows]
             calls.append((x, qw, weight_bytes(K, n)))
     return calls
 
@@ -263,19 +266,40 @@ def run_reference(args, rank, world, pg):
     if rank != 0:
         return
     import oracle
-    cols = args.ref_cols
-    calls = oracle_calls(wl, cols)
+    # The sample of a step: the first `cols` columns of every weight (and, if
+    # that is not enough, the first `rows` rows of every x), shrunk after a
+    # trial step until the whole run (warm-up and timed steps) fits the time
+    # budget (two minutes by default).  The trial step is the first warm-up
+    # step.  A step has a floor (one column, one row of x), so very many steps
+    # can still overrun the budget.
+    budget_s = args.ref_seconds
+    cols, rows = args.ref_cols, None
+    for _ in range(8):
+        calls = oracle_calls(wl, cols, rows)
+        t0 = time.perf_counter()
+        oracle_step(wl, calls)
+        projected = (time.perf_counter() - t0) * (args.steps + args.warmup)
+        if projected <= budget_s:
+            break
+        f = budget_s / projected
+        if cols > 1:
+            cols = max(1, int(cols * f))
+        elif rows != 1:
+            rows = max(1, int((rows or max(wl["Ms"])) * f))
+        else:
+            break
     bytes_step = sum(c[2] for c in calls) * wl["experts"]
     threads = oracle.num_threads()
-    for _ in range(max(args.warmup, 3)):          # untimed warm-up steps
+    for _ in range(max(args.warmup, 3) - 1):      # the other untimed warm-up steps
         oracle_step(wl, calls)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle_step(wl, calls)
     elapsed = time.perf_counter() - t0
     gbs = bytes_step * args.steps / elapsed / 1e9
-    sample = ("%d of each weight's columns (all K rows, all M in %s) per call, fp64 oracle "
-              "(quantize once, then dequantize + fp64 matmul per call)" % (cols, wl["Ms"]))
+    sample = ("%d of each weight's columns (all K rows, %s of x, M in %s) per call, fp64 oracle "
+              "(quantize once, then dequantize + fp64 matmul per call)"
+              % (cols, "all rows" if rows is None else "the first %d rows" % rows, wl["Ms"]))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4),
         "unit": "GB/s (weight stream)", "n_gpus": world, "steps": args.steps,
@@ -629,6 +653,8 @@ def main():
     ap.add_argument("--only-m", type=int, default=None,
                     help="profiling aid: keep only this M of the workload")
     ap.add_argument("--ref-cols", type=int, default=256)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: time budget of the whole run (the sample shrinks to fit)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     if args.only_shape is not None or args.only_m is not None:
