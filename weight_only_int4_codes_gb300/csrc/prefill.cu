@@ -311,8 +311,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 // ---------------------------------------------------------------------------
 // Split-ring kernel (the default for wide tiles, A in tensor memory).  It is
 // persistent: one CTA per SM walks the output tiles t = blockIdx.x, +gridDim.x,
-// ... (weight-column tile fastest), and its rings run on across tile
-// boundaries, so the next tile's copies and dequantization overlap the
+// ... (in the grouped order of split_tile below), and its rings run on across
+// tile boundaries, so the next tile's copies and dequantization overlap the
 // current tile's last MMAs and epilogue.  The weights travel on their own
 // ring, apart from the x tile:
 //   stage slots  xs slots, each holding one 128-k x tile (two 64-k chunks,
