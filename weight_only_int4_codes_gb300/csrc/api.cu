@@ -231,7 +231,6 @@ bool tma_variant_possible(int N, int group) {
 // (measured on GB300: at M = 16 the decode kernels are still ahead).
 constexpr int kDecodeMaxM = 16;
 
-// rows of x per prefill CTA: all of M up to 256, else 256
 // Rows of x per prefill CTA (measured on GB300): 256 from M = 256 up; below,
 // all of M in one tile -- except that for M <= 64 with fewer 128-column tiles
 // than SMs, a 128-row tile (one CTA per SM) beats narrow tiles two to an SM.

@@ -13,13 +13,14 @@
 //   * packed words land 128B-swizzled; consumer thread g reads 16-byte chunk
 //     perm(g) of its row, which makes every ld.shared.v4 conflict-free (the
 //     column permutation is undone when the results are stored).
-//   * 8 consumer warps split a stage: 32-column strips x 32-k steps.
+//   * 4, 8 or 16 consumer warps split a stage: 32-column strips x 32-k steps.
 //   * split-K across the CTAs of one thread-block cluster, reduced in a fixed
 //     order through distributed shared memory (no atomics, no workspace).
-//   * the CTA uses under half of an SM (about 100 KB of shared memory, 288
-//     threads), and signals programmatic dependent launch at its start, so the
-//     next GEMM on the stream can start streaming its weights while this one
-//     finishes.  Only x and out wait for the previous kernel (griddepcontrol).
+//   * the CTA uses under half of an SM (at most about 108 KB of shared memory;
+//     a third of one with 4 consumer warps), and signals programmatic
+//     dependent launch at its start, so the next GEMM on the stream can start
+//     streaming its weights while this one finishes.  Only x and out wait for
+//     the previous kernel (griddepcontrol).
 //   * every mbarrier wait is bounded in wall time; a wait that gives up records
 //     W4A16_ERR_TIMEOUT in the device status word and the kernel runs to its
 //     end without touching memory it does not own.
