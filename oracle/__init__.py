@@ -61,11 +61,12 @@ class Oracle:
         lib.oracle_double_to_half.argtypes = [ctypes.c_double]
         lib.oracle_double_to_half.restype = ctypes.c_uint16
         lib.oracle_quantize_pack.argtypes = [P, I, I, I, P, P, P, P]
+        lib.oracle_quantize_pack_symmetric.argtypes = [P, I, I, I, P, P, P, P]
         lib.oracle_unpack.argtypes = [P, I, I, P]
         lib.oracle_dequant.argtypes = [P, P, P, I, I, I, P]
         lib.oracle_gemm.argtypes = [P, P, P, P, I, I, I, I, P]
         lib.oracle_num_threads.argtypes = []
-        for f in (lib.oracle_quantize_pack, lib.oracle_unpack,
+        for f in (lib.oracle_quantize_pack, lib.oracle_quantize_pack_symmetric, lib.oracle_unpack,
                   lib.oracle_dequant, lib.oracle_gemm, lib.oracle_num_threads):
             f.restype = ctypes.c_int
         self.lib = lib
@@ -79,8 +80,10 @@ class Oracle:
         return int(self.lib.oracle_double_to_half(float(v)))
 
     # ------------------------------------------------------ quantize/pack
-    def quantize_pack(self, W, group: int = 128, return_codes: bool = False):
-        """W [K,N] fp16 -> (packed uint32 [K/8,N], scales fp16 [K/g,N], zeros fp16 [K/g,N])."""
+    def quantize_pack(self, W, group: int = 128, return_codes: bool = False,
+                      symmetric: bool = False):
+        """W [K,N] fp16 -> (packed uint32 [K/8,N], scales fp16 [K/g,N], zeros fp16 [K/g,N]).
+        symmetric=True: s = fp16(max|w| / 7), z = 8 (signed codes stored with +8)."""
         Wb = _as_half_bits(W)
         K, N = Wb.shape
         G = K // group if group > 0 else 0
@@ -88,8 +91,9 @@ class Oracle:
         scales = np.zeros((G, N), dtype=np.uint16)
         zeros = np.zeros((G, N), dtype=np.uint16)
         q = np.zeros((K, N), dtype=np.uint8) if return_codes else None
-        rc = self.lib.oracle_quantize_pack(_ptr(Wb), K, N, group, _ptr(packed), _ptr(scales),
-                                           _ptr(zeros), _ptr(q) if q is not None else None)
+        fn = self.lib.oracle_quantize_pack_symmetric if symmetric else self.lib.oracle_quantize_pack
+        rc = fn(_ptr(Wb), K, N, group, _ptr(packed), _ptr(scales), _ptr(zeros),
+                _ptr(q) if q is not None else None)
         _check(rc, "quantize_pack")
         out = (packed, scales.view(np.float16), zeros.view(np.float16))
         return out + (q,) if return_codes else out
@@ -165,8 +169,8 @@ def double_to_half(v: float) -> int:
     return default().double_to_half(v)
 
 
-def quantize_pack(W, group: int = 128, return_codes: bool = False):
-    return default().quantize_pack(W, group, return_codes)
+def quantize_pack(W, group: int = 128, return_codes: bool = False, symmetric: bool = False):
+    return default().quantize_pack(W, group, return_codes, symmetric)
 
 
 def unpack(packed):

@@ -148,6 +148,51 @@ int oracle_quantize_pack(const uint16_t *W, int K, int N, int group,
     return 0;
 }
 
+/*
+ * Symmetric variant (the pages test "symmetric and asymmetric quantization"
+ * and name the "+8 zero-point" of the symmetric packing): signed codes
+ * c in [-8, 7] stored as q = c + 8, so the zero is 8 and the dequantization
+ * (q - z) * s is the same.  Per (group j, column n):
+ *   a = max_k |W[k,n]|;  s = binary16(a / 7) (fp64 quotient, one rounding),
+ *   s = 1.0 if that rounds to 0;  z = 8;  q = clamp(rint(W / s) + 8, 0, 15).
+ */
+int oracle_quantize_pack_symmetric(const uint16_t *W, int K, int N, int group,
+                                   uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                   uint8_t *q_out)
+{
+    int rc = check_shape(K, N, group);
+    if (rc) return rc;
+    int G = K / group;
+    memset(packed, 0, sizeof(uint32_t) * (size_t)(K / 8) * (size_t)N);
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        for (int j = 0; j < G; ++j) {
+            double a = 0.0;
+            for (int k = j * group; k < (j + 1) * group; ++k) {
+                double w = fabs(oracle_half_to_double(W[(size_t)k * N + n]));
+                if (w > a) a = w;
+            }
+            uint16_t s_bits = oracle_double_to_half(a / 7.0);
+            double s = oracle_half_to_double(s_bits);
+            if (s == 0.0) {          /* all-zero group */
+                s_bits = 0x3c00;
+                s = 1.0;
+            }
+            scales[(size_t)j * N + n] = s_bits;
+            zeros[(size_t)j * N + n] = oracle_double_to_half(8.0);
+            for (int k = j * group; k < (j + 1) * group; ++k) {
+                double w = oracle_half_to_double(W[(size_t)k * N + n]);
+                double cd = rint(w / s) + 8.0;        /* signed code + 8 */
+                cd = cd < 0.0 ? 0.0 : (cd > 15.0 ? 15.0 : cd);
+                uint32_t code = (uint32_t)cd;
+                packed[(size_t)(k / 8) * N + n] |= code << (4 * (k % 8));
+                if (q_out) q_out[(size_t)k * N + n] = (uint8_t)code;
+            }
+        }
+    }
+    return 0;
+}
+
 /* Codes back out of the packed words: q[k,n] = (packed[k/8,n] >> 4*(k%8)) & 15. */
 int oracle_unpack(const uint32_t *packed, int K, int N, uint8_t *q)
 {

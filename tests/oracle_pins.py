@@ -146,6 +146,36 @@ def pin_golden_zero_from_rounded_scale(orc):
     assert wdq[:, 0].tolist() == [_hex16(h) for h in g["wdq_hex"]]
 
 
+def pin_golden_symmetric_8x4(orc):
+    g = json.load(open(os.path.join(GOLDEN, "hand_8x4_g8_symmetric.json")))
+    W = np.zeros((g["K"], g["N"]))
+    for n, col in g["columns"].items():
+        W[:, int(n)] = col["w"]
+    packed, scales, zeros = orc.quantize_pack(_f16_exact(W), group=g["group"], symmetric=True)
+    assert [int(v) for v in packed[0]] == [int(h, 16) for h in g["packed_hex"]]
+    assert scales.view(np.uint16)[0].tolist() == [_hex16(h) for h in g["scales_hex"]]
+    assert zeros.view(np.uint16)[0].tolist() == [_hex16(h) for h in g["zeros_hex"]]
+
+
+def pin_symmetric_invariants(orc):
+    """Symmetric quantizer on a random weight with outliers: z = 8 everywhere,
+    the scale is the fp16 rounding of max|w| / 7 (checked with numpy's
+    binary16), every code is within half a scale of w and never clipped, and
+    the codes c = q - 8 are odd-symmetric: quantizing -W gives -c (the
+    maximum magnitude maps to +-7, so -8 is never needed)."""
+    W = synth.weight(512, 16, seed=41, outliers=True)
+    packed, scales, zeros, q = orc.quantize_pack(W, group=128, return_codes=True, symmetric=True)
+    assert np.all(zeros.view(np.uint16) == 0x4800)
+    a = np.abs(W.astype(np.float64)).reshape(4, 128, 16).max(axis=1)
+    assert np.array_equal(scales, (a / 7.0).astype(np.float16))
+    s = np.repeat(scales.astype(np.float64), 128, axis=0)
+    c = q.astype(np.int64) - 8
+    assert np.all(np.abs(W.astype(np.float64) - c * s) <= s / 2 * (1 + 1e-12))
+    assert c.min() >= -7 and c.max() <= 7
+    _, _, _, qn = orc.quantize_pack(-W, group=128, return_codes=True, symmetric=True)
+    assert np.array_equal(qn.astype(np.int64) - 8, -c)
+
+
 def _hand_128x4():
     K = 128
     W = np.zeros((K, 4))
@@ -260,6 +290,8 @@ ALL_PINS = [
     pin_golden_8x8,
     pin_golden_128x4,
     pin_golden_zero_from_rounded_scale,
+    pin_golden_symmetric_8x4,
+    pin_symmetric_invariants,
     pin_dequant_closed_form,
     pin_gemm_one_hot,
     pin_gemm_linear,

@@ -52,6 +52,15 @@ MUTANTS = [
     ("codec_decode_bias",
      "v = ldexp((double)(1024 + frac), expo - 25);",
      "v = ldexp((double)(1024 + frac), expo - 24);"),
+    ("symmetric_missing_plus_8",
+     "double cd = rint(w / s) + 8.0;",
+     "double cd = rint(w / s);"),
+    ("symmetric_divisor_8",
+     "oracle_double_to_half(a / 7.0);",
+     "oracle_double_to_half(a / 8.0);"),
+    ("symmetric_max_not_absolute",
+     "double w = fabs(oracle_half_to_double(W[(size_t)k * N + n]));",
+     "double w = oracle_half_to_double(W[(size_t)k * N + n]);"),
     ("degenerate_scale_kept_zero",
      "s_bits = 0x3c00;     /* 1.0 */\n                s = 1.0;",
      "s_bits = 0x3c00;     /* 1.0 */\n                s = 1e-300;"),
