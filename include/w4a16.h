@@ -136,6 +136,27 @@ W4A16_API w4a16_status w4a16_quantize_pack(const uint16_t *W, int K, int N, int 
                                  cudaStream_t stream);
 
 /*
+ * Quantization modes of w4a16_quantize_pack_ex.
+ *   W4A16_QUANT_ASYMMETRIC  the min/max recipe above (w4a16_quantize_pack).
+ *   W4A16_QUANT_SYMMETRIC   signed codes stored with a +8 offset (page "Beating
+ *       FP16 with 4-bit Weights", section "Code": its tests cover symmetric
+ *       and asymmetric quantization; section "Things I got wrong along the
+ *       way": the +8 zero-point of the symmetric packing).  Per (group j,
+ *       column n):
+ *           s = fp16(max_k |W| / 7)    fp64 arithmetic, one rounding;
+ *                                      s = 1.0 if that rounds to 0
+ *           z = 8
+ *           q = clamp(rint(W / s) + 8, 0, 15)
+ *       so the largest magnitude codes as +-7 and the same (q - z) * s
+ *       dequantization, and every GEMM path, apply unchanged.
+ * An unknown mode returns W4A16_ERR_INVALID_ARG (checked first).
+ */
+enum { W4A16_QUANT_ASYMMETRIC = 0, W4A16_QUANT_SYMMETRIC = 1 };
+W4A16_API w4a16_status w4a16_quantize_pack_ex(const uint16_t *W, int K, int N, int group,
+                                    int mode, uint32_t *packed, uint16_t *scales,
+                                    uint16_t *zeros, cudaStream_t stream);
+
+/*
  * Dequantize the packed weight back to fp16: W_out[k,n] = fp16((q - z) * s),
  * one rounding of the exact product.  Test aid (bit-exact with the oracle).
  */

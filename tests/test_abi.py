@@ -76,6 +76,16 @@ def test_gemm_rejects_before_touching_the_gpu(lib):
     assert lib.w4a16_gemm(8, 16, 16, 16, 16, 1, 256, 512, 128, None) == 3
 
 
+def test_quantize_mode_is_checked_first(lib):
+    # an unknown mode is refused before anything else is looked at
+    assert lib.w4a16_quantize_pack_ex(None, 512, 256, 128, 2, None, None, None, None) == 1
+    assert b"mode" in lib.w4a16_last_error()
+    # known modes go on to the usual checks (null pointers here)
+    for mode in (0, 1):
+        assert lib.w4a16_quantize_pack_ex(None, 512, 256, 128, mode, None, None, None, None) == 1
+        assert b"null" in lib.w4a16_last_error()
+
+
 def test_grouped_rejects_before_touching_the_gpu(lib):
     P = ctypes.c_void_p
     good = (P * 2)(16, 32)

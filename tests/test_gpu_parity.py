@@ -81,6 +81,37 @@ def test_quantize_pack_and_dequantize_bit_exact(K, N, group, outliers):
                           oracle.dequant(*ref, group=group).view(np.uint16))
 
 
+@pytest.mark.parametrize("K,N,group,outliers", [
+    (512, 256, 128, False), (4096, 4096, 128, False), (4096, 14336, 128, True),
+    (256, 260, 128, False), (256, 64, 32, False), (512, 96, 64, True), (1024, 128, 256, False),
+])
+def test_quantize_symmetric_bit_exact(K, N, group, outliers):
+    """Symmetric quantizer (signed codes stored with +8): packed words,
+    scales, zeros and the dequantized weight bit-exact against the oracle."""
+    W = synth.weight(K, N, seed=synth.weight_seed(1) + 3 * K + N, outliers=outliers)
+    ref = oracle.quantize_pack(W, group, symmetric=True)
+    got = w4.quantize_pack(to_dev(W), group, symmetric=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(got[0].cpu().numpy().view(np.uint32), ref[0])
+    assert np.array_equal(got[1].cpu().numpy().view(np.uint16), ref[1].view(np.uint16))
+    assert np.array_equal(got[2].cpu().numpy().view(np.uint16), ref[2].view(np.uint16))
+    wdq = w4.dequantize(*got, group=group)
+    torch.cuda.synchronize()
+    assert np.array_equal(wdq.cpu().numpy().view(np.uint16),
+                          oracle.dequant(*ref, group=group).view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 300])
+def test_gemm_symmetric_weights(M):
+    """GEMM on symmetric-quantized weights, decode and prefill paths."""
+    K, N = 2048, 1024
+    W = synth.weight(K, N, seed=57, outliers=True)
+    ref_w = oracle.quantize_pack(W, 128, symmetric=True)
+    dev_w = w4.quantize_pack(to_dev(W), 128, symmetric=True)
+    x = synth.activations(M, K, seed=58 + M)
+    check_gemm(x, dev_w, ref_w, 128)
+
+
 def test_quantize_special_columns():
     """Constant, all-positive, all-negative, zero and subnormal-range groups."""
     K, N = 256, 16

@@ -324,6 +324,15 @@ extern "C" {
 
 w4a16_status w4a16_quantize_pack(const uint16_t *W, int K, int N, int group, uint32_t *packed,
                                  uint16_t *scales, uint16_t *zeros, cudaStream_t stream) {
+    return w4a16_quantize_pack_ex(W, K, N, group, W4A16_QUANT_ASYMMETRIC, packed, scales, zeros,
+                                  stream);
+}
+
+w4a16_status w4a16_quantize_pack_ex(const uint16_t *W, int K, int N, int group, int mode,
+                                    uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                    cudaStream_t stream) {
+    if (mode != W4A16_QUANT_ASYMMETRIC && mode != W4A16_QUANT_SYMMETRIC)
+        return fail(W4A16_ERR_INVALID_ARG, "unknown quantization mode %d", mode);
     w4a16_status st = check_shape(0, N, K, group);
     if (st != W4A16_OK) return st;
     if (N == 0) return W4A16_OK;
@@ -332,7 +341,8 @@ w4a16_status w4a16_quantize_pack(const uint16_t *W, int K, int N, int group, uin
     if (((uintptr_t)W & 1) || ((uintptr_t)packed & 3) || ((uintptr_t)scales & 1) ||
         ((uintptr_t)zeros & 1))
         return fail(W4A16_ERR_MISALIGNED, "pointer not aligned to its element size");
-    cudaError_t e = launch_quantize_pack(W, K, N, group, packed, scales, zeros, stream);
+    cudaError_t e = launch_quantize_pack(W, K, N, group, mode == W4A16_QUANT_SYMMETRIC, packed,
+                                         scales, zeros, stream);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "quantize_pack launch");
 }
 

@@ -44,7 +44,7 @@ struct GroupedGemmArgs {
 };
 
 // Each returns cudaSuccess or the launch error; they never synchronize.
-cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group,
+cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group, bool symmetric,
                                  uint32_t *packed, uint16_t *scales, uint16_t *zeros,
                                  cudaStream_t stream);
 cudaError_t launch_dequantize(const uint32_t *packed, const uint16_t *scales,

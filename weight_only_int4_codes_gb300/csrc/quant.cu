@@ -5,6 +5,11 @@
 // rows, eight 4-bit values per int32 along K; the codes are unsigned in [0,15]
 // and dequantize as (q - z) * s, the HQQ form of the GemLite README).
 //
+// Symmetric variant (the first page's tests cover symmetric and asymmetric
+// quantization; its "+8 zero-point" bug is the symmetric packing): signed
+// codes c = clamp(rint(w / s), -8, 7) stored as q = c + 8, z = 8, with
+// s = fp16(max|w| / 7) -- the largest magnitude maps to +-7.
+//
 // One thread owns one (group, column): it scans the group's rows for min/max,
 // forms s, z in fp64, then codes and packs the rows.  Neighbouring threads own
 // neighbouring columns, so every load and store is coalesced along N.  The
@@ -19,7 +24,7 @@ namespace {
 constexpr int kQuantThreads = 128;
 
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_pack_kernel(const __half *__restrict__ W, int K, int N, int group,
+quantize_pack_kernel(const __half *__restrict__ W, int K, int N, int group, bool symmetric,
                      uint32_t *__restrict__ packed, __half *__restrict__ scales,
                      __half *__restrict__ zeros)
 {
@@ -34,16 +39,21 @@ quantize_pack_kernel(const __half *__restrict__ W, int K, int N, int group,
         mn = fminf(mn, v);
         mx = fmaxf(mx, v);
     }
-    // difference and quotient in fp64, one rounding to binary16 (RN-even)
-    __half sh = __double2half(((double)mx - (double)mn) / 15.0);
+    // difference (or largest magnitude) and quotient in fp64, one rounding to
+    // binary16 (RN-even)
+    __half sh = symmetric ? __double2half(fmax(-(double)mn, (double)mx) / 7.0)
+                          : __double2half(((double)mx - (double)mn) / 15.0);
     double s = (double)__half2float(sh);
-    if (s == 0.0) {                                 // degenerate (constant) group
+    if (s == 0.0) {                                 // degenerate (constant or all-zero) group
         sh = __float2half_rn(1.0f);
         s = 1.0;
     }
-    double zr = rint(-(double)mn / s);
-    zr = fmin(fmax(zr, 0.0), 15.0);
-    const int z = (int)zr;                          // +0 for a clamped -0
+    int z = 8;
+    if (!symmetric) {
+        double zr = rint(-(double)mn / s);
+        zr = fmin(fmax(zr, 0.0), 15.0);
+        z = (int)zr;                                // +0 for a clamped -0
+    }
     scales[(size_t)j * N + n] = sh;
     zeros[(size_t)j * N + n] = __int2half_rn(z);
     for (int r = 0; r < group / 8; ++r) {
@@ -87,13 +97,13 @@ dequantize_kernel(const uint32_t *__restrict__ packed, const __half *__restrict_
 
 }  // namespace
 
-cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group,
+cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group, bool symmetric,
                                  uint32_t *packed, uint16_t *scales, uint16_t *zeros,
                                  cudaStream_t stream)
 {
     dim3 grid((N + kQuantThreads - 1) / kQuantThreads, K / group < 65535 ? K / group : 65535);
     quantize_pack_kernel<<<grid, kQuantThreads, 0, stream>>>(
-        reinterpret_cast<const __half *>(W), K, N, group, packed,
+        reinterpret_cast<const __half *>(W), K, N, group, symmetric, packed,
         reinterpret_cast<__half *>(scales), reinterpret_cast<__half *>(zeros));
     return cudaGetLastError();
 }

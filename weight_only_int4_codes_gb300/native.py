@@ -24,6 +24,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4:
 PATHS = {"auto": 0, "decode": 1, "prefill": 2}
 VARIANTS = {"auto": 0, "tma": 1, "registers": 2,      # decode path
             "tmem": 1, "smem": 2, "pair": 3}       # prefill path: A's home, CTA pairs
+QUANT_ASYMMETRIC, QUANT_SYMMETRIC = 0, 1
 FLAG_PDL = 0x1
 FLAG_TEST_TIMEOUT = 0x100
 
@@ -98,6 +99,7 @@ def load_library():
         P, I = ctypes.c_void_p, ctypes.c_int
         sig = {
             "w4a16_quantize_pack": [P, I, I, I, P, P, P, P],
+            "w4a16_quantize_pack_ex": [P, I, I, I, I, P, P, P, P],
             "w4a16_dequantize": [P, P, P, P, I, I, I, P],
             "w4a16_gemm": [P, P, P, P, P, I, I, I, I, P],
             "w4a16_gemm_ex": [P, P, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
@@ -153,14 +155,16 @@ def _dev(t: torch.Tensor, name: str, dtype) -> int:
     return t.data_ptr()
 
 
-def quantize_pack(W: torch.Tensor, group: int = 128, stream=None):
-    """fp16 W [K,N] -> (packed int32 [K/8,N], scales fp16 [K/g,N], zeros fp16 [K/g,N])."""
+def quantize_pack(W: torch.Tensor, group: int = 128, stream=None, symmetric: bool = False):
+    """fp16 W [K,N] -> (packed int32 [K/8,N], scales fp16 [K/g,N], zeros fp16 [K/g,N]).
+    symmetric=True: s = fp16(max|w| / 7), z = 8 (signed codes stored with +8)."""
     K, N = W.shape
     packed = torch.empty((K // 8, N), dtype=torch.int32, device=W.device)
     scales = torch.empty((K // group, N), dtype=torch.float16, device=W.device)
     zeros = torch.empty((K // group, N), dtype=torch.float16, device=W.device)
-    _check(load_library().w4a16_quantize_pack(
-        _dev(W, "W", torch.float16), K, N, group, _dev(packed, "packed", torch.int32),
+    _check(load_library().w4a16_quantize_pack_ex(
+        _dev(W, "W", torch.float16), K, N, group, QUANT_SYMMETRIC if symmetric else QUANT_ASYMMETRIC,
+        _dev(packed, "packed", torch.int32),
         _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
         _stream_handle(stream)))
     return packed, scales, zeros
