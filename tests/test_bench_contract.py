@@ -49,3 +49,19 @@ def test_reference_arm_bounds_its_sample():
     assert d["steps"] == 100
     assert "columns" in d["cpu_baseline"]["sample"]
     assert d["ms_per_step"] * 100 / 1e3 < 20                   # the timed steps fit the budget
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched like the multi-GPU bench (torchrun, two ranks; gloo here): rank 0
+    alone runs the oracle and prints the line, the other rank exits 0."""
+    r = subprocess.run(
+        [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+         "--master-addr", "127.0.0.1", "--master-port", "29547",
+         os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "3"],
+        capture_output=True, text=True, timeout=600, cwd=ROOT,
+        env=dict(os.environ, CUDA_VISIBLE_DEVICES="", W4A16_BENCH_BACKEND="gloo"))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
