@@ -76,7 +76,9 @@ typedef enum w4a16_path {
                                 kernel streams its weights before waiting for the
                                 previous kernel on the stream.  Only valid when
                                 packed/scales/zeros are NOT written by the kernel
-                                immediately before it on the same stream. */
+                                immediately before it on the same stream.  Decode
+                                kernels only; the prefill kernels are compute-bound
+                                and always launch in stream order. */
 #define W4A16_FLAG_TEST_TIMEOUT 0x100  /* test aid (TMA decode kernel only): arm the
                                 last pipeline stage without loading it, so its
                                 bounded wait runs out (5 ms); the output is
@@ -91,8 +93,6 @@ typedef enum w4a16_path {
 /* Prefill kernel variants (w4a16_config.variant on the prefill path). */
 #define W4A16_PREFILL_A_TMEM 1    /* dequantized W^T operand in tensor memory (default) */
 #define W4A16_PREFILL_A_SMEM 2    /* dequantized W^T operand in shared memory */
-#define W4A16_PREFILL_PAIR 3      /* CTA pairs (cta_group::2): UMMA M = 256, each CTA
-                                     holds 128 weight columns and half of the x tile */
 
 /*
  * Launch configuration of one GEMM call.  Zero in any field means "choose
@@ -103,15 +103,15 @@ typedef struct w4a16_config {
     int split_k;    /* decode: CTAs of one cluster that split K (1..8);
                        prefill: the same for the one-ring kernel (1..8; its
                        CTAs' fp32 partials are summed in rank order by the
-                       cluster's first CTA; not with CTA pairs) */
+                       cluster's first CTA) */
     int warps_k;    /* decode, registers variant: warps per CTA that split K;
                        decode, TMA variant: consumer warps per CTA (4, 8 or 16;
                        4 lets three CTAs share an SM);
-                       prefill: dequantizing warps (4, 8 or 16; 4 or 8 for CTA pairs) */
+                       prefill: dequantizing warps (4, 8 or 16) */
     int warps_n;    /* decode: 32-column strips per CTA (TMA variant: 2 or 4) */
     int steps;      /* decode: K per warp in 32-row steps (registers variant) or
                        K per CTA in 256-row stages (TMA variant) */
-    int tile_m;     /* prefill: rows of x per CTA (CTA pair) tile (16..256, multiple of 16) */
+    int tile_m;     /* prefill: rows of x per CTA tile (16..256, multiple of 16) */
     int flags;      /* W4A16_FLAG_* */
     int variant;    /* decode: W4A16_DECODE_*; prefill: W4A16_PREFILL_* */
 } w4a16_config;
@@ -217,9 +217,16 @@ W4A16_API w4a16_status w4a16_gemm_grouped(int E, const uint16_t *const *x,
 W4A16_API w4a16_status w4a16_plan(int M, int N, int K, int group, const w4a16_config *request,
                         w4a16_config *plan_out);
 
-/* Reads and clears the device-side status word that bounded waits inside the
- * kernels set when they give up (W4A16_ERR_TIMEOUT), after synchronizing
- * `stream`.  W4A16_OK if no kernel reported a problem. */
+/* Reads and clears, in one atomic exchange on the device, the status word that
+ * bounded waits inside the kernels set when they give up (W4A16_ERR_TIMEOUT).
+ * The exchange is queued on `stream` after the work already there, and the
+ * call returns once it has run.  W4A16_OK if no kernel reported a problem.
+ * The word is one per device, shared by every stream: the status covers every
+ * kernel of this library on the current device that finished before the
+ * exchange ran, whichever stream it ran on; a kernel still running on another
+ * stream reports at the next call.  A bounded wait's limit is counted from
+ * after its kernel's wait for the previous kernel on the stream (programmatic
+ * dependent launch), so a long-running predecessor never causes a timeout. */
 W4A16_API w4a16_status w4a16_get_kernel_status(cudaStream_t stream);
 
 /* Message for the last non-OK status returned to the calling thread

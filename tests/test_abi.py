@@ -140,7 +140,7 @@ def test_plan_respects_requests():
 def test_prefill_split_k_requests():
     p = w4.plan(64, 4096, 4096, 128, path="prefill", tile_m=64, split_k=4)
     assert (p["path"], p["split_k"], p["tile_m"]) == (2, 4, 64)
-    for bad in (dict(split_k=9), dict(split_k=2, variant="pair"), dict(split_k=2, variant="smem"),
+    for bad in (dict(split_k=9), dict(split_k=2, variant=3), dict(split_k=2, variant="smem"),
                 dict(split_k=4, tile_m=128, warps_k=4)):
         with pytest.raises(native.W4A16Error) as e:
             w4.plan(64, 4096, 4096, 128, path="prefill", **dict(dict(tile_m=64), **bad))

@@ -256,29 +256,6 @@ def test_gemm_prefill_dequant_warps(warps, variant):
                config=dict(path="prefill", warps_k=warps, variant=variant, tile_m=256))
 
 
-@pytest.mark.parametrize("warps", [4, 8])
-@pytest.mark.parametrize("M,tile_m", [(16, 16), (100, 48), (300, 128), (600, 256), (257, 256)])
-def test_gemm_prefill_cta_pair(M, tile_m, warps):
-    """CTA-pair kernel (cta_group::2, UMMA M = 256): each CTA holds 128 weight
-    columns and half of the x tile; N ragged against the 256-column pair tile,
-    M ragged against tile_m."""
-    K, N = 2048, 392
-    _, dev_w, ref_w = quantized(K, N, 128, 81, True)
-    x = synth.activations(M, K, seed=82 + M)
-    check_gemm(x, dev_w, ref_w, 128,
-               config=dict(path="prefill", variant="pair", tile_m=tile_m, warps_k=warps))
-
-
-@pytest.mark.parametrize("K,group", [(1088, 64), (1152, 192), (576, 192), (960, 320)])
-def test_gemm_prefill_cta_pair_groups(K, group):
-    """Groups of 64, groups starting mid-stage, a half last stage; N = 520
-    leaves the odd CTA of the last pair entirely past N."""
-    N, M = 520, 131
-    _, dev_w, ref_w = quantized(K, N, group, 17 + group, True)
-    x = synth.activations(M, K, seed=19 + K)
-    check_gemm(x, dev_w, ref_w, group, config=dict(path="prefill", variant="pair", tile_m=144))
-
-
 @pytest.mark.parametrize("tile_m,N", [(112, 264), (256, 264), (112, 7000)])
 @pytest.mark.parametrize("K,group", [(1088, 64), (1152, 192), (576, 192), (960, 320), (1024, 512)])
 def test_gemm_prefill_group_boundaries(K, group, tile_m, N):
@@ -406,7 +383,6 @@ def test_gemm_random_encodings():
     (9, dict(path="decode", variant="tma", warps_k=16)),
     (64, dict(path="prefill", tile_m=64)), (128, dict(path="prefill", tile_m=128)),
     (300, dict(path="prefill", tile_m=256)), (300, dict(path="prefill", variant="smem", tile_m=128)),
-    (300, dict(path="prefill", variant="pair", tile_m=256)),
 ])
 def test_one_hot_is_exact(M, config):
     """x = e_k: a single nonzero product, so out equals the dequantized row
@@ -427,7 +403,6 @@ def test_one_hot_is_exact(M, config):
 
 
 @pytest.mark.parametrize("config", [dict(path="prefill", tile_m=256),
-                                    dict(path="prefill", variant="pair", tile_m=256),
                                     dict(path="prefill", tile_m=64)])
 def test_prefill_zero_input_dirty_output_determinism(config):
     """The tcgen05 kernels overwrite every output element (NaN-filled out),

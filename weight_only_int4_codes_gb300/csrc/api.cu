@@ -12,17 +12,28 @@
 namespace w4a16 {
 
 __device__ int g_kernel_status = 0;
+__device__ int g_kernel_status_taken = 0;
 
 cudaError_t kernel_status_address(int **ptr) {
     return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_kernel_status);
 }
 
-cudaError_t kernel_status_read_clear(int *value) {
-    int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(value, g_kernel_status, sizeof(int));
-    if (e == cudaSuccess && *value != 0)
-        e = cudaMemcpyToSymbol(g_kernel_status, &zero, sizeof(int));
-    return e;
+namespace {
+// Swaps the status word with zero in one atomic step, so a status set by a
+// kernel between a read and a clear can never be lost.
+__global__ void status_take_kernel() { g_kernel_status_taken = atomicExch(&g_kernel_status, 0); }
+}  // namespace
+
+cudaError_t kernel_status_read_clear(int *value, cudaStream_t stream) {
+    static std::mutex mu;   // one taker at a time: the snapshot word is shared
+    std::lock_guard<std::mutex> lock(mu);
+    status_take_kernel<<<1, 1, 0, stream>>>();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbolAsync(value, g_kernel_status_taken, sizeof(int), 0,
+                                  cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
 }
 
 namespace {
@@ -471,7 +482,7 @@ w4a16_status w4a16_get_kernel_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     int v = 0;
-    e = kernel_status_read_clear(&v);
+    e = kernel_status_read_clear(&v, stream);
     if (e != cudaSuccess) return cuda_fail(e, "read/clear the device status word");
     if (v != 0)
         return fail((w4a16_status)v, "a kernel reported status %d (bounded wait gave up)", v);

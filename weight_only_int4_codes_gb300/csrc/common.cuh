@@ -11,10 +11,12 @@ namespace w4a16 {
 
 // Device-side status word: kernels with bounded waits receive its address and
 // write W4A16_ERR_TIMEOUT there (first writer wins) when a wait gives up;
-// w4a16_get_kernel_status reads and clears it.  The word lives in api.cu
-// (one copy per device); these host helpers are the only way to reach it.
-cudaError_t kernel_status_address(int **ptr);        // current device
-cudaError_t kernel_status_read_clear(int *value);    // current device, synchronous
+// w4a16_get_kernel_status swaps it with zero (one atomic exchange on the
+// device, after the work queued on `stream`).  The word lives in api.cu (one
+// copy per device, shared by every stream); these host helpers are the only
+// way to reach it.
+cudaError_t kernel_status_address(int **ptr);                             // current device
+cudaError_t kernel_status_read_clear(int *value, cudaStream_t stream);    // synchronous
 
 __device__ __forceinline__ void report_status(int *status, int code) {
     atomicCAS(status, 0, code);
@@ -68,8 +70,6 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
 // Prefill path (tcgen05).  Returns cudaErrorNotSupported if unavailable.
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group);
-cudaError_t launch_prefill_pair(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
-bool prefill_pair_supported(const w4a16_config &cfg, int M, int N, int K, int group);
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (device, kernel): the attribute belongs to the device's

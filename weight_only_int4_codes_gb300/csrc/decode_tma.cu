@@ -33,27 +33,6 @@
 
 namespace w4a16 {
 
-#ifdef W4A16_TRACE
-// Optional timeline instrumentation (compiled only with -DW4A16_TRACE):
-// per CTA, clock64 offsets of: [0] entry (globaltimer), [1] smid, [2] barriers
-// ready, [3] producer done issuing, [4..11] consumer warp 0 got stage s,
-// [12] main loop done, [13] epilogue done; [14..15] compute of stages 0/1
-// done; [16] consumers' griddepcontrol.wait returned; [17] CTA partial
-// written; [18] leader: every partial landed.  Across launches: g_trace_launch[i] = {globaltimer at the entry of the
-// launch's first CTA, at the producer's griddepcontrol.wait return, at the
-// leader's final store} for the i-th launch (slot from g_trace_next).
-__device__ unsigned long long g_trace[4096][24];
-__device__ unsigned long long g_trace_launch[64][4];
-__device__ unsigned int g_trace_next;
-#define W4A16_TRACE_AT(slot, v)                                                         \
-    do {                                                                                 \
-        const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z); \
-        if (cta_ < 4096) g_trace[cta_][slot] = (v);                                     \
-    } while (0)
-#else
-#define W4A16_TRACE_AT(slot, v) do { } while (0)
-#endif
-
 namespace {
 
 constexpr int kStageRows = 32;                 // packed rows per stage
@@ -123,21 +102,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     const int Mc = min(16, a.M - m_base);
 
     pdl_launch_dependents();
-#ifdef W4A16_TRACE
-    __shared__ unsigned trace_slot;
-    if (threadIdx.x == 0) {
-        const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-        trace_slot = cta_ == 0 ? (atomicAdd(&g_trace_next, 1u) & 63u) : 64u;
-        if (trace_slot < 64) g_trace_launch[trace_slot][0] = globaltimer_ns();
-    }
-    const long long t_entry = clock64();
-    if (threadIdx.x == 0) {
-        unsigned smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        W4A16_TRACE_AT(0, globaltimer_ns());
-        W4A16_TRACE_AT(1, smid);
-    }
-#endif
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
@@ -154,9 +118,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     // first half of a split cluster barrier: every CTA's barriers exist before
     // any CTA signals another (the wait comes just before the reduction)
     if (a.split > 1) cluster_arrive();
-#ifdef W4A16_TRACE
-    if (threadIdx.x == 0) W4A16_TRACE_AT(2, clock64() - t_entry);
-#endif
 
     float acc[NT][2][4];
 #pragma unroll
@@ -195,9 +156,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 tma_load_2d(slot + a.z_off, &tm_z, &full[st], col_base, grow, pol_stream);
             }
             pdl_wait();   // x may be the previous kernel's output
-#ifdef W4A16_TRACE
-            if (trace_slot < 64) g_trace_launch[trace_slot][1] = globaltimer_ns();
-#endif
             for (int st = 0; st < first; ++st) {
                 if (st == skip) continue;
                 tma_load_2d(ring + st * a.stage_bytes + a.x_off, &tm_x, &full[st],
@@ -231,9 +189,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 grow += gstep;
                 if (++slot == a.stages) { slot = 0; ++round; }
             }
-#ifdef W4A16_TRACE
-            W4A16_TRACE_AT(3, clock64() - t_entry);
-#endif
             // no copy of this CTA may still be landing when it exits (normally
             // the consumers have long seen every stage complete; after a
             // timed-out wait this bounds the rest)
@@ -251,9 +206,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         // spinning on the stage barriers and stealing issue slots from the
         // previous kernel's warps on the same SM.
         pdl_wait();
-#ifdef W4A16_TRACE
-        if (threadIdx.x == 0) W4A16_TRACE_AT(16, clock64() - t_entry);
-#endif
         const int x0_row = g < Mc ? g : 0;         // rows past M read row 0, then zeroed
         const int x1_row = g + 8 < Mc ? g + 8 : 0;
         const bool x0_ok = g < Mc, x1_ok = g + 8 < Mc;
@@ -262,9 +214,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         for (int st = 0; st < n_st; ++st) {
             if (!mbar_wait_bounded(&full[slot], phase, a.timeout_ns))
                 report_status(a.status, W4A16_ERR_TIMEOUT);
-#ifdef W4A16_TRACE
-            if (threadIdx.x == 0 && st < 8) W4A16_TRACE_AT(4 + st, clock64() - t_entry);
-#endif
             const uint32_t base = smem_u32(ring) + slot * a.stage_bytes;
             const uint32_t wtile = base + wn * 4096;
             const int r0 = wk * 4 * SPW;                // first row of this warp in the stage
@@ -312,22 +261,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 if (!ONE_GROUP) flush_group_split<NT>(acc, gs, k);
             }
             if (ONE_GROUP) flush_group_split<NT>(acc, gs, k);
-#ifdef W4A16_TRACE
-            if (threadIdx.x == 0 && st < 2) {
-                // make the timestamp wait for this stage's arithmetic
-                float sink = 0.f;
-#pragma unroll
-                for (int p = 0; p < NT; ++p) sink += acc[p][0][0] + acc[p][1][3];
-                W4A16_TRACE_AT(14 + st, (clock64() - t_entry) + (sink == 12345.f ? 1 : 0));
-            }
-#endif
         }
     }
 
     // ---------------------------------------------------------- epilogue
-#ifdef W4A16_TRACE
-    if (threadIdx.x == 0) W4A16_TRACE_AT(12, clock64() - t_entry);
-#endif
     // The consumer warps sum their fragment partials in shared memory (fixed
     // warp order) into this CTA's partial tile [Mc][BN].  With split-K, every
     // CTA but the cluster leader (rank 0) then ships its tile with one bulk
@@ -356,9 +293,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
             for (int w = 0; w < WK; ++w) v += red[(w * MB + m) * BN + c];
             mine[e] = v;
         }
-#ifdef W4A16_TRACE
-        if (threadIdx.x == 0) W4A16_TRACE_AT(17, clock64() - t_entry);
-#endif
         if (a.split > 1 && rank != 0) {
             fence_proxy_async_smem();              // the bulk copy reads these writes
             named_bar_sync(1, kConsumerWarps * 32);
@@ -375,9 +309,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         // the producer warp and the non-leader consumers only complete the
         // split cluster barrier (thread 0 already waited on it)
         if (threadIdx.x != 0) cluster_wait();
-#ifdef W4A16_TRACE
-        if (threadIdx.x == 0) W4A16_TRACE_AT(13, clock64() - t_entry);
-#endif
         return;
     }
     __syncthreads();                               // the leader's own partial is in slot 0
@@ -386,13 +317,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         if (!mbar_wait_cluster_bounded(cl_done, 0, a.timeout_ns))
             report_status(a.status, W4A16_ERR_TIMEOUT);
     }
-#ifdef W4A16_TRACE
-    if (threadIdx.x == 0) W4A16_TRACE_AT(18, clock64() - t_entry);
-#endif
     pdl_wait();        // out may still be in use by the previous kernel
-#ifdef W4A16_TRACE
-    if (threadIdx.x == 0 && trace_slot < 64) g_trace_launch[trace_slot][2] = globaltimer_ns();
-#endif
     for (int e = threadIdx.x; e < E; e += kThreads) {
         float v = 0.f;
         for (int q = 0; q < a.split; ++q) v += slots[q * E + e];
@@ -401,9 +326,6 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         if (col < a.N)
             a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
     }
-#ifdef W4A16_TRACE
-    if (threadIdx.x == 0) W4A16_TRACE_AT(13, clock64() - t_entry);
-#endif
 }
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
@@ -484,21 +406,6 @@ int *status_word() {
 
 }  // namespace
 
-#ifdef W4A16_TRACE
-extern "C" __attribute__((visibility("default"))) int w4a16_trace_read(void *host, size_t bytes) {
-    return (int)cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
-}
-extern "C" __attribute__((visibility("default"))) int w4a16_trace_launches(void *host, int reset) {
-    cudaError_t e = cudaMemcpyFromSymbol(host, g_trace_launch, sizeof(g_trace_launch));
-    if (reset) {
-        static unsigned long long init[64][4];
-        unsigned zero = 0;
-        cudaMemcpyToSymbol(g_trace_launch, init, sizeof(init));
-        cudaMemcpyToSymbol(g_trace_next, &zero, sizeof(zero));
-    }
-    return (int)e;
-}
-#endif
 
 int consumer_warps(const w4a16_config &cfg) {
     return cfg.warps_k == 16 ? 16 : (cfg.warps_k == 4 ? 4 : 8);

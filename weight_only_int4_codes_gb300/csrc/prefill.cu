@@ -117,8 +117,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_u32(tmem_slot), a.tmem_cols);
-        tmem_relinquish<1>();
+        tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
+        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -189,17 +189,17 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                     const uint64_t bd = b_desc + c * b_chunk16 + w * 2;
                     const uint32_t acc = (kt != kt0) || (kk != 0);
                     if (ATMEM)
-                        umma_f16_ts<1>(tmem_u, a_tmem + kk * 8, bd, idesc, acc);
+                        umma_f16_ts(tmem_u, a_tmem + kk * 8, bd, idesc, acc);
                     else
-                        umma_f16_ss<1>(tmem_u, a_desc + c * (kTileN * kChunkK * 2 / 16) + w * 2, bd,
+                        umma_f16_ss(tmem_u, a_desc + c * (kTileN * kChunkK * 2 / 16) + w * 2, bd,
                                  idesc, acc);
                 }
-                umma_commit<1>(&empty[s]);
+                umma_commit(&empty[s]);
             }
             __syncwarp();
             if (++s == a.stages) { s = 0; ++r; }
         }
-        if (lane == 0) umma_commit<1>(accum);
+        if (lane == 0) umma_commit(accum);
         __syncwarp();
     } else {
         // ------------------------------------------------------ dequant
@@ -305,7 +305,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     if (SPLIT && !(rank != 0 && warp == kDeqWarp0 && lane == 0)) cluster_wait();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc<1>(tmem_d, a.tmem_cols);
+    if (warp == 1) tmem_dealloc(tmem_d, a.tmem_cols);
 }
 
 // ---------------------------------------------------------------------------
@@ -491,8 +491,8 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_u32(tmem_slot), a.tmem_cols);
-        tmem_relinquish<1>();
+        tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
+        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -567,15 +567,15 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                     // step inside a chunk, a whole chunk between chunks
 #pragma unroll
                     for (int kk = 0; kk < kStageK / 16; ++kk)
-                        umma_f16_ts<1>(tmem_u, a_tmem + kk * 8,
+                        umma_f16_ts(tmem_u, a_tmem + kk * 8,
                                        b_desc + (kk / 4) * chunk16 + (kk % 4) * 2, idesc,
                                        (kt | kk) != 0);
-                    umma_commit<1>(&sempty[s]);
+                    umma_commit(&sempty[s]);
                 }
                 __syncwarp();
                 if (++s == a.xs) { s = 0; ++r; }
             }
-            if (lane == 0) umma_commit<1>(accum_full);
+            if (lane == 0) umma_commit(accum_full);
             __syncwarp();
         }
     } else {
@@ -637,7 +637,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc<1>(tmem_d, a.tmem_cols);
+    if (warp == 1) tmem_dealloc(tmem_d, a.tmem_cols);
 }
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
@@ -761,8 +761,9 @@ bool ring_layout(const w4a16_config &cfg, int K, int group, PrefillArgs &pa) {
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group) {
     if (cfg.split_k < 0 || cfg.split_k > kMaxPrefillSplit) return false;
     if (cfg.split_k > 1 && cfg.variant == W4A16_PREFILL_A_SMEM) return false;
-    if (cfg.variant == W4A16_PREFILL_PAIR)
-        return cfg.split_k <= 1 && prefill_pair_supported(cfg, M, N, K, group);
+    if (cfg.variant != 0 && cfg.variant != W4A16_PREFILL_A_TMEM &&
+        cfg.variant != W4A16_PREFILL_A_SMEM)
+        return false;
     const bool warps_ok = cfg.warps_k == 0 || cfg.warps_k == 4 || cfg.warps_k == 8 ||
                           cfg.warps_k == 16;
     if (!(warps_ok && cfg.tile_m >= 16 && cfg.tile_m <= 256 && cfg.tile_m % 16 == 0 &&
@@ -852,7 +853,6 @@ cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cud
 }
 
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
-    if (cfg.variant == W4A16_PREFILL_PAIR) return launch_prefill_pair(a, cfg, stream);
     if (!prefill_config_supported(cfg, a.M, a.N, a.K, a.group)) return cudaErrorNotSupported;
     // Wide tiles: the split-ring kernel (its x ring runs far enough ahead to
     // cover the copy latency at 1024+ MMA cycles per stage).  Narrower tiles

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4:
                 5: "TIMEOUT"}
 PATHS = {"auto": 0, "decode": 1, "prefill": 2}
 VARIANTS = {"auto": 0, "tma": 1, "registers": 2,      # decode path
-            "tmem": 1, "smem": 2, "pair": 3}       # prefill path: A's home, CTA pairs
+            "tmem": 1, "smem": 2}                  # prefill path: A's home
 QUANT_ASYMMETRIC, QUANT_SYMMETRIC = 0, 1
 FLAG_PDL = 0x1
 FLAG_TEST_TIMEOUT = 0x100
