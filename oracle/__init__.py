@@ -66,8 +66,13 @@ class Oracle:
         lib.oracle_dequant.argtypes = [P, P, P, I, I, I, P]
         lib.oracle_gemm.argtypes = [P, P, P, P, I, I, I, I, P]
         lib.oracle_num_threads.argtypes = []
+        lib.oracle_permuted_words.argtypes = [I, I, I]
+        lib.oracle_permuted_words.restype = ctypes.c_longlong
+        lib.oracle_permute.argtypes = [P, P, P, I, I, I, P]
+        lib.oracle_unpermute.argtypes = [P, I, I, I, P, P, P]
         for f in (lib.oracle_quantize_pack, lib.oracle_quantize_pack_symmetric, lib.oracle_unpack,
-                  lib.oracle_dequant, lib.oracle_gemm, lib.oracle_num_threads):
+                  lib.oracle_dequant, lib.oracle_gemm, lib.oracle_num_threads,
+                  lib.oracle_permute, lib.oracle_unpermute):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -133,6 +138,34 @@ class Oracle:
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
+    # ------------------------------------------------- pre-permuted layout
+    def permute(self, packed, scales, zeros, group: int = 128) -> np.ndarray:
+        """natural (packed [K/8,N], scales, zeros) -> repacked uint32 words (the
+        pre-permuted layout defined in w4a16_oracle.c)."""
+        packed = np.ascontiguousarray(packed, dtype=np.uint32)
+        sb, zb = _as_half_bits(scales), _as_half_bits(zeros)
+        K, N = packed.shape[0] * 8, packed.shape[1]
+        n = int(self.lib.oracle_permuted_words(K, N, group))
+        if n <= 0:
+            raise ValueError("permute: unsupported shape K=%d N=%d group=%d" % (K, N, group))
+        out = np.zeros(n, dtype=np.uint32)
+        _check(self.lib.oracle_permute(_ptr(packed), _ptr(sb), _ptr(zb), K, N, group, _ptr(out)),
+               "permute")
+        return out
+
+    def unpermute(self, words, K: int, N: int, group: int = 128):
+        """repacked words -> (packed uint32 [K/8,N], scales fp16, zeros fp16)."""
+        words = np.ascontiguousarray(words, dtype=np.uint32)
+        if words.size != int(self.lib.oracle_permuted_words(K, N, group)):
+            raise ValueError("unpermute: %d words do not fit K=%d N=%d group=%d"
+                             % (words.size, K, N, group))
+        packed = np.zeros((K // 8, N), dtype=np.uint32)
+        scales = np.zeros((K // group, N), dtype=np.uint16)
+        zeros = np.zeros((K // group, N), dtype=np.uint16)
+        _check(self.lib.oracle_unpermute(_ptr(words), K, N, group, _ptr(packed), _ptr(scales),
+                                         _ptr(zeros)), "unpermute")
+        return packed, scales.view(np.float16), zeros.view(np.float16)
+
 
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
@@ -187,6 +220,14 @@ def gemm(x, packed, scales, zeros, group: int = 128):
 
 def num_threads() -> int:
     return default().num_threads()
+
+
+def permute(packed, scales, zeros, group: int = 128):
+    return default().permute(packed, scales, zeros, group)
+
+
+def unpermute(words, K: int, N: int, group: int = 128):
+    return default().unpermute(words, K, N, group)
 
 
 def rel_err(out, ref) -> float:

@@ -264,6 +264,134 @@ int oracle_gemm(const uint16_t *x, const uint32_t *packed, const uint16_t *scale
     return 0;
 }
 
+/* --------------------------------------------------- pre-permuted layout
+ *
+ * "Beating FP16 with 4-bit Weights", section "What's next": permute the packed
+ * weights offline so that they reach the tensor cores in the order the MMA
+ * consumes them, and pipeline the loads with asynchronous copies; "Triton
+ * Kernel Matches bitsandbytes", section "Why Marlin Is Still Faster" credits
+ * the same offline reordering.  The pages give no byte layout; this library's
+ * layout (the repacked form) is defined here, as a plain index map:
+ *
+ *   requirements: K % 256 == 0, N % 32 == 0, and either group divides 256 or
+ *   256 divides group (group a multiple of 32).
+ *   gps = 256 / group if group < 256, else 1   (group rows stored per block)
+ *   block (sn, kb), sn = 32-column strip in [0, N/32), kb = 256-row block of K
+ *   in [0, K/256), starts at 32-bit word  (sn * (K/256) + kb) * BW,
+ *   BW = 1024 + 32 * gps words (4096 + 128 * gps bytes).
+ *   Word i = u8 * 128 + L * 4 + c of a block (u8 in 0..7, L in 0..31, c in 0..3)
+ *   holds the codes of packed row  r = 32 * kb + 4 * u8 + (L % 4)  and column
+ *   n = 32 * sn + 4 * (L / 4) + c, with its nibbles reordered: nibble p of the
+ *   repacked word is nibble 2 * (p % 4) + p / 4 of the natural word (so the
+ *   nibble pairs (0,4), (1,5), (2,6), (3,7) hold the codes of k = 8r + (0,1),
+ *   (2,3), (4,5), (6,7)).
+ *   After the 1024 words, the block's scales and zeros as binary16 values:
+ *   half index  h = (gi * 8 + g) * 8 + c  (scale) and  h + 4  (zero), for
+ *   gi in 0..gps-1, g in 0..7, c in 0..3, of group row  256 * kb / group + gi
+ *   and column  32 * sn + 4 * g + c.
+ */
+static int check_permuted_shape(int K, int N, int group)
+{
+    if (K <= 0 || N <= 0 || K % 256 != 0 || N % 32 != 0) return -1;
+    if (group <= 0 || group % 32 != 0 || K % group != 0) return -2;
+    if (group < 256 ? (256 % group != 0) : (group % 256 != 0)) return -2;
+    return 0;
+}
+
+static int permuted_gps(int group) { return group < 256 ? 256 / group : 1; }
+
+/* nibble p of the result = nibble 2*(p%4) + p/4 of w */
+static uint32_t permute_nibbles(uint32_t w)
+{
+    uint32_t r = 0;
+    for (int p = 0; p < 8; ++p) {
+        uint32_t src = (uint32_t)(2 * (p % 4) + p / 4);
+        r |= ((w >> (4 * src)) & 15u) << (4 * p);
+    }
+    return r;
+}
+
+static uint32_t unpermute_nibbles(uint32_t w)
+{
+    uint32_t r = 0;
+    for (int p = 0; p < 8; ++p) {
+        uint32_t dst = (uint32_t)(2 * (p % 4) + p / 4);
+        r |= ((w >> (4 * p)) & 15u) << (4 * dst);
+    }
+    return r;
+}
+
+/* Number of 32-bit words of the repacked form (0 for an unsupported shape). */
+long long oracle_permuted_words(int K, int N, int group)
+{
+    if (check_permuted_shape(K, N, group)) return 0;
+    return (long long)(N / 32) * (K / 256) * (1024 + 32 * permuted_gps(group));
+}
+
+/* natural (packed [K/8,N], scales/zeros [K/g,N]) -> repacked words */
+int oracle_permute(const uint32_t *packed, const uint16_t *scales, const uint16_t *zeros,
+                   int K, int N, int group, uint32_t *out)
+{
+    int rc = check_permuted_shape(K, N, group);
+    if (rc) return rc;
+    const int gps = permuted_gps(group), KB = K / 256;
+    const long long BW = 1024 + 32 * gps;
+    for (int sn = 0; sn < N / 32; ++sn)
+        for (int kb = 0; kb < KB; ++kb) {
+            uint32_t *blk = out + ((long long)sn * KB + kb) * BW;
+            for (int u8 = 0; u8 < 8; ++u8)
+                for (int L = 0; L < 32; ++L)
+                    for (int c = 0; c < 4; ++c) {
+                        int r = 32 * kb + 4 * u8 + L % 4;
+                        int n = 32 * sn + 4 * (L / 4) + c;
+                        blk[u8 * 128 + L * 4 + c] = permute_nibbles(packed[(size_t)r * N + n]);
+                    }
+            uint16_t *sz = (uint16_t *)(blk + 1024);
+            for (int gi = 0; gi < gps; ++gi)
+                for (int g = 0; g < 8; ++g)
+                    for (int c = 0; c < 4; ++c) {
+                        int j = 256 * kb / group + gi;
+                        int n = 32 * sn + 4 * g + c;
+                        int h = (gi * 8 + g) * 8 + c;
+                        sz[h] = scales[(size_t)j * N + n];
+                        sz[h + 4] = zeros[(size_t)j * N + n];
+                    }
+        }
+    return 0;
+}
+
+/* repacked words -> natural (packed, scales, zeros): the inverse map */
+int oracle_unpermute(const uint32_t *in, int K, int N, int group, uint32_t *packed,
+                     uint16_t *scales, uint16_t *zeros)
+{
+    int rc = check_permuted_shape(K, N, group);
+    if (rc) return rc;
+    const int gps = permuted_gps(group), KB = K / 256;
+    const long long BW = 1024 + 32 * gps;
+    for (int sn = 0; sn < N / 32; ++sn)
+        for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t *blk = in + ((long long)sn * KB + kb) * BW;
+            for (int u8 = 0; u8 < 8; ++u8)
+                for (int L = 0; L < 32; ++L)
+                    for (int c = 0; c < 4; ++c) {
+                        int r = 32 * kb + 4 * u8 + L % 4;
+                        int n = 32 * sn + 4 * (L / 4) + c;
+                        packed[(size_t)r * N + n] = unpermute_nibbles(blk[u8 * 128 + L * 4 + c]);
+                    }
+            const uint16_t *sz = (const uint16_t *)(blk + 1024);
+            for (int gi = 0; gi < gps; ++gi)
+                for (int g = 0; g < 8; ++g)
+                    for (int c = 0; c < 4; ++c) {
+                        int j = 256 * kb / group + gi;
+                        int n = 32 * sn + 4 * g + c;
+                        int h = (gi * 8 + g) * 8 + c;
+                        scales[(size_t)j * N + n] = sz[h];
+                        zeros[(size_t)j * N + n] = sz[h + 4];
+                    }
+        }
+    return 0;
+}
+
 /* Threads the OpenMP loops above run on (1 when built without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -282,6 +282,95 @@ def pin_brute_force(orc):
         assert np.max(np.abs(ref - bref)) <= 1e-13 * max(1.0, float(np.max(np.abs(bref))))
 
 
+# ------------------------------------------------------- pre-permuted layout
+def _fixture_inputs(case):
+    K, N, group = case["K"], case["N"], case["group"]
+    packed = np.zeros((K // 8, N), dtype=np.uint32)
+    G = K // group
+    jj, nn = np.meshgrid(np.arange(G), np.arange(N), indexing="ij")
+    if case["N"] == 64:            # third case: every nibble of a word equal
+        rr, cc = np.meshgrid(np.arange(K // 8), np.arange(N), indexing="ij")
+        packed[:] = (0x11111111 * ((rr + cc) % 16)).astype(np.uint32)
+        scales = (0x3C00 + 64 * jj + nn).astype(np.uint16)
+        zeros = (0x4000 + 64 * jj + nn).astype(np.uint16)
+    else:
+        scales = (0x3C00 + 32 * jj + nn).astype(np.uint16)
+        zeros = (0x4000 + 32 * jj + nn).astype(np.uint16)
+    for w in case["words"]:
+        packed[w["r"], w["n"]] = int(w["natural"], 16)
+    return packed, scales, zeros
+
+
+def pin_golden_permuted_layout(orc):
+    """Hand-worked positions and values of the repacked layout (words, nibble
+    order, scale/zero halves) for groups 128, 512 and 32; every word not listed
+    is zero (the first two cases) and the inverse map restores the input."""
+    with open(os.path.join(GOLDEN, "permuted_layout_hand.json")) as f:
+        fx = json.load(f)
+    for case in fx["cases"]:
+        K, N, group = case["K"], case["N"], case["group"]
+        packed, scales, zeros = _fixture_inputs(case)
+        words = orc.permute(packed, scales.view(np.float16), zeros.view(np.float16), group)
+        halves = words.view(np.uint16)
+        for w in case["words"]:
+            assert int(words[w["index"]]) == int(w["repacked"], 16), (case["group"], w)
+        for h in case["halves"]:
+            assert int(halves[h["half_index"]]) == int(h["bits"], 16), (case["group"], h)
+        if N == 32:
+            gps = 256 // group if group < 256 else 1
+            bw = 1024 + 32 * gps
+            listed = {w["index"] for w in case["words"]}
+            for b in range(words.size // bw):
+                blk = words[b * bw:b * bw + 1024]
+                nz = set((np.nonzero(blk)[0] + b * bw).tolist())
+                assert nz <= listed, sorted(nz - listed)[:4]
+        back = orc.unpermute(words, K, N, group)
+        assert np.array_equal(back[0], packed)
+        assert np.array_equal(back[1].view(np.uint16), scales)
+        assert np.array_equal(back[2].view(np.uint16), zeros)
+
+
+def _permute_numpy(packed, scales, zeros, group):
+    """The same layout written as an axis permutation of numpy arrays (an
+    independent restatement of the index map)."""
+    K8, N = packed.shape
+    K = K8 * 8
+    KB, S = K // 256, N // 32
+    gps = 256 // group if group < 256 else 1
+    # packed rows r = 32 kb + 4 u8 + t, columns n = 32 sn + 4 g + c
+    p6 = packed.reshape(KB, 8, 4, S, 8, 4)                  # kb, u8, t, sn, g, c
+    words = p6.transpose(3, 0, 1, 4, 2, 5).reshape(S, KB, 1024)   # sn, kb, (u8, g, t, c)
+    nib = [(words >> np.uint32(4 * q)) & np.uint32(15) for q in range(8)]
+    rep = np.zeros_like(words)
+    for p in range(8):
+        rep |= nib[2 * (p % 4) + p // 4] << np.uint32(4 * p)
+    # scales / zeros of group rows 256 kb / group + gi
+    rows = (np.arange(KB)[:, None] * 256 // group + np.arange(gps)[None, :])   # kb, gi
+    sc = scales.view(np.uint16)[rows].reshape(KB, gps, S, 8, 4)             # kb, gi, sn, g, c
+    ze = zeros.view(np.uint16)[rows].reshape(KB, gps, S, 8, 4)
+    sz = np.concatenate([sc, ze], axis=-1)                                    # kb, gi, sn, g, 8
+    sz = sz.transpose(2, 0, 1, 3, 4).reshape(S, KB, gps * 64)                 # sn, kb, halves
+    sz_words = np.ascontiguousarray(sz).view(np.uint32)                       # sn, kb, 32 gps
+    return np.concatenate([rep, sz_words], axis=2).reshape(-1)
+
+
+def pin_permuted_layout_numpy(orc):
+    """The C map equals the numpy axis-permutation restatement on random words,
+    for every supported group size, and the inverse restores the input."""
+    rng = np.random.default_rng(2024)
+    for K, N, group in [(256, 32, 128), (512, 64, 32), (1024, 96, 64), (768, 32, 256),
+                        (1024, 64, 512), (2048, 32, 1024)]:
+        packed = rng.integers(0, 2 ** 32, size=(K // 8, N), dtype=np.uint64).astype(np.uint32)
+        scales = rng.integers(0, 2 ** 16, size=(K // group, N), dtype=np.uint64).astype(np.uint16)
+        zeros = rng.integers(0, 16, size=(K // group, N)).astype(np.uint16)
+        words = orc.permute(packed, scales.view(np.float16), zeros.view(np.float16), group)
+        assert np.array_equal(words, _permute_numpy(packed, scales, zeros, group)), (K, N, group)
+        back = orc.unpermute(words, K, N, group)
+        assert np.array_equal(back[0], packed)
+        assert np.array_equal(back[1].view(np.uint16), scales)
+        assert np.array_equal(back[2].view(np.uint16), zeros)
+
+
 ALL_PINS = [
     pin_half_decode_exhaustive,
     pin_half_encode,
@@ -296,4 +385,6 @@ ALL_PINS = [
     pin_gemm_one_hot,
     pin_gemm_linear,
     pin_brute_force,
+    pin_golden_permuted_layout,
+    pin_permuted_layout_numpy,
 ]

@@ -61,6 +61,21 @@ MUTANTS = [
     ("symmetric_max_not_absolute",
      "double w = fabs(oracle_half_to_double(W[(size_t)k * N + n]));",
      "double w = oracle_half_to_double(W[(size_t)k * N + n]);"),
+    ("permute_lane_swaps_g_and_t",
+     "int r = 32 * kb + 4 * u8 + L % 4;\n                        int n = 32 * sn + 4 * (L / 4) + c;\n                        blk[u8 * 128 + L * 4 + c] = permute_nibbles",
+     "int r = 32 * kb + 4 * u8 + L / 8;\n                        int n = 32 * sn + 4 * (L % 8) + c;\n                        blk[u8 * 128 + L * 4 + c] = permute_nibbles"),
+    ("permute_nibble_map_transposed",
+     "uint32_t src = (uint32_t)(2 * (p % 4) + p / 4);",
+     "uint32_t src = (uint32_t)(4 * (p % 2) + p / 2);"),
+    ("permute_blocks_strip_inner",
+     "uint32_t *blk = out + ((long long)sn * KB + kb) * BW;",
+     "uint32_t *blk = out + ((long long)kb * (N / 32) + sn) * BW;"),
+    ("permute_scale_zero_swapped",
+     "sz[h] = scales[(size_t)j * N + n];\n                        sz[h + 4] = zeros[(size_t)j * N + n];",
+     "sz[h] = zeros[(size_t)j * N + n];\n                        sz[h + 4] = scales[(size_t)j * N + n];"),
+    ("permute_group_row_ignores_block",
+     "int j = 256 * kb / group + gi;\n                        int n = 32 * sn + 4 * g + c;\n                        int h = (gi * 8 + g) * 8 + c;\n                        sz[h]",
+     "int j = gi;\n                        int n = 32 * sn + 4 * g + c;\n                        int h = (gi * 8 + g) * 8 + c;\n                        sz[h]"),
     ("degenerate_scale_kept_zero",
      "s_bits = 0x3c00;     /* 1.0 */\n                s = 1.0;",
      "s_bits = 0x3c00;     /* 1.0 */\n                s = 1e-300;"),

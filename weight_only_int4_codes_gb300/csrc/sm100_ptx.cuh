@@ -206,6 +206,18 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// One-dimensional bulk copy of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned) from global to this CTA's shared memory, completing `bytes`
+// on `bar`'s transaction count, with an L2 cache policy.
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void *src, uint32_t bytes,
+                                          uint32_t bar_smem, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst_smem),
+        "l"(src), "r"(bytes), "r"(bar_smem), "l"(policy)
+        : "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t p;
