@@ -39,6 +39,7 @@
 #ifndef W4A16_H_
 #define W4A16_H_
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -89,6 +90,9 @@ typedef enum w4a16_path {
 #define W4A16_DECODE_AUTO 0
 #define W4A16_DECODE_TMA 1        /* weights staged by TMA into a shared-memory ring */
 #define W4A16_DECODE_REGISTERS 2  /* weights streamed by 128-bit loads into registers */
+#define W4A16_DECODE_STREAM 3     /* persistent: at most one CTA per SM, each streams a
+                                     contiguous run of (column tile, stage) units
+                                     through a ring of bulk copies */
 
 /* Prefill kernel variants (w4a16_config.variant on the prefill path). */
 #define W4A16_PREFILL_A_TMEM 1    /* dequantized W^T operand in tensor memory (default) */
@@ -114,6 +118,7 @@ typedef struct w4a16_config {
     int tile_m;     /* prefill: rows of x per CTA tile (16..256, multiple of 16) */
     int flags;      /* W4A16_FLAG_* */
     int variant;    /* decode: W4A16_DECODE_*; prefill: W4A16_PREFILL_* */
+    int ctas;       /* decode, stream variant: CTAs in the grid (0: one per SM) */
 } w4a16_config;
 
 /*
@@ -197,8 +202,9 @@ W4A16_API w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed,
  *              read during the call and may be reused afterwards
  *   M, N, K, group  the shape shared by all experts
  *   cfg        NULL (automatic) or a decode-path configuration (registers
- *              variant); the grouped kernel serves M <= 16, larger M runs the
- *              experts' GEMMs one launch after another on the same stream
+ *              or stream variant); the grouped kernels serve M <= 16, larger M
+ *              runs the experts' GEMMs one launch after another on the same
+ *              stream
  * Errors: W4A16_ERR_INVALID_ARG for E out of range or any NULL pointer,
  * W4A16_ERR_MISALIGNED as w4a16_gemm, W4A16_ERR_UNSUPPORTED for a
  * configuration with no kernel; nothing is enqueued on an error.
@@ -210,6 +216,66 @@ W4A16_API w4a16_status w4a16_gemm_grouped(int E, const uint16_t *const *x,
                                 const uint16_t *const *zeros, uint16_t *const *out,
                                 int M, int N, int K, int group, const w4a16_config *cfg,
                                 cudaStream_t stream);
+
+/*
+ * The pre-permuted ("repacked") weight layout.  Page "Beating FP16 with 4-bit
+ * Weights", section "What's next", names permuting the packed weights offline
+ * into the order the tensor-core MMA consumes them, with asynchronous copies,
+ * as the way to the remaining speed; page "Triton Kernel Matches
+ * bitsandbytes", section "Why Marlin Is Still Faster", credits the same
+ * offline reordering.  The pages give no byte layout; this library's is:
+ *
+ *   requirements: K % 256 == 0, N % 32 == 0, and group (a multiple of 32)
+ *   divides 256 or is a multiple of 256.  gps = 256/group if group < 256,
+ *   else 1.
+ *   The weight is cut into 32-column strips sn and 256-row blocks kb; block
+ *   (sn, kb) starts at byte (sn * K/256 + kb) * B, B = 4096 + 128 * gps, and is:
+ *     1024 uint32 words: word u8*128 + L*4 + c (u8 < 8, L < 32, c < 4) holds
+ *       the codes of packed row 32kb + 4u8 + L%4 of column 32sn + 4(L/4) + c,
+ *       nibble p holding the code of k = 8*row + 2(p%4) + p/4;
+ *     then 16 bytes per (gi < gps, g < 8): the fp16 scales of columns
+ *       32sn + 4g .. +3 of group row 256kb/group + gi, then their four zeros.
+ *   So a 256-k stage of a strip is one contiguous block holding its scales and
+ *   zeros, each lane of a consumer warp reads its MMA fragment with one
+ *   128-bit load, and x enters the MMA without byte permutes.
+ */
+
+/* Bytes of the repacked form of a [K, N] weight; 0 if the shape or group is
+ * not supported by the layout.  Host only. */
+W4A16_API size_t w4a16_repacked_bytes(int K, int N, int group);
+
+/*
+ * natural (packed [K/8, N], scales, zeros [K/g, N]) -> repacked, on the GPU.
+ *   repacked  device buffer of w4a16_repacked_bytes(K, N, group) bytes
+ * packed and repacked 16-byte aligned, scales and zeros 8-byte aligned
+ * (W4A16_ERR_MISALIGNED); an unsupported shape or group returns
+ * W4A16_ERR_UNSUPPORTED.  Offline step: bit-exact with the oracle's map.
+ */
+W4A16_API w4a16_status w4a16_repack(const uint32_t *packed, const uint16_t *scales,
+                          const uint16_t *zeros, int K, int N, int group, void *repacked,
+                          cudaStream_t stream);
+
+/*
+ * out[M,N] = x[M,K] . W, with W given in the repacked form: the stream decode
+ * kernel (W4A16_DECODE_STREAM) reading one contiguous block per strip and
+ * stage.  cfg NULL or a stream-variant configuration (warps_n, split_k, ctas,
+ * flags).  M up to 16 per launch; larger M runs ceil(M/16) launches in
+ * stream order.  Same x / out layouts and alignment rules as w4a16_gemm;
+ * `repacked` 16-byte aligned.  The result equals w4a16_gemm on the natural
+ * weights within the GEMM tolerance (the MMAs see the same values; only the
+ * summation order of the k-permutation differs).
+ */
+W4A16_API w4a16_status w4a16_gemm_repacked(const uint16_t *x, const void *repacked, uint16_t *out,
+                                 int M, int N, int K, int group, const w4a16_config *cfg,
+                                 cudaStream_t stream);
+
+/* Grouped form of w4a16_gemm_repacked: E <= W4A16_MAX_EXPERTS experts of one
+ * shape in one launch, M <= 16; host arrays of E device pointers as in
+ * w4a16_gemm_grouped. */
+W4A16_API w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const *x,
+                                         const void *const *repacked, uint16_t *const *out,
+                                         int M, int N, int K, int group,
+                                         const w4a16_config *cfg, cudaStream_t stream);
 
 /* Host-only: the launch configuration w4a16_gemm_ex would use for this shape
  * with `request` (may be NULL) filled in.  Touches no GPU.  Returns the same

@@ -175,6 +175,32 @@ void plan_decode_tma(int M, int N, int K, int group, int sm_count, w4a16_config 
     }
 }
 
+// Decode path, stream variant: tiles of 32*warps_n columns cut into 16 KB
+// stages; split_k = 1 gives every CTA whole tiles (no shared tile, no
+// scratch), 2 gives every CTA an equal share of all stages (stream-K).  The
+// choice compares the busiest CTA's stages, counting one more stage for the
+// cross-CTA sum of a shared tile.  Narrow tiles (long stages along K) at small
+// M, wide ones when the x rows of a stage would crowd the ring.
+void plan_decode_stream(int M, int N, int K, int group, int experts, bool perm, int sm_count,
+                        w4a16_config &c) {
+    if (c.warps_n <= 0) {
+        c.warps_n = M <= 2 ? 1 : (M <= 8 ? 2 : 4);
+        while (c.warps_n < 4 && !decode_stream_supported(M, N, K, group, c.warps_n, perm))
+            c.warps_n *= 2;
+    }
+    if (c.split_k <= 0 && c.warps_n >= 1 && c.warps_n <= 4) {
+        const int BN = 32 * c.warps_n, SK = decode_stream_stage_k(c.warps_n);
+        const long long T = (long long)experts * ((N + BN - 1) / BN);
+        const long long KS = (K + SK - 1) / SK, U = T * KS;
+        const long long G = c.ctas > 0 ? c.ctas : sm_count;
+        const long long ga = G < T ? G : T;
+        const long long gs = G < U ? G : U;
+        const long long load_align = (T + ga - 1) / ga * KS;
+        const long long load_shared = (U + gs - 1) / gs + 1;
+        c.split_k = load_align <= load_shared ? 1 : 2;
+    }
+}
+
 // Measured dispatch table (GB300, group 128, one call per distinct weight copy
 // in a CUDA graph with programmatic dependent launch): the fastest decode
 // configuration for the projection shapes of the benchmark workloads.
@@ -278,6 +304,14 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
                             "TMA decode configuration not available (split_k=%d warps_n=%d "
                             "steps=%d, group=%d, N=%d)",
                             c.split_k, c.warps_n, c.steps, group, N);
+        } else if (c.variant == W4A16_DECODE_STREAM) {
+            plan_decode_stream(M, N, K, group, 1, false, device_info().sm_count, c);
+            if (M > 16 || !decode_stream_supported(M, N, K, group, c.warps_n, false) ||
+                c.split_k < 1 || c.split_k > 2 || c.ctas < 0)
+                return fail(W4A16_ERR_UNSUPPORTED,
+                            "stream decode configuration not available (M=%d warps_n=%d "
+                            "split_k=%d ctas=%d, group=%d, N=%d)",
+                            M, c.warps_n, c.split_k, c.ctas, group, N);
         } else if (c.variant == W4A16_DECODE_REGISTERS) {
             plan_decode(M, N, K, group, device_info().sm_count, c);
             if (!decode_config_supported(c, M) || c.steps % decode_steps_per_batch(group) != 0 ||
@@ -398,11 +432,26 @@ w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed, const uint
     if (st != W4A16_OK) return st;
     GemmArgs a{x, packed, scales, zeros, out, M, N, K, group};
     cudaError_t e;
-    if (c.path == W4A16_PATH_DECODE)
+    if (c.path == W4A16_PATH_DECODE && c.variant == W4A16_DECODE_STREAM) {
+        StreamCall sc;
+        sc.E = 1;
+        sc.x[0] = x;
+        sc.w[0] = packed;
+        sc.s[0] = scales;
+        sc.z[0] = zeros;
+        sc.out[0] = out;
+        sc.M = M;
+        sc.N = N;
+        sc.K = K;
+        sc.group = group;
+        sc.permuted = false;
+        e = launch_decode_stream(sc, c, stream);
+    } else if (c.path == W4A16_PATH_DECODE) {
         e = c.variant == W4A16_DECODE_TMA ? launch_decode_tma(a, c, stream)
                                           : launch_decode(a, c, stream);
-    else
+    } else {
         e = launch_prefill(a, c, stream);
+    }
     if (e == cudaErrorNotSupported)
         return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "gemm launch");
@@ -446,8 +495,36 @@ w4a16_status w4a16_gemm_grouped(int E, const uint16_t *const *x, const uint32_t 
     }
     w4a16_config c = cfg ? *cfg : w4a16_config{};
     if ((c.path != W4A16_PATH_AUTO && c.path != W4A16_PATH_DECODE) ||
-        (c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_REGISTERS))
-        return fail(W4A16_ERR_UNSUPPORTED, "grouped GEMM: decode path, registers variant only");
+        (c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_REGISTERS &&
+         c.variant != W4A16_DECODE_STREAM))
+        return fail(W4A16_ERR_UNSUPPORTED,
+                    "grouped GEMM: decode path, registers or stream variant only");
+    if (c.variant == W4A16_DECODE_STREAM) {
+        c.path = W4A16_PATH_DECODE;
+        plan_decode_stream(M, N, K, group, E, false, device_info().sm_count, c);
+        if (!decode_stream_supported(M, N, K, group, c.warps_n, false) || c.split_k < 1 ||
+            c.split_k > 2 || c.ctas < 0)
+            return fail(W4A16_ERR_UNSUPPORTED, "grouped stream configuration not available "
+                        "(warps_n=%d split_k=%d, group=%d, N=%d)", c.warps_n, c.split_k, group, N);
+        StreamCall sc;
+        sc.E = E;
+        for (int e = 0; e < E; ++e) {
+            sc.x[e] = x[e];
+            sc.w[e] = packed[e];
+            sc.s[e] = scales[e];
+            sc.z[e] = zeros[e];
+            sc.out[e] = out[e];
+        }
+        sc.M = M;
+        sc.N = N;
+        sc.K = K;
+        sc.group = group;
+        sc.permuted = false;
+        cudaError_t err = launch_decode_stream(sc, c, stream);
+        if (err == cudaErrorNotSupported)
+            return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
+        return err == cudaSuccess ? W4A16_OK : cuda_fail(err, "grouped gemm launch");
+    }
     c.path = W4A16_PATH_DECODE;
     c.variant = W4A16_DECODE_REGISTERS;
     // measured rows for the expert shapes; otherwise the E experts' column
@@ -473,6 +550,130 @@ w4a16_status w4a16_gemm_grouped(int E, const uint16_t *const *x, const uint32_t 
     a.K = K;
     a.group = group;
     cudaError_t err = launch_decode_grouped(a, c, stream);
+    if (err == cudaErrorNotSupported)
+        return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
+    return err == cudaSuccess ? W4A16_OK : cuda_fail(err, "grouped gemm launch");
+}
+
+size_t w4a16_repacked_bytes(int K, int N, int group) { return repacked_bytes(K, N, group); }
+
+w4a16_status w4a16_repack(const uint32_t *packed, const uint16_t *scales, const uint16_t *zeros,
+                          int K, int N, int group, void *repacked, cudaStream_t stream) {
+    w4a16_status st = check_shape(0, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if (!repack_supported(K, N, group))
+        return fail(W4A16_ERR_UNSUPPORTED, "repacked layout needs K %% 256 == 0, N %% 32 == 0 and "
+                    "a group that divides 256 or is a multiple of it (K=%d N=%d group=%d)",
+                    K, N, group);
+    if (!packed || !scales || !zeros || !repacked)
+        return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(packed) || !aligned16(repacked) || ((uintptr_t)scales & 7) ||
+        ((uintptr_t)zeros & 7))
+        return fail(W4A16_ERR_MISALIGNED, "packed and repacked must be 16-byte aligned, scales "
+                    "and zeros 8-byte aligned");
+    cudaError_t e = launch_repack(packed, scales, zeros, K, N, group, repacked, stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "repack launch");
+}
+
+namespace {
+// Checks shared by the repacked GEMM entry points; fills the stream plan.
+w4a16_status plan_repacked(int M, int N, int K, int group, int experts, const w4a16_config *cfg,
+                           w4a16_config &c) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!repack_supported(K, N, group))
+        return fail(W4A16_ERR_UNSUPPORTED, "repacked layout needs K %% 256 == 0, N %% 32 == 0 and "
+                    "a group that divides 256 or is a multiple of it (K=%d N=%d group=%d)",
+                    K, N, group);
+    c = cfg ? *cfg : w4a16_config{};
+    if ((c.path != W4A16_PATH_AUTO && c.path != W4A16_PATH_DECODE) ||
+        (c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_STREAM))
+        return fail(W4A16_ERR_UNSUPPORTED, "repacked weights: decode path, stream variant only");
+    c.path = W4A16_PATH_DECODE;
+    c.variant = W4A16_DECODE_STREAM;
+    const int m = M < 16 ? M : 16;
+    plan_decode_stream(m > 0 ? m : 1, N, K, group, experts, true, device_info().sm_count, c);
+    if (!decode_stream_supported(m > 0 ? m : 1, N, K, group, c.warps_n, true) || c.split_k < 1 ||
+        c.split_k > 2 || c.ctas < 0)
+        return fail(W4A16_ERR_UNSUPPORTED, "repacked stream configuration not available "
+                    "(warps_n=%d split_k=%d ctas=%d)", c.warps_n, c.split_k, c.ctas);
+    return W4A16_OK;
+}
+}  // namespace
+
+w4a16_status w4a16_gemm_repacked(const uint16_t *x, const void *repacked, uint16_t *out, int M,
+                                 int N, int K, int group, const w4a16_config *cfg,
+                                 cudaStream_t stream) {
+    w4a16_config c;
+    w4a16_status st = plan_repacked(M, N, K, group, 1, cfg, c);
+    if (st != W4A16_OK) return st;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if (!x || !repacked || !out) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(repacked) || !aligned16(out))
+        return fail(W4A16_ERR_MISALIGNED, "x, repacked and out must be 16-byte aligned");
+    StreamCall sc;
+    sc.E = 1;
+    sc.s[0] = sc.z[0] = nullptr;
+    sc.w[0] = static_cast<const uint32_t *>(repacked);
+    sc.N = N;
+    sc.K = K;
+    sc.group = group;
+    sc.permuted = true;
+    // 16 rows of x per launch (the decode kernel's batch); larger M runs
+    // several launches in stream order
+    for (int m0 = 0; m0 < M; m0 += 16) {
+        sc.M = M - m0 < 16 ? M - m0 : 16;
+        sc.x[0] = x + (size_t)m0 * K;
+        sc.out[0] = out + (size_t)m0 * N;
+        w4a16_config cm = c;
+        if (sc.M != (M < 16 ? M : 16)) {
+            // a ragged last chunk keeps the tile width when its layout fits
+            if (!decode_stream_supported(sc.M, N, K, group, cm.warps_n, true)) cm.warps_n = 4;
+        }
+        cudaError_t e = launch_decode_stream(sc, cm, stream);
+        if (e == cudaErrorNotSupported)
+            return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
+        if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    }
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const *x,
+                                         const void *const *repacked, uint16_t *const *out, int M,
+                                         int N, int K, int group, const w4a16_config *cfg,
+                                         cudaStream_t stream) {
+    if (E < 1 || E > W4A16_MAX_EXPERTS)
+        return fail(W4A16_ERR_INVALID_ARG, "E=%d: 1..%d experts per grouped call", E,
+                    W4A16_MAX_EXPERTS);
+    if (!x || !repacked || !out) return fail(W4A16_ERR_INVALID_ARG, "null pointer table");
+    if (M > 16)
+        return fail(W4A16_ERR_UNSUPPORTED, "grouped repacked GEMM: M <= 16 (got %d)", M);
+    w4a16_config c;
+    w4a16_status st = plan_repacked(M, N, K, group, E, cfg, c);
+    if (st != W4A16_OK) return st;
+    for (int e = 0; e < E; ++e) {
+        if (!x[e] || !repacked[e] || !out[e])
+            return fail(W4A16_ERR_INVALID_ARG, "null pointer (expert %d)", e);
+        if (!aligned16(x[e]) || !aligned16(repacked[e]) || !aligned16(out[e]))
+            return fail(W4A16_ERR_MISALIGNED, "expert %d: x, repacked and out must be 16-byte "
+                        "aligned", e);
+    }
+    if (M == 0 || N == 0) return W4A16_OK;
+    StreamCall sc;
+    sc.E = E;
+    for (int e = 0; e < E; ++e) {
+        sc.x[e] = x[e];
+        sc.w[e] = static_cast<const uint32_t *>(repacked[e]);
+        sc.s[e] = sc.z[e] = nullptr;
+        sc.out[e] = out[e];
+    }
+    sc.M = M;
+    sc.N = N;
+    sc.K = K;
+    sc.group = group;
+    sc.permuted = true;
+    cudaError_t err = launch_decode_stream(sc, c, stream);
     if (err == cudaErrorNotSupported)
         return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
     return err == cudaSuccess ? W4A16_OK : cuda_fail(err, "grouped gemm launch");

@@ -45,6 +45,20 @@ struct GroupedGemmArgs {
     int M, N, K, group;
 };
 
+// One call of the stream decode kernel (decode_stream.cu): E GEMMs of one
+// shape (E = 1 for a plain GEMM), natural or repacked weights.  For repacked
+// weights w[e] is the block array of w4a16_repack and s, z are unused.
+struct StreamCall {
+    int E;
+    const uint16_t *x[kMaxExperts];
+    const uint32_t *w[kMaxExperts];
+    const uint16_t *s[kMaxExperts];
+    const uint16_t *z[kMaxExperts];
+    uint16_t *out[kMaxExperts];
+    int M, N, K, group;
+    bool permuted;
+};
+
 // Each returns cudaSuccess or the launch error; they never synchronize.
 cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group, bool symmetric,
                                  uint32_t *packed, uint16_t *scales, uint16_t *zeros,
@@ -52,6 +66,12 @@ cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group, boo
 cudaError_t launch_dequantize(const uint32_t *packed, const uint16_t *scales,
                               const uint16_t *zeros, uint16_t *W_out, int K, int N,
                               int group, cudaStream_t stream);
+// The pre-permuted (repacked) weight layout: support check, size, and the
+// natural -> repacked transform (quant.cu).
+bool repack_supported(int K, int N, int group);
+size_t repacked_bytes(int K, int N, int group);
+cudaError_t launch_repack(const uint32_t *packed, const uint16_t *scales, const uint16_t *zeros,
+                          int K, int N, int group, void *out, cudaStream_t stream);
 // Decode path: cfg already fully resolved (split_k, warps_k, warps_n, steps > 0).
 // Returns cudaErrorNotSupported for a configuration with no compiled kernel.
 cudaError_t launch_decode(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
@@ -67,6 +87,13 @@ int decode_ctas_per_sm(const w4a16_config &cfg, int M, int group);
 bool decode_tma_supported(const w4a16_config &cfg, int group);
 int decode_tma_smem_bytes(const w4a16_config &cfg, int M, int group);
 cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
+// Decode path, stream variant (decode_stream.cu): cfg.warps_n strips per
+// tile (1, 2 or 4), cfg.split_k 1 (whole tiles per CTA) or 2 (stream-K
+// shares), cfg.ctas CTAs (0: one per SM).
+bool decode_stream_supported(int M, int N, int K, int group, int bns, bool perm);
+int decode_stream_stage_k(int bns);   // k per stage of a tile of bns strips
+cudaError_t launch_decode_stream(const StreamCall &call, const w4a16_config &cfg,
+                                 cudaStream_t stream);
 // Prefill path (tcgen05).  Returns cudaErrorNotSupported if unavailable.
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group);

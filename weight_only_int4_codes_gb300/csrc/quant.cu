@@ -95,6 +95,45 @@ dequantize_kernel(const uint32_t *__restrict__ packed, const __half *__restrict_
     }
 }
 
+// Repack (the pre-permuted layout; page "Beating FP16 with 4-bit Weights",
+// section "What's next": permute the packed weights offline into the order the
+// MMA consumes them).  One CTA per block (32-column strip sn, 256-row block
+// kb): block words u8 * 128 + L * 4 + c take packed row 32 kb + 4 u8 + L % 4,
+// column 32 sn + 4 (L / 4) + c, with the nibbles reordered so that nibble p
+// holds natural nibble 2 (p % 4) + p / 4; then the block's scales and zeros,
+// 16 bytes per (group row gi, 4-column group g): four scales, four zeros.
+__device__ __forceinline__ uint32_t repack_nibbles(uint32_t w) {
+    uint32_t r = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) r |= ((w >> (4 * (2 * (p % 4) + p / 4))) & 15u) << (4 * p);
+    return r;
+}
+
+__global__ void __launch_bounds__(256)
+repack_kernel(const uint32_t *__restrict__ packed, const uint16_t *__restrict__ scales,
+              const uint16_t *__restrict__ zeros, int K, int N, int group, int gps,
+              uint32_t *__restrict__ out)
+{
+    const int KB = K >> 8;
+    const int sn = blockIdx.x / KB, kb = blockIdx.x - sn * KB;
+    uint32_t *blk = out + (size_t)blockIdx.x * (1024 + 32 * gps);
+    const int u8 = threadIdx.x >> 5, L = threadIdx.x & 31;
+    const int r = 32 * kb + 4 * u8 + (L & 3);
+    const int n0 = 32 * sn + 4 * (L >> 2);
+    const uint4 v = *reinterpret_cast<const uint4 *>(packed + (size_t)r * N + n0);
+    *reinterpret_cast<uint4 *>(blk + u8 * 128 + L * 4) =
+        make_uint4(repack_nibbles(v.x), repack_nibbles(v.y), repack_nibbles(v.z),
+                   repack_nibbles(v.w));
+    if (threadIdx.x < gps * 8) {
+        const int gi = threadIdx.x >> 3, g = threadIdx.x & 7;
+        const int j = (256 * kb) / group + gi;
+        const size_t src = (size_t)j * N + 32 * sn + 4 * g;
+        const uint2 sv = *reinterpret_cast<const uint2 *>(scales + src);
+        const uint2 zv = *reinterpret_cast<const uint2 *>(zeros + src);
+        *reinterpret_cast<uint4 *>(blk + 1024 + 4 * threadIdx.x) = make_uint4(sv.x, sv.y, zv.x, zv.y);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group, bool symmetric,
@@ -117,6 +156,29 @@ cudaError_t launch_dequantize(const uint32_t *packed, const uint16_t *scales,
         packed, reinterpret_cast<const __half *>(scales),
         reinterpret_cast<const __half *>(zeros), reinterpret_cast<__half *>(W_out), K, N,
         group);
+    return cudaGetLastError();
+}
+
+bool repack_supported(int K, int N, int group) {
+    if (K <= 0 || N <= 0 || K % 256 != 0 || N % 32 != 0 || group % 32 != 0 || K % group != 0)
+        return false;
+    return group < 256 ? 256 % group == 0 : group % 256 == 0;
+}
+
+size_t repacked_bytes(int K, int N, int group) {
+    if (!repack_supported(K, N, group)) return 0;
+    const int gps = group < 256 ? 256 / group : 1;
+    return (size_t)(N / 32) * (K / 256) * (4096 + 128 * gps);
+}
+
+cudaError_t launch_repack(const uint32_t *packed, const uint16_t *scales, const uint16_t *zeros,
+                          int K, int N, int group, void *out, cudaStream_t stream) {
+    if (!repack_supported(K, N, group)) return cudaErrorNotSupported;
+    const int gps = group < 256 ? 256 / group : 1;
+    const long long blocks = (long long)(N / 32) * (K / 256);
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    repack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(packed, scales, zeros, K, N, group, gps,
+                                                          static_cast<uint32_t *>(out));
     return cudaGetLastError();
 }
 

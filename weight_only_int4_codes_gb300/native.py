@@ -22,7 +22,7 @@ _LIB_NAME = "libw4a16.so"
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA",
                 5: "TIMEOUT"}
 PATHS = {"auto": 0, "decode": 1, "prefill": 2}
-VARIANTS = {"auto": 0, "tma": 1, "registers": 2,      # decode path
+VARIANTS = {"auto": 0, "tma": 1, "registers": 2, "stream": 3,   # decode path
             "tmem": 1, "smem": 2}                  # prefill path: A's home
 QUANT_ASYMMETRIC, QUANT_SYMMETRIC = 0, 1
 FLAG_PDL = 0x1
@@ -38,7 +38,7 @@ class W4A16Error(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("warps_k", ctypes.c_int),
                 ("warps_n", ctypes.c_int), ("steps", ctypes.c_int), ("tile_m", ctypes.c_int),
-                ("flags", ctypes.c_int), ("variant", ctypes.c_int)]
+                ("flags", ctypes.c_int), ("variant", ctypes.c_int), ("ctas", ctypes.c_int)]
 
     @classmethod
     def make(cls, cfg):
@@ -105,6 +105,9 @@ def load_library():
             "w4a16_gemm_ex": [P, P, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_plan": [I, I, I, I, ctypes.POINTER(Config), ctypes.POINTER(Config)],
             "w4a16_gemm_grouped": [I, P, P, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
+            "w4a16_repack": [P, P, P, I, I, I, P, P],
+            "w4a16_gemm_repacked": [P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
+            "w4a16_gemm_grouped_repacked": [I, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_get_kernel_status": [P],
             "w4a16_last_error": [],
             "w4a16_version": [],
@@ -114,6 +117,8 @@ def load_library():
             fn.argtypes = args
             fn.restype = ctypes.c_int
         lib.w4a16_last_error.restype = ctypes.c_char_p
+        lib.w4a16_repacked_bytes.argtypes = [I, I, I]
+        lib.w4a16_repacked_bytes.restype = ctypes.c_size_t
         _lib = lib
         return lib
 
@@ -211,6 +216,39 @@ def gemm(x, packed, scales, zeros, group: int = 128, out=None, stream=None):
     return out
 
 
+def repacked_bytes(K: int, N: int, group: int = 128) -> int:
+    """Bytes of the repacked (pre-permuted) form of a [K, N] weight; 0 if unsupported."""
+    return int(load_library().w4a16_repacked_bytes(K, N, group))
+
+
+def repack(packed, scales, zeros, group: int = 128, stream=None) -> torch.Tensor:
+    """natural (packed, scales, zeros) -> the repacked layout, a uint8 device
+    tensor of ``repacked_bytes(K, N, group)`` bytes."""
+    K, N = packed.shape[0] * 8, packed.shape[1]
+    n = repacked_bytes(K, N, group)
+    if n == 0:
+        raise W4A16Error(2, "repacked layout does not support K=%d N=%d group=%d" % (K, N, group))
+    out = torch.empty(n, dtype=torch.uint8, device=packed.device)
+    _check(load_library().w4a16_repack(
+        _dev(packed, "packed", torch.int32), _dev(scales, "scales", torch.float16),
+        _dev(zeros, "zeros", torch.float16), K, N, group, _dev(out, "repacked", torch.uint8),
+        _stream_handle(stream)))
+    return out
+
+
+def gemm_repacked(x, repacked, N: int, group: int = 128, out=None, config=None, stream=None):
+    """out [M,N] fp16 = x [M,K] @ W with W in the repacked layout."""
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    cfg = Config.make(config)
+    _check(_lib_fast().w4a16_gemm_repacked(
+        _dev(x, "x", torch.float16), _dev(repacked, "repacked", torch.uint8),
+        _dev(out, "out", torch.float16), M, N, K, group,
+        ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
+    return out
+
+
 MAX_EXPERTS = 64
 
 
@@ -246,6 +284,26 @@ def gemm_grouped(xs, packed, scales, zeros, group: int = 128, out=None, config=N
     tables = [(ctypes.c_void_p * E)(*p) for p in ptrs]
     cfg = Config.make(config)
     _check(load_library().w4a16_gemm_grouped(
+        E, *[ctypes.cast(t, ctypes.c_void_p) for t in tables], M, N, K, group,
+        ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
+    return out
+
+
+def gemm_grouped_repacked(xs, repacked, N: int, group: int = 128, out=None, config=None,
+                          stream=None):
+    """E expert GEMMs of one shape in one launch with repacked weights (M <= 16)."""
+    E = xs.shape[0] if isinstance(xs, torch.Tensor) else len(xs)
+    x0 = xs[0]
+    M, K = x0.shape
+    if out is None:
+        out = torch.empty((E, M, N), dtype=torch.float16, device=x0.device)
+    ptrs = [_experts(xs, "x", torch.float16), _experts(repacked, "repacked", torch.uint8),
+            _experts(out, "out", torch.float16)]
+    if any(len(p) != E for p in ptrs):
+        raise ValueError("every argument needs %d experts" % E)
+    tables = [(ctypes.c_void_p * E)(*p) for p in ptrs]
+    cfg = Config.make(config)
+    _check(load_library().w4a16_gemm_grouped_repacked(
         E, *[ctypes.cast(t, ctypes.c_void_p) for t in tables], M, N, K, group,
         ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
     return out
