@@ -1,21 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of the W4A16 GEMM hot path on GB300.
 
-A step is one pass of the hot path over one batch of synthetic input: for the
-default workload (the decode square projection: K = N = 4096, group 128) one
-W4A16 GEMM call for each M in {1, 2, 4, 8, 16}.  Every call in the timed
-region uses a distinct copy of the quantized weight (enough copies to exceed
-three times the L2 size), so the weight stream always comes from HBM.  The
-timed region is one replay of a CUDA graph holding exactly --steps steps,
-bracketed by CUDA events on the capture stream.
+A step is one pass of the hot path over one batch of synthetic input.  The
+default workload, `decode`, covers every decode configuration: the square
+projection (K = N = 4096), the FFN projections (4096 x 14336 and 14336 x 4096,
+with outliers) and the MoE expert shapes (2048 x 768 and 768 x 2048, 64 expert
+weight sets called back to back on one stream), each at M = 1, 2, 4, 8, 16,
+group 128: one W4A16 GEMM call per (shape, M, expert).  Every call reads a
+distinct copy of its weights (the rotation of copies exceeds three times the
+L2), so the weight stream always comes from HBM.  The timed region is the
+requested number of steps, run as replays of one CUDA graph per configuration
+(programmatic dependent launch inside), every replay bracketed by CUDA events
+on the capture stream; per-configuration times come from the same events.
 
-Printed: one JSON line (rank 0).  `value` is the weight-stream bandwidth of
-the whole job (packed words + scales + zeros of every call, all ranks) over the
-timed region; per-M microseconds per call (CUDA graph, and eager launches one
-by one), GB/s in three conventions (packed + scales + zeros; packed words
-only; every algorithmic byte), roofline fractions, a cuBLAS fp16 reference
-(torch.matmul on the dequantized weight, same rotation) and the fp64 oracle on
-the host cores (`cpu_baseline`) ride along.
+Printed: one JSON line (rank 0).  `value` is the weight-stream bandwidth of the
+whole job (packed words + scales + zeros of every call, all ranks) over the
+timed region.  Beside it: per-shape microseconds per call (CUDA graph and eager
+launches), GB/s and roofline fractions, a cuBLAS fp16 reference (torch.matmul on
+the dequantized weight), the same GEMMs on the repacked weight layout, the 64
+experts of a MoE shape in one grouped launch (natural and repacked weights),
+the streaming-read ceiling of a launch of the same size in the same launch
+chain, the fp64 oracle on the host cores (`cpu_baseline`), and `e2e`: the step
+through the public API with activations copied from pinned host memory and
+results copied back on every call.
 
 --impl reference times the fp64 CPU oracle instead (the reference arm).
 Multi-GPU (torchrun): every rank runs the same step on its own GPU with its own
@@ -40,19 +47,32 @@ if ROOT not in sys.path:
 
 METRIC = ("W4A16 µs/call and weight-stream HBM GB/s (% of GB300 roofline), M=1..16")
 GROUP = 128
+DECODE_MS = [1, 2, 4, 8, 16]
+PREFILL_MS = [16, 32, 64, 128, 256, 1024, 4096]
 
-# workload name -> shapes (K, N), Ms, outliers, experts
-WORKLOADS = {
-    "decode_square": dict(shapes=[(4096, 4096)], Ms=[1, 2, 4, 8, 16], outliers=False, experts=1,
-                          config=1),
-    "decode_ffn": dict(shapes=[(4096, 14336), (14336, 4096)], Ms=[1, 2, 4, 8, 16], outliers=True,
-                       experts=1, config=2),
-    "moe_experts": dict(shapes=[(2048, 768), (768, 2048)], Ms=[1, 2, 4, 8, 16], outliers=False,
-                        experts=64, config=3),
-    "prefill_sweep": dict(shapes=[(4096, 14336), (8192, 28672)],
-                          Ms=[16, 32, 64, 128, 256, 1024, 4096], outliers=False, experts=1,
-                          config=4),
+# configuration -> its shapes; si = index of the shape within the configuration
+# (it picks the seeds of that shape's weights and activations)
+CONFIGS = {
+    "decode_square": [dict(K=4096, N=4096, config=1, si=0, outliers=False, experts=1)],
+    "decode_ffn": [dict(K=4096, N=14336, config=2, si=0, outliers=True, experts=1),
+                   dict(K=14336, N=4096, config=2, si=1, outliers=True, experts=1)],
+    "moe_experts": [dict(K=2048, N=768, config=3, si=0, outliers=False, experts=64),
+                    dict(K=768, N=2048, config=3, si=1, outliers=False, experts=64)],
+    "prefill_sweep": [dict(K=4096, N=14336, config=4, si=0, outliers=False, experts=1),
+                      dict(K=8192, N=28672, config=4, si=1, outliers=False, experts=1)],
 }
+# workload -> the configurations its step runs, and the batch rows
+WORKLOADS = {
+    "decode": dict(configs=["decode_square", "decode_ffn", "moe_experts"], Ms=DECODE_MS),
+    "decode_square": dict(configs=["decode_square"], Ms=DECODE_MS),
+    "decode_ffn": dict(configs=["decode_ffn"], Ms=DECODE_MS),
+    "moe_experts": dict(configs=["moe_experts"], Ms=DECODE_MS),
+    "prefill_sweep": dict(configs=["prefill_sweep"], Ms=PREFILL_MS),
+}
+
+
+def shapes_of(wl):
+    return [dict(sh, cfg=c) for c in wl["configs"] for sh in CONFIGS[c]]
 
 
 def weight_bytes(K, N, group=GROUP):
@@ -75,13 +95,13 @@ def load_peaks():
                     source="fallback")
 
 
-# The sources each workload's kernels are built from: a committed ncu summary
-# is used only while these are unchanged.
+# The sources each kind of workload's kernels are built from: a committed ncu
+# summary is used only while these are unchanged.
 KERNEL_SOURCES = {
     "decode": ["api.cu", "common.cuh", "decode.cu", "decode_math.cuh", "decode_tma.cu",
                "sm100_ptx.cuh", "tmap.cu", "tmap.cuh"],
-    "prefill": ["api.cu", "common.cuh", "prefill.cu", "prefill_tile.cuh",
-                "sm100_ptx.cuh", "tcgen05.cuh", "tmap.cu", "tmap.cuh"],
+    "prefill": ["api.cu", "common.cuh", "prefill.cu", "prefill_tile.cuh", "sm100_ptx.cuh",
+                "tcgen05.cuh", "tmap.cu", "tmap.cuh"],
 }
 
 
@@ -98,11 +118,11 @@ def source_sha(kind):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
-    """Per-launch DRAM bytes of the workload's kernels from the committed ncu
+def ncu_traffic(name):
+    """Per-launch DRAM bytes of a configuration's kernels from the committed ncu
     summary, or None when absent or taken on a different kernel source."""
-    kind = workload_kind(workload)
-    path = os.path.join(ROOT, "profiles", "%s_kernel_%s.txt" % (kind, workload))
+    kind = workload_kind(name)
+    path = os.path.join(ROOT, "profiles", "%s_kernel_%s.txt" % (kind, name))
     if not os.path.exists(path):
         return None
     kv = {}
@@ -217,28 +237,33 @@ def barrier(pg):
 def oracle_calls(wl, cols, rows=None):
     """Inputs of one sampled step for the fp64 oracle: the first `cols` columns
     of every weight (quantized once, offline) and the step's activations (their
-    first `rows` rows when given)."""
+    first `rows` rows when given); each entry runs once per expert."""
     import oracle
     from weight_only_int4_codes_gb300 import synth
     calls = []
-    for si, (K, N) in enumerate(wl["shapes"]):
+    for sh in shapes_of(wl):
+        K, N = sh["K"], sh["N"]
         n = min(cols, N)
-        W = synth.weight(K, n, seed=synth.weight_seed(wl["config"], shape_index=si),
-                         outliers=wl["outliers"])
+        W = synth.weight(K, n, seed=synth.weight_seed(sh["config"], shape_index=sh["si"]),
+                         outliers=sh["outliers"])
         qw = oracle.quantize_pack(W, GROUP)
         for M in wl["Ms"]:
-            x = synth.activations(M, K, seed=synth.x_seed(wl["config"], M, shape_index=si))
+            x = synth.activations(M, K, seed=synth.x_seed(sh["config"], M, shape_index=sh["si"]))
             if rows is not None:
                 x = x[:rows]
-            calls.append((x, qw, weight_bytes(K, n)))
+            calls.append((x, qw, weight_bytes(K, n), sh["experts"]))
     return calls
 
 
-def oracle_step(wl, calls):
+def oracle_step(calls):
     import oracle
-    for _ in range(wl["experts"]):
-        for x, qw, _b in calls:
+    for x, qw, _b, experts in calls:
+        for _ in range(experts):
             oracle.gemm(x, *qw, group=GROUP)
+
+
+def step_bytes(calls):
+    return sum(b * e for _x, _q, b, e in calls)
 
 
 def oracle_sample(wl, cols, reps_min_s):
@@ -247,17 +272,31 @@ def oracle_sample(wl, cols, reps_min_s):
     sampled step, weight bytes per sampled step, threads used)."""
     import oracle
     calls = oracle_calls(wl, cols)
-    per_step_bytes = sum(c[2] for c in calls) * wl["experts"]
-    oracle_step(wl, calls)                       # warm (library load, page faults)
+    oracle_step(calls)                           # warm (library load, page faults)
     times = []
     t_all = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        oracle_step(wl, calls)
+        oracle_step(calls)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_all >= reps_min_s:
             break
-    return statistics.median(times), per_step_bytes, oracle.num_threads()
+    return statistics.median(times), step_bytes(calls), oracle.num_threads()
+
+
+def config_obj(args, world):
+    """The `config` object both arms print (the same keys and values)."""
+    wl = WORKLOADS[args.workload]
+    return {"workload": args.workload, "group": GROUP,
+            "shapes": [[sh["K"], sh["N"]] for sh in shapes_of(wl)],
+            "experts": [sh["experts"] for sh in shapes_of(wl)], "Ms": wl["Ms"],
+            "l2": "inputs larger than L2: every call reads a distinct weight copy (rotation "
+                  "footprint >= 3x L2)",
+            "timing": "replays of one CUDA graph per configuration, each bracketed by CUDA "
+                      "events; value over the sum",
+            "pdl": not args.no_pdl,
+            "launch": "one call per GEMM (MoE: 64 expert calls back to back per shape and M)",
+            "parallelism": "replicas" if world > 1 else "1gpu"}
 
 
 def run_reference(args, rank, world, pg):
@@ -277,7 +316,7 @@ def run_reference(args, rank, world, pg):
     for _ in range(8):
         calls = oracle_calls(wl, cols, rows)
         t0 = time.perf_counter()
-        oracle_step(wl, calls)
+        oracle_step(calls)
         projected = (time.perf_counter() - t0) * (args.steps + args.warmup)
         if projected <= budget_s:
             break
@@ -288,17 +327,17 @@ def run_reference(args, rank, world, pg):
             rows = max(1, int((rows or max(wl["Ms"])) * f))
         else:
             break
-    bytes_step = sum(c[2] for c in calls) * wl["experts"]
+    bytes_step = step_bytes(calls)
     threads = oracle.num_threads()
     for _ in range(max(args.warmup, 3) - 1):      # the other untimed warm-up steps
-        oracle_step(wl, calls)
+        oracle_step(calls)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(wl, calls)
+        oracle_step(calls)
     elapsed = time.perf_counter() - t0
     gbs = bytes_step * args.steps / elapsed / 1e9
-    sample = ("%d of each weight's columns (all K rows, %s of x, M in %s) per call, fp64 oracle "
-              "(quantize once, then dequantize + fp64 matmul per call)"
+    sample = ("%d of each weight's columns (all K rows, %s of x, M in %s) per call, every call "
+              "of the step, fp64 oracle (quantize once, then dequantize + fp64 matmul per call)"
               % (cols, "all rows" if rows is None else "the first %d rows" % rows, wl["Ms"]))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4),
@@ -306,8 +345,7 @@ def run_reference(args, rank, world, pg):
         "warmup": args.warmup, "ms_per_step": round(1e3 * elapsed / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded numpy PCG64; x~N(0,1), W~N(0,0.02) fp16)",
-        "config": {"workload": args.workload, "group": GROUP,
-                   "shapes": wl["shapes"], "Ms": wl["Ms"], "experts": wl["experts"]},
+        "config": config_obj(args, world),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s (weight stream)",
                          "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s (weight stream)",
@@ -318,6 +356,15 @@ def run_reference(args, rank, world, pg):
 
 
 # -------------------------------------------------------------------- GPU
+def graph_of(fns, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in fns:
+            f()
+    return g
+
+
 def timed_replays(graph, stream, reps, calls_per_replay):
     """Microseconds per call of `reps` replays of a graph holding
     `calls_per_replay` calls, each replay bracketed by events on `stream`
@@ -359,6 +406,17 @@ def timed_eager(calls, stream, reps):
     return out
 
 
+def steps_per_replay(steps, calls_per_step, max_nodes=8000, min_replays=20):
+    """Steps per graph replay: the largest divisor of `steps` that leaves at
+    least `min_replays` replays and at most `max_nodes` launches per graph."""
+    best = 1
+    for d in range(1, steps + 1):
+        if steps % d == 0 and steps // d >= min(min_replays, steps) and \
+                d * calls_per_step <= max_nodes:
+            best = d
+    return best
+
+
 def run_ours(args, rank, local, world, pg):
     import numpy as np
     import torch
@@ -370,96 +428,99 @@ def run_ours(args, rank, local, world, pg):
     dev = torch.device("cuda", local)
     w4.load_library()
     wl = WORKLOADS[args.workload]
+    Ms = wl["Ms"]
     peaks = load_peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     stream = torch.cuda.Stream(device=dev)
     gemm_cfg = dict(pdl=not args.no_pdl)
     if args.variant != "auto":
         gemm_cfg.update(path="decode", variant=args.variant)
-    # MoE workloads: by default one grouped launch per (shape, M) covers all
-    # experts (w4a16_gemm_grouped); --no-grouped issues one call per expert
-    E = wl["experts"]
-    grouped = E > 1 and not args.no_grouped
-    group_cfg = dict(pdl=not args.no_pdl)
+    decode = workload_kind(args.workload) == "decode"
 
     # weights: quantize once per shape on the GPU (offline step), then R
     # byte-identical copies at distinct addresses per shape so that the
-    # rotation's footprint exceeds 3x L2.
+    # rotation's footprint exceeds 3x L2; the same for the repacked layout
     shapes = []
-    for si, (K, N) in enumerate(wl["shapes"]):
-        W = synth.weight(K, N, seed=synth.weight_seed(wl["config"], shape_index=si) + 7919 * rank,
-                         outliers=wl["outliers"])
+    for sh in shapes_of(wl):
+        K, N, E = sh["K"], sh["N"], sh["experts"]
+        W = synth.weight(K, N, seed=synth.weight_seed(sh["config"], shape_index=sh["si"]) +
+                         7919 * rank, outliers=sh["outliers"])
         Wd = torch.from_numpy(W).to(dev)
         base = w4.quantize_pack(Wd, GROUP)
         wdq = w4.dequantize(*base, group=GROUP) if args.cublas else None
         del Wd
-        per_copy = weight_bytes(K, N)
-        R = max(2, math.ceil(3 * l2 / per_copy) + 1)
+        R = max(2, math.ceil(3 * l2 / weight_bytes(K, N)) + 1)
         copies = [tuple(t.clone() for t in base) for _ in range(R)]
-        dq_copies = None
+        rep_ok = decode and w4.repacked_bytes(K, N, GROUP) > 0 and not args.no_extras
+        repacked = [w4.repack(*c, group=GROUP) for c in copies] if rep_ok else None
+        dq = None
         if wdq is not None:
             Rq = max(2, math.ceil(3 * l2 / (2 * K * N)) + 1)
-            dq_copies = [wdq.clone() for _ in range(Rq)]
-        xs = {}
-        outs = {}
-        xg, og = {}, {}
-        for M in wl["Ms"]:
-            x = synth.activations(M, K, seed=synth.x_seed(wl["config"], M, shape_index=si))
-            xs[M] = torch.from_numpy(x).to(dev)
-            outs[M] = torch.empty((M, N), dtype=torch.float16, device=dev)
-            if grouped:
-                # distinct activations per expert, stacked [E, M, K]
-                xg[M] = torch.from_numpy(np.stack([
-                    synth.activations(M, K, seed=synth.x_seed(wl["config"], M, expert=e,
-                                                              shape_index=si))
-                    for e in range(E)])).to(dev)
-                og[M] = torch.empty((E, M, N), dtype=torch.float16, device=dev)
-        shapes.append(dict(K=K, N=N, copies=copies, dq=dq_copies, xs=xs, outs=outs, xg=xg,
-                           og=og))
+            dq = [wdq.clone() for _ in range(Rq)]
+        xs, outs = {}, {}
+        for M in Ms:
+            # distinct activations per expert, stacked [E, M, K]
+            xs[M] = torch.from_numpy(np.stack([
+                synth.activations(M, K, seed=synth.x_seed(sh["config"], M, expert=e,
+                                                          shape_index=sh["si"]))
+                for e in range(E)])).to(dev)
+            outs[M] = torch.empty((E, M, N), dtype=torch.float16, device=dev)
+        shapes.append(dict(sh, copies=copies, repacked=repacked, dq=dq, xs=xs, outs=outs))
     torch.cuda.synchronize(dev)
 
-    if grouped:
-        calls_per_step = [(s, M) for s in shapes for M in wl["Ms"]]
-        per_call = E                   # GEMMs (experts) per launch
-    else:
-        calls_per_step = [(s, M) for s in shapes for M in wl["Ms"]] * E
-        per_call = 1
-    step_weight_bytes = per_call * sum(weight_bytes(s["K"], s["N"]) for s, _ in calls_per_step)
-    step_total_bytes = per_call * sum(total_bytes(M, s["K"], s["N"]) for s, M in calls_per_step)
-    counters = {id(s): 0 for s in shapes}
+    counters = {}
 
-    def grouped_call(s, M, api=False):
-        """One launch over E experts, each reading the next distinct weight copy."""
-        R = len(s["copies"])
-        i = counters[id(s)]
-        counters[id(s)] = (i + E) % R
-        ws = [s["copies"][(i + e) % R] for e in range(E)]
-        w4.gemm_grouped(s["xg"][M], [w[0] for w in ws], [w[1] for w in ws], [w[2] for w in ws],
-                        group=GROUP, out=s["og"][M], config=None if api else group_cfg)
+    def call_fns(s, M, api=False, cfg=None):
+        """The step's calls of one (shape, M): one per expert, each reading the
+        next distinct weight copy."""
+        fns = []
+        for e in range(s["experts"]):
+            R = len(s["copies"])
+            i = counters.get(id(s), 0)
+            counters[id(s)] = (i + 1) % R
+            w = s["copies"][i]
+            x, o = s["xs"][M][e], s["outs"][M][e]
+            if api:
+                fns.append(lambda x=x, w=w, o=o: w4.gemm(x, *w, group=GROUP, out=o))
+            else:
+                fns.append(lambda x=x, w=w, o=o: w4.gemm_ex(x, *w, group=GROUP, out=o,
+                                                            config=cfg or gemm_cfg))
+        return fns
 
-    def one_step():
-        for s, M in calls_per_step:
-            if grouped:
-                grouped_call(s, M)
-                continue
-            i = counters[id(s)]
-            counters[id(s)] = (i + 1) % len(s["copies"])
-            w4.gemm_ex(s["xs"][M], *s["copies"][i], group=GROUP, out=s["outs"][M],
-                       config=gemm_cfg)
+    def part_fns(cfgname, steps):
+        fns = []
+        for _ in range(steps):
+            for s in shapes:
+                if s["cfg"] == cfgname:
+                    for M in Ms:
+                        fns += call_fns(s, M)
+        return fns
 
-    # warm-up (eager, also loads the kernels and fills the plan cache)
+    calls_per_step = {c: sum(s["experts"] * len(Ms) for s in shapes if s["cfg"] == c)
+                      for c in wl["configs"]}
+    wbytes_step = {c: sum(s["experts"] * len(Ms) * weight_bytes(s["K"], s["N"])
+                          for s in shapes if s["cfg"] == c) for c in wl["configs"]}
+    tbytes_step = {c: sum(s["experts"] * total_bytes(M, s["K"], s["N"])
+                          for s in shapes if s["cfg"] == c for M in Ms) for c in wl["configs"]}
+    flops_step = {c: sum(s["experts"] * 2.0 * M * s["K"] * s["N"]
+                         for s in shapes if s["cfg"] == c for M in Ms) for c in wl["configs"]}
+
+    # warm-up steps (eager: also loads the kernels and fills the plan caches)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            one_step()
+            for c in wl["configs"]:
+                for f in part_fns(c, 1):
+                    f()
     torch.cuda.synchronize(dev)
 
-    # capture exactly `steps` steps in one graph
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for _ in range(args.steps):
-            one_step()
+    # the timed region: `steps` steps as replays of one graph per configuration
+    spr = steps_per_replay(args.steps, max(calls_per_step.values()))
+    replays = args.steps // spr
+    graphs = {c: graph_of(part_fns(c, spr), stream) for c in wl["configs"]}
     with torch.cuda.stream(stream):
-        graph.replay()                 # untimed replay (graph upload)
+        for g in graphs.values():
+            g.replay()                      # untimed replay (graph upload)
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local) if rank == 0 else None
@@ -467,98 +528,138 @@ def run_ours(args, rank, local, world, pg):
         clocks.start()
     barrier(pg)
     torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    evs = []
     if clocks:
         clocks.mark_start()
     with torch.cuda.stream(stream):          # replay() launches on the current stream
-        ev0.record(stream)
-        graph.replay()
-        ev1.record(stream)
+        for _ in range(replays):
+            for c in wl["configs"]:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                graphs[c].replay()
+                b.record(stream)
+                evs.append((c, a, b))
     torch.cuda.synchronize(dev)
     if clocks:
         clocks.mark_end()
     barrier(pg)
     clock_rec = clocks.stop() if clocks else None
-    ms = ev0.elapsed_time(ev1)
+    part_ms = {c: 0.0 for c in wl["configs"]}
+    replay_ms = []
+    for i in range(0, len(evs), len(wl["configs"])):
+        t = 0.0
+        for c, a, b in evs[i:i + len(wl["configs"])]:
+            ms_ = a.elapsed_time(b)
+            part_ms[c] += ms_
+            t += ms_
+        replay_ms.append(t)
+    ms = sum(replay_ms)
     ms = reduce_max(pg, ms, dev)
+    for c in part_ms:
+        part_ms[c] = reduce_max(pg, part_ms[c], dev)
     ms_step = ms / args.steps
+    step_weight_bytes = sum(wbytes_step.values())
     gbs = world * step_weight_bytes * args.steps / (ms * 1e-3) / 1e9
+    launches = sum(calls_per_step.values()) * args.steps
+    per_config = {}
+    for c in wl["configs"]:
+        t_s = part_ms[c] * 1e-3
+        per_config[c] = {
+            "ms_in_timed_region": round(part_ms[c], 3),
+            "weight_GBs": round(world * wbytes_step[c] * args.steps / t_s / 1e9, 1),
+            "us_per_call": round(part_ms[c] * 1e3 / (calls_per_step[c] * args.steps), 3),
+            "roofline_frac": round(tbytes_step[c] * args.steps / t_s / (peaks["hbm_gbs"] * 1e9), 4)
+            if decode else round(flops_step[c] * args.steps / t_s /
+                                 (peaks["bf16_tflops_sustained"] * 1e12), 4),
+        }
 
-    # ---- per-M microseconds per call (graphs of R rotating calls), and cuBLAS
+    # ---- per shape and M: graphs of R rotating calls (every weight copy once)
+    def one_graph_us(fns, n_calls, reps=args.reps):
+        return statistics.median(timed_replays(graph_of(fns, stream), stream, reps, n_calls))
+
+    sink = torch.zeros(max(n_sm, 1024), dtype=torch.int32, device=dev)
     per_m = {}
-    for si, s in enumerate(shapes):
-        for M in wl["Ms"]:
-            R = len(s["copies"])
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(R):
-                    w4.gemm_ex(s["xs"][M], *s["copies"][i], group=GROUP, out=s["outs"][M],
-                               config=gemm_cfg)
-            ts = timed_replays(g, stream, args.reps, R)
-            us = statistics.median(ts)
-            K, N = s["K"], s["N"]
-            calls = [lambda i=i: w4.gemm_ex(s["xs"][M], *s["copies"][i], group=GROUP,
-                                            out=s["outs"][M], config=gemm_cfg)
-                     for i in range(R)]
-            us_eager = statistics.median(timed_eager(calls, stream, args.reps))
-            rec = {"us_per_call": round(us, 3),
-                   "us_per_call_eager": round(us_eager, 3),
+    for s in shapes:
+        K, N, E = s["K"], s["N"], s["experts"]
+        R = len(s["copies"])
+        tb = lambda M: total_bytes(M, K, N)
+        frac = lambda M, us: max(tb(M) / (peaks["hbm_gbs"] * 1e9),
+                                 2.0 * M * N * K / (peaks["bf16_tflops"] * 1e12)) / (us * 1e-6)
+        for M in Ms:
+            x, o = s["xs"][M][0], s["outs"][M][0]
+            fns = [lambda i=i: w4.gemm_ex(x, *s["copies"][i], group=GROUP, out=o, config=gemm_cfg)
+                   for i in range(R)]
+            us = one_graph_us(fns, R)
+            us_eager = statistics.median(timed_eager(fns, stream, args.reps))
+            rec = {"us_per_call": round(us, 3), "us_per_call_eager": round(us_eager, 3),
                    "weight_GBs": round(weight_bytes(K, N) / us / 1e3, 1),
                    "packed_GBs": round(K * N // 2 / us / 1e3, 1),
-                   "total_GBs": round(total_bytes(M, K, N) / us / 1e3, 1),
-                   "roofline_frac": round(max(total_bytes(M, K, N) / (peaks["hbm_gbs"] * 1e9),
-                                              2.0 * M * N * K / (peaks["bf16_tflops"] * 1e12))
-                                          / (us * 1e-6), 4)}
+                   "total_GBs": round(tb(M) / us / 1e3, 1),
+                   "roofline_frac": round(frac(M, us), 4)}
             if s["dq"] is not None:
                 Rq = len(s["dq"])
                 with torch.cuda.stream(stream):       # cuBLAS handle/workspace outside capture
-                    torch.matmul(s["xs"][M], s["dq"][0], out=s["outs"][M])
+                    torch.matmul(x, s["dq"][0], out=o)
                 torch.cuda.synchronize(dev)
-                gq = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gq, stream=stream):
-                    for i in range(Rq):
-                        torch.matmul(s["xs"][M], s["dq"][i], out=s["outs"][M])
-                tq = timed_replays(gq, stream, args.reps, Rq)
-                rec["cublas_fp16_us_per_call"] = round(statistics.median(tq), 3)
-                rec["speedup_vs_cublas"] = round(rec["cublas_fp16_us_per_call"] / us, 3)
-            if grouped:
-                # one grouped launch per E experts (all distinct weight copies)
-                nG = max(1, R // E)
-                gg = torch.cuda.CUDAGraph()
-                counters[id(s)] = 0
-                with torch.cuda.graph(gg, stream=stream):
-                    for _ in range(nG):
-                        grouped_call(s, M)
-                tg = statistics.median(timed_replays(gg, stream, args.reps, nG))
-                rec["grouped_us_per_%d_experts" % E] = round(tg, 3)
-                rec["grouped_weight_GBs"] = round(E * weight_bytes(K, N) / tg / 1e3, 1)
-                rec["grouped_roofline_frac"] = round(
-                    E * total_bytes(M, K, N) / (peaks["hbm_gbs"] * 1e9) / (tg * 1e-6), 4)
-                rec["grouped_speedup_vs_%d_calls" % E] = round(E * us / tg, 2)
-            key = "M=%d" % M if len(shapes) == 1 else "K=%d,N=%d,M=%d" % (K, N, M)
-            per_m[key] = rec
+                tq = one_graph_us([lambda i=i: torch.matmul(x, s["dq"][i], out=o)
+                                   for i in range(Rq)], Rq)
+                rec["cublas_fp16_us_per_call"] = round(tq, 3)
+                rec["speedup_vs_cublas"] = round(tq / us, 3)
+            if decode and not args.no_extras:
+                if s["repacked"] is not None:
+                    ur = one_graph_us([lambda i=i: w4.gemm_repacked(
+                        x, s["repacked"][i], N, group=GROUP, out=o, config=gemm_cfg)
+                        for i in range(R)], R)
+                    rec["repacked_us_per_call"] = round(ur, 3)
+                    rec["repacked_roofline_frac"] = round(frac(M, ur), 4)
+                # the streaming-read ceiling: a chain of launches reading the
+                # same weight bytes the same way, doing no arithmetic
+                ucs = one_graph_us([lambda i=i: w4.native.stream_read(
+                    s["copies"][i][0], sink, pdl=not args.no_pdl) for i in range(R)], R)
+                rec["stream_read_us"] = round(ucs, 3)
+                rec["stream_read_GBs"] = round(K * N // 2 / ucs / 1e3, 1)
+                rec["stream_read_frac"] = round(K * N // 2 / (peaks["hbm_gbs"] * 1e9) /
+                                                (ucs * 1e-6), 4)
+                if E > 1:
+                    nG = max(1, R // E)
+                    grp = [lambda j=j: w4.gemm_grouped(
+                        s["xs"][M], *[[s["copies"][(j * E + e) % R][t] for e in range(E)]
+                                      for t in range(3)],
+                        group=GROUP, out=s["outs"][M], config=gemm_cfg) for j in range(nG)]
+                    tg = one_graph_us(grp, nG)
+                    rec["grouped_us_per_%d_experts" % E] = round(tg, 3)
+                    rec["grouped_roofline_frac"] = round(E * tb(M) / (peaks["hbm_gbs"] * 1e9) /
+                                                         (tg * 1e-6), 4)
+                    if s["repacked"] is not None:
+                        grr = [lambda j=j: w4.gemm_grouped_repacked(
+                            s["xs"][M], [s["repacked"][(j * E + e) % R] for e in range(E)], N,
+                            group=GROUP, out=s["outs"][M], config=gemm_cfg) for j in range(nG)]
+                        tr = one_graph_us(grr, nG)
+                        rec["grouped_repacked_us_per_%d_experts" % E] = round(tr, 3)
+                        rec["grouped_repacked_roofline_frac"] = round(
+                            E * tb(M) / (peaks["hbm_gbs"] * 1e9) / (tr * 1e-6), 4)
+                    rec["single_calls_us_per_%d_experts" % E] = round(E * us, 3)
+            per_m["K=%d,N=%d,M=%d" % (K, N, M)] = rec
 
     # ---- end to end through the public API: x from pinned host memory and
     # the result back to pinned host memory every call; weights resident.
-    h2d = per_call * sum(2 * M * s["K"] for s, M in calls_per_step)
-    d2h = per_call * sum(2 * M * s["N"] for s, M in calls_per_step)
-    xkey, okey = ("xg", "og") if grouped else ("xs", "outs")
-    host_x = {(id(s), M): s[xkey][M].cpu().pin_memory() for s in shapes for M in wl["Ms"]}
-    host_o = {(id(s), M): torch.empty_like(s[okey][M], device="cpu").pin_memory()
-              for s in shapes for M in wl["Ms"]}
-    e2e_steps = max(3, min(args.steps, 50))
+    h2d = sum(s["experts"] * 2 * M * s["K"] for s in shapes for M in Ms)
+    d2h = sum(s["experts"] * 2 * M * s["N"] for s in shapes for M in Ms)
+    host_x = {(id(s), M): s["xs"][M].cpu().pin_memory() for s in shapes for M in Ms}
+    host_o = {(id(s), M): torch.empty_like(s["outs"][M], device="cpu").pin_memory()
+              for s in shapes for M in Ms}
+    e2e_steps = max(3, min(args.steps, 20))
     with torch.cuda.stream(stream):
         def e2e_step():
-            for s, M in calls_per_step:
-                s[xkey][M].copy_(host_x[(id(s), M)], non_blocking=True)
-                if grouped:
-                    grouped_call(s, M, api=True)
-                else:
-                    i = counters[id(s)]
-                    counters[id(s)] = (i + 1) % len(s["copies"])
-                    w4.gemm(s["xs"][M], *s["copies"][i], group=GROUP, out=s["outs"][M])
-                host_o[(id(s), M)].copy_(s[okey][M], non_blocking=True)
+            for s in shapes:
+                for M in Ms:
+                    hx, ho = host_x[(id(s), M)], host_o[(id(s), M)]
+                    fns = call_fns(s, M, api=True)
+                    for e, f in enumerate(fns):
+                        s["xs"][M][e].copy_(hx[e], non_blocking=True)
+                        f()
+                        ho[e].copy_(s["outs"][M][e], non_blocking=True)
             stream.synchronize()
         e2e_step()
         barrier(pg)
@@ -569,28 +670,25 @@ def run_ours(args, rank, local, world, pg):
     e2e_s = reduce_max(pg, e2e_s, dev)
     e2e_gbs = world * step_weight_bytes * e2e_steps / e2e_s / 1e9
 
-    # ---- roofline of the dominant kernel, from the timed region: every launch
-    # in it is one of the workload's GEMM kernels.  Decode shapes are bound by
-    # HBM (algorithmic bytes per launch / mean launch time); the prefill sweep
-    # by the fp16 tensor cores (fp16 and bf16 dense rates are equal on GB300).
-    launches = len(calls_per_step) * args.steps
-    mean_launch_s = ms * 1e-3 / launches
-    if workload_kind(args.workload) == "prefill":
-        step_flops = sum(2.0 * M * s["K"] * s["N"] for s, M in calls_per_step)
-        achieved = step_flops / len(calls_per_step) / mean_launch_s / 1e12
+    # ---- roofline of the dominant kernel: the configuration that takes most
+    # of the timed region; its algorithmic bytes (flops) per launch over its
+    # mean launch time, both from the timed region's events
+    dom = max(wl["configs"], key=lambda c: part_ms[c])
+    mean_launch_s = part_ms[dom] * 1e-3 / (calls_per_step[dom] * args.steps)
+    if not decode:
+        achieved = flops_step[dom] / calls_per_step[dom] / mean_launch_s / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1),
                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                     "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                    "traffic": ncu_traffic(args.workload),
+                    "traffic": ncu_traffic(dom), "kernel_of": dom,
                     "peak_source": (peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops_sustained: "
                                     "a seconds-long step)") if peaks["source"] == "measured"
                     else "fallback 1700 TFLOP/s sustained"}
     else:
-        alg_bytes_launch = step_total_bytes / len(calls_per_step)
-        achieved = alg_bytes_launch / mean_launch_s / 1e9
+        achieved = tbytes_step[dom] / calls_per_step[dom] / mean_launch_s / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                    "traffic": ncu_traffic(args.workload),
+                    "traffic": ncu_traffic(dom), "kernel_of": dom,
                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
                     if peaks["source"] == "measured" else "fallback 6800 GB/s"}
 
@@ -610,15 +708,12 @@ def run_ours(args, rank, local, world, pg):
             "vs_baseline": None, "dtype": "f16 (fp32 accumulate)",
             "data": "synthetic (seeded numpy PCG64; x~N(0,1), W~N(0,0.02) fp16, "
                     "quantized on the GPU)",
-            "config": {"workload": args.workload, "group": GROUP, "shapes": wl["shapes"],
-                       "Ms": wl["Ms"], "experts": wl["experts"],
-                       "l2": "inputs larger than L2: every call reads a distinct weight copy "
-                             "(rotation footprint >= 3x L2)",
-                       "timing": "one CUDA-graph replay of exactly `steps` steps, CUDA events",
-                       "pdl": not args.no_pdl, "variant": args.variant,
-                       "launch": ("grouped: one launch per (shape, M) over %d experts" % E)
-                       if grouped else "one call per GEMM",
-                       "parallelism": "replicas" if world > 1 else "1gpu"},
+            "config": config_obj(args, world),
+            "timed_region": {"replays": replays, "steps_per_replay": spr,
+                             "replay_ms_median": round(statistics.median(replay_ms), 4),
+                             "replay_ms_min": round(min(replay_ms), 4),
+                             "replay_ms_max": round(max(replay_ms), 4)},
+            "per_config": per_config,
             "us_per_call": per_m,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -635,17 +730,17 @@ def run_ours(args, rank, local, world, pg):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=240)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_square")
-    ap.add_argument("--reps", type=int, default=20, help="repeats of the per-M timing graphs")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--reps", type=int, default=20, help="repeats of the per-shape timing graphs")
     ap.add_argument("--no-pdl", action="store_true")
-    ap.add_argument("--no-grouped", action="store_true",
-                    help="MoE workload: one call per expert instead of one grouped launch")
-    ap.add_argument("--variant", choices=["auto", "tma", "registers"], default="auto",
+    ap.add_argument("--variant", choices=["auto", "tma", "registers", "stream"], default="auto",
                     help="decode kernel variant (auto = the library's dispatch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the repacked, grouped and streaming-read fields")
     ap.add_argument("--cublas", action=argparse.BooleanOptionalAction, default=True)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-shape", type=int, default=None,
@@ -660,7 +755,9 @@ def main():
     if args.only_shape is not None or args.only_m is not None:
         wl = dict(WORKLOADS[args.workload])
         if args.only_shape is not None:
-            wl["shapes"] = [wl["shapes"][args.only_shape]]
+            sh = shapes_of(wl)[args.only_shape]
+            CONFIGS["_only"] = [{k: v for k, v in sh.items() if k != "cfg"}]
+            wl["configs"] = ["_only"]
         if args.only_m is not None:
             wl["Ms"] = [args.only_m]
         WORKLOADS[args.workload] = wl

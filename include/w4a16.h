@@ -277,6 +277,20 @@ W4A16_API w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const 
                                          int M, int N, int K, int group,
                                          const w4a16_config *cfg, cudaStream_t stream);
 
+/*
+ * Measurement aid, not part of the GEMM: reads `bytes` from `src` (device, 16-byte
+ * aligned, a multiple of 16) into shared memory the way the decode kernels
+ * stream their weights -- 16 KB bulk copies into a ring of shared-memory slots,
+ * one CTA per SM, each taking a contiguous share -- with no arithmetic, and
+ * writes one word per CTA to `sink` (device, at least one uint32 per SM).
+ * flags: W4A16_FLAG_PDL launches it with programmatic dependent launch (the
+ * copies start before the previous kernel ends; the store to `sink` waits for
+ * it).  A chain of these calls over distinct buffers measures the per-launch
+ * streaming ceiling a decode GEMM of the same size can reach.
+ */
+W4A16_API w4a16_status w4a16_stream_read(const void *src, size_t bytes, uint32_t *sink,
+                               int flags, cudaStream_t stream);
+
 /* Host-only: the launch configuration w4a16_gemm_ex would use for this shape
  * with `request` (may be NULL) filled in.  Touches no GPU.  Returns the same
  * validation status the GEMM would (pointer checks excepted). */

@@ -29,7 +29,7 @@ def test_reference_arm_json_line():
     assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0
     assert d["scaling"] == "weak" and d["vs_baseline"] is None and d["dtype"] == "f64"
-    assert d["config"]["workload"] == "decode_square"
+    assert d["config"]["workload"] == "decode"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert "columns" in cb["sample"]

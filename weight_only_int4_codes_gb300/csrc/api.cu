@@ -679,6 +679,21 @@ w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const *x,
     return err == cudaSuccess ? W4A16_OK : cuda_fail(err, "grouped gemm launch");
 }
 
+w4a16_status w4a16_stream_read(const void *src, size_t bytes, uint32_t *sink, int flags,
+                               cudaStream_t stream) {
+    if (!src || !sink || bytes == 0)
+        return fail(W4A16_ERR_INVALID_ARG, "stream_read: null pointer or zero bytes");
+    if (!aligned16(src) || bytes % 16 != 0 || ((uintptr_t)sink & 3))
+        return fail(W4A16_ERR_MISALIGNED, "stream_read: src 16-byte aligned, bytes a multiple of "
+                    "16, sink 4-byte aligned");
+    int *status = nullptr;
+    cudaError_t e = kernel_status_address(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status word");
+    e = launch_read_probe(src, bytes, sink, device_info().sm_count, (flags & W4A16_FLAG_PDL) != 0,
+                          status, stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "stream_read launch");
+}
+
 w4a16_status w4a16_get_kernel_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

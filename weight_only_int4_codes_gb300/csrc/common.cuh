@@ -98,6 +98,12 @@ cudaError_t launch_decode_stream(const StreamCall &call, const w4a16_config &cfg
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group);
 
+// Measurement aid (read_probe.cu): stream `bytes` into shared memory the way
+// the decode kernels stream their weights, with no arithmetic; one word per
+// CTA to sink[ctas].
+cudaError_t launch_read_probe(const void *src, size_t bytes, uint32_t *sink, int ctas, bool pdl,
+                              int *status, cudaStream_t stream);
+
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (device, kernel): the attribute belongs to the device's
 // context, so a process that drives several GPUs sets it on each.

@@ -109,6 +109,7 @@ def load_library():
             "w4a16_gemm_repacked": [P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_gemm_grouped_repacked": [I, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_get_kernel_status": [P],
+            "w4a16_stream_read": [P, ctypes.c_size_t, P, I, P],
             "w4a16_last_error": [],
             "w4a16_version": [],
         }
@@ -247,6 +248,16 @@ def gemm_repacked(x, repacked, N: int, group: int = 128, out=None, config=None, 
         _dev(out, "out", torch.float16), M, N, K, group,
         ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
     return out
+
+
+def stream_read(src: torch.Tensor, sink: torch.Tensor, pdl: bool = False, stream=None):
+    """Measurement aid: stream all of ``src`` into shared memory the way the
+    decode kernels stream weights (no arithmetic); one word per SM to ``sink``."""
+    if not (src.is_cuda and src.is_contiguous()):
+        raise ValueError("src must be a contiguous CUDA tensor")
+    _check(_lib_fast().w4a16_stream_read(src.data_ptr(), src.numel() * src.element_size(),
+                                         _dev(sink, "sink", torch.int32),
+                                         FLAG_PDL if pdl else 0, _stream_handle(stream)))
 
 
 MAX_EXPERTS = 64
