@@ -278,6 +278,40 @@ W4A16_API w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const 
                                          const w4a16_config *cfg, cudaStream_t stream);
 
 /*
+ * w4a16_gemm_noalloc: the decode GEMM for callers that must not allocate GPU
+ * memory.  The pages have no counterpart to this entry point; it exists for
+ * callers such as a runtime that may only use memory reserved at start-up, a
+ * real-time loop where an allocation's unbounded latency is not allowed, or an
+ * application whose memory is owned entirely by its own allocator.  w4a16_gemm
+ * never allocates per call either, but the first stream-K call on a new stream
+ * allocates that stream's scratch once; this entry point never does.
+ *
+ * It runs the stream decode kernel (W4A16_DECODE_STREAM) with stream-K shares
+ * and the natural weight layout, and takes its scratch -- the arrival counters
+ * and fp32 partial sums of output tiles shared by two CTAs -- from one array of
+ * 4 MiB that the library keeps in device memory: 64 KiB of counters (one per
+ * 32..128-column tile) and 4,128,768 bytes of partials (two tiles of M x 32..128
+ * floats per CTA, one CTA per SM).  Every GPU that loads the library holds the
+ * array until the process exits.  A shape that needs more than that returns
+ * W4A16_ERR_UNSUPPORTED with the needed sizes in w4a16_last_error(); so do
+ * M > 16, N % 8 != 0 and groups that are not powers of two.
+ *
+ * Arguments, layouts, alignment and result: as w4a16_gemm (x, packed, scales,
+ * zeros, out device pointers; out fully overwritten).  The call allocates
+ * nothing (no cudaMalloc or any allocating library routine); it enqueues a
+ * clearing of the counters and the kernel on `stream`.
+ * - The first call on a device looks up the array's device address on that
+ *   device (once); make that first call before any stream capture begins.
+ * - All calls share the one array and it keeps the last call's contents: calls
+ *   whose work overlaps on the GPU (on different streams, or different threads
+ *   without ordering) race on it and their results are undefined.  Order them,
+ *   for example on one stream.
+ */
+W4A16_API w4a16_status w4a16_gemm_noalloc(const uint16_t *x, const uint32_t *packed,
+                                const uint16_t *scales, const uint16_t *zeros, uint16_t *out,
+                                int M, int N, int K, int group, cudaStream_t stream);
+
+/*
  * Measurement aid, not part of the GEMM: reads `bytes` from `src` (device, 16-byte
  * aligned, a multiple of 16) into shared memory the way the decode kernels
  * stream their weights -- 16 KB bulk copies into a ring of shared-memory slots,

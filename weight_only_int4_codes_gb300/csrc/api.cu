@@ -679,6 +679,50 @@ w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const *x,
     return err == cudaSuccess ? W4A16_OK : cuda_fail(err, "grouped gemm launch");
 }
 
+w4a16_status w4a16_gemm_noalloc(const uint16_t *x, const uint32_t *packed,
+                                const uint16_t *scales, const uint16_t *zeros, uint16_t *out,
+                                int M, int N, int K, int group, cudaStream_t stream) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if (!x || !packed || !scales || !zeros || !out)
+        return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales) || !aligned16(zeros) ||
+        !aligned16(out))
+        return fail(W4A16_ERR_MISALIGNED, "x, packed, scales, zeros and out must be 16-byte "
+                    "aligned");
+    if (M > 16)
+        return fail(W4A16_ERR_UNSUPPORTED, "gemm_noalloc: M <= 16 (got %d)", M);
+    w4a16_config c = {};
+    c.path = W4A16_PATH_DECODE;
+    c.variant = W4A16_DECODE_STREAM;
+    c.split_k = 2;
+    plan_decode_stream(M, N, K, group, 1, false, device_info().sm_count, c);
+    if (!decode_stream_supported(M, N, K, group, c.warps_n, false))
+        return fail(W4A16_ERR_UNSUPPORTED, "gemm_noalloc: no stream kernel for M=%d N=%d K=%d "
+                    "group=%d (N %% 8 == 0 and a power-of-two group are required)", M, N, K, group);
+    StreamCall sc;
+    sc.E = 1;
+    sc.x[0] = x;
+    sc.w[0] = packed;
+    sc.s[0] = scales;
+    sc.z[0] = zeros;
+    sc.out[0] = out;
+    sc.M = M;
+    sc.N = N;
+    sc.K = K;
+    sc.group = group;
+    sc.permuted = false;
+    const NoAllocResult r = launch_decode_stream_noalloc(sc, c.warps_n, false, stream);
+    if (r.err == cudaErrorInvalidValue)
+        return fail(W4A16_ERR_UNSUPPORTED, "gemm_noalloc: the call needs %zu bytes of tile "
+                    "counters and %zu bytes of partial sums; the library's fixed scratch holds "
+                    "65536 and 4128768", r.need_counters, r.need_partials);
+    if (r.err == cudaErrorNotSupported)
+        return fail(W4A16_ERR_UNSUPPORTED, "gemm_noalloc: no kernel for this configuration");
+    return r.err == cudaSuccess ? W4A16_OK : cuda_fail(r.err, "gemm_noalloc");
+}
+
 w4a16_status w4a16_stream_read(const void *src, size_t bytes, uint32_t *sink, int flags,
                                cudaStream_t stream) {
     if (!src || !sink || bytes == 0)

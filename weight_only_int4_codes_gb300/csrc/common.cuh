@@ -94,6 +94,15 @@ bool decode_stream_supported(int M, int N, int K, int group, int bns, bool perm)
 int decode_stream_stage_k(int bns);   // k per stage of a tile of bns strips
 cudaError_t launch_decode_stream(const StreamCall &call, const w4a16_config &cfg,
                                  cudaStream_t stream);
+// The same kernel with stream-K shares and its scratch in a fixed device array
+// of this library (w4a16_gemm_noalloc): nothing is allocated.  `need_*` report
+// the scratch a call asked for (cudaErrorInvalidValue when it is too large).
+struct NoAllocResult {
+    cudaError_t err;
+    size_t need_counters, need_partials;
+};
+NoAllocResult launch_decode_stream_noalloc(const StreamCall &call, int bns, bool pdl,
+                                           cudaStream_t stream);
 // Prefill path (tcgen05).  Returns cudaErrorNotSupported if unavailable.
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group);

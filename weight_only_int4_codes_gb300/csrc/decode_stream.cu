@@ -899,6 +899,95 @@ int layout_for_call(bool permuted, int E, int N) {
 
 int decode_stream_stage_k(int bns) { return 8 * stage_rows(bns); }
 
+// ---------------------------------------------------------------- no-alloc
+// Scratch of w4a16_gemm_noalloc: one fixed array in device memory that every
+// GPU loading this library holds until the process exits.  Its first
+// kNoAllocCounterBytes hold the per-tile arrival counters, the rest the fp32
+// partials of shared tiles.  In host code the name below is only a stand-in
+// for the array; its device address comes from cudaGetSymbolAddress.
+constexpr size_t kNoAllocBytes = (size_t)4 << 20;            // 4 MiB in all
+constexpr size_t kNoAllocCounterBytes = (size_t)64 << 10;    // 16384 tiles
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// The array's device address on the current device, looked up once per device.
+static bool noalloc_scratch(unsigned char **ptr) {
+    static std::mutex mu;
+    static unsigned char *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return false;
+        }
+        addr[dev] = static_cast<unsigned char *>(p);
+    }
+    *ptr = addr[dev];
+    return true;
+}
+
+NoAllocResult launch_decode_stream_noalloc(const StreamCall &call, int bns, bool pdl,
+                                           cudaStream_t stream) {
+    const int M = call.M, N = call.N, K = call.K, group = call.group;
+    if (call.E != 1 || call.permuted || !decode_stream_supported(M, N, K, group, bns, false))
+        return NoAllocResult{cudaErrorNotSupported, 0, 0};
+    // per-row copies of the natural layout: no tensor map to encode
+    StreamLayout L;
+    if (!stream_layout(M, group, bns, kRows, L)) return NoAllocResult{cudaErrorNotSupported, 0, 0};
+    const int BN = 32 * bns, SK = 8 * stage_rows(bns);
+    StreamArgs sa = {};
+    sa.M = M;
+    sa.N = N;
+    sa.K = K;
+    sa.group = group;
+    sa.T = (N + BN - 1) / BN;
+    sa.KS = (K + SK - 1) / SK;
+    const long long units = (long long)sa.T * sa.KS;
+    int grid = device_info().sm_count;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    if (grid > units) grid = (int)units;
+    // what the call needs: one counter per tile, two fp32 partial tiles per CTA
+    const size_t need_counters = (size_t)sa.T * sizeof(int);
+    const size_t need_partials = (size_t)2 * grid * M * BN * sizeof(float);
+    if (units > (1ll << 30) || need_counters > kNoAllocCounterBytes ||
+        need_partials > kNoAllocBytes - kNoAllocCounterBytes)
+        return NoAllocResult{cudaErrorInvalidValue, need_counters, need_partials};
+    unsigned char *base = nullptr;
+    if (!noalloc_scratch(&base)) return NoAllocResult{cudaErrorInvalidSymbol, 0, 0};
+    sa.U = (int)units;
+    sa.align = 0;                                  // stream-K shares: the scratch is used
+    sa.counters = reinterpret_cast<int *>(base);
+    sa.scratch = reinterpret_cast<float *>(base + kNoAllocCounterBytes);
+    // the counters must read zero when the kernel starts; the array keeps
+    // whatever the previous call (on any stream) left there
+    cudaError_t e = cudaMemsetAsync(sa.counters, 0, need_counters, stream);
+    if (e != cudaSuccess) return NoAllocResult{e, 0, 0};
+    sa.stages = L.stages;
+    sa.stage_bytes = L.stage_bytes;
+    sa.w_pitch = L.w_pitch;
+    sa.sz_off = L.sz_off;
+    sa.sz_rows = L.sz_rows;
+    sa.z_delta = L.z_delta;
+    sa.x_off = L.x_off;
+    sa.x_pitch = L.x_pitch;
+    sa.blk_bytes = L.blk_bytes;
+    sa.red_off = L.red_off;
+    sa.bar_off = L.bar_off;
+    sa.status = stream_status_word();
+    if (!sa.status) return NoAllocResult{cudaErrorInvalidDevice, 0, 0};
+    sa.timeout_ns = 1000000000ull;
+    const bool og = group >= 32 * kSPW;
+    const int nt = M > 8 ? 2 : 1;
+    CUtensorMap maps[3];
+    memset(maps, 0, sizeof maps);
+    StreamTable<1> tab;
+    tab.e[0] = StreamOperands{call.x[0], call.w[0], call.s[0], call.z[0], call.out[0]};
+    e = dispatch_shape<kRows, 1>(nt, bns, og, sa, tab, maps, grid, L.smem_bytes, pdl, stream);
+    return NoAllocResult{e, need_counters, need_partials};
+}
+
 bool decode_stream_supported(int M, int N, int K, int group, int bns, bool perm) {
     const bool g_ok = group == 32 || group == 64 || group == 128 || group == 256 ||
                       group == 512 || group == 1024;

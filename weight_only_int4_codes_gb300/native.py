@@ -110,6 +110,7 @@ def load_library():
             "w4a16_gemm_grouped_repacked": [I, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_get_kernel_status": [P],
             "w4a16_stream_read": [P, ctypes.c_size_t, P, I, P],
+            "w4a16_gemm_noalloc": [P, P, P, P, P, I, I, I, I, P],
             "w4a16_last_error": [],
             "w4a16_version": [],
         }
@@ -247,6 +248,21 @@ def gemm_repacked(x, repacked, N: int, group: int = 128, out=None, config=None, 
         _dev(x, "x", torch.float16), _dev(repacked, "repacked", torch.uint8),
         _dev(out, "out", torch.float16), M, N, K, group,
         ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
+    return out
+
+
+def gemm_noalloc(x, packed, scales, zeros, group: int = 128, out=None, stream=None):
+    """out [M,N] fp16 = x [M,K] @ dequant(packed, scales, zeros) through the entry
+    point that allocates no GPU memory (its scratch is a fixed array inside the
+    library; calls that overlap on the GPU must not share it).  M <= 16."""
+    M, K = x.shape
+    N = packed.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(_lib_fast().w4a16_gemm_noalloc(
+        _dev(x, "x", torch.float16), _dev(packed, "packed", torch.int32),
+        _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
+        _dev(out, "out", torch.float16), M, N, K, group, _stream_handle(stream)))
     return out
 
 
