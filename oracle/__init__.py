@@ -66,13 +66,21 @@ class Oracle:
         lib.oracle_dequant.argtypes = [P, P, P, I, I, I, P]
         lib.oracle_gemm.argtypes = [P, P, P, P, I, I, I, I, P]
         lib.oracle_num_threads.argtypes = []
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_quantize_pack_bf16.argtypes = [P, I, I, I, P, P, P, P]
+        lib.oracle_dequant_bf16.argtypes = [P, P, P, I, I, I, P]
+        lib.oracle_gemm_bf16.argtypes = [P, P, P, P, I, I, I, I, P]
         lib.oracle_permuted_words.argtypes = [I, I, I]
         lib.oracle_permuted_words.restype = ctypes.c_longlong
         lib.oracle_permute.argtypes = [P, P, P, I, I, I, P]
         lib.oracle_unpermute.argtypes = [P, I, I, I, P, P, P]
         for f in (lib.oracle_quantize_pack, lib.oracle_quantize_pack_symmetric, lib.oracle_unpack,
                   lib.oracle_dequant, lib.oracle_gemm, lib.oracle_num_threads,
-                  lib.oracle_permute, lib.oracle_unpermute):
+                  lib.oracle_permute, lib.oracle_unpermute, lib.oracle_quantize_pack_bf16,
+                  lib.oracle_dequant_bf16, lib.oracle_gemm_bf16):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -138,6 +146,53 @@ class Oracle:
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
+    # ------------------------------------------------------------- bfloat16
+    # bfloat16 values travel as uint16 bit patterns (numpy has no bfloat16)
+    def bf16_to_double(self, bits: int) -> float:
+        return self.lib.oracle_bf16_to_double(int(bits))
+
+    def double_to_bf16(self, v: float) -> int:
+        return int(self.lib.oracle_double_to_bf16(float(v)))
+
+    def quantize_pack_bf16(self, W_bits, group: int = 128, return_codes: bool = False):
+        """W [K,N] bfloat16 bit patterns -> (packed uint32 [K/8,N], scales and zeros
+        as bfloat16 bit patterns [K/g,N])."""
+        Wb = _as_u16(W_bits)
+        K, N = Wb.shape
+        G = K // group if group > 0 else 0
+        packed = np.zeros((max(K // 8, 0), N), dtype=np.uint32)
+        scales = np.zeros((G, N), dtype=np.uint16)
+        zeros = np.zeros((G, N), dtype=np.uint16)
+        q = np.zeros((K, N), dtype=np.uint8) if return_codes else None
+        _check(self.lib.oracle_quantize_pack_bf16(_ptr(Wb), K, N, group, _ptr(packed),
+                                                  _ptr(scales), _ptr(zeros),
+                                                  _ptr(q) if q is not None else None),
+               "quantize_pack_bf16")
+        out = (packed, scales, zeros)
+        return out + (q,) if return_codes else out
+
+    def dequant_bf16(self, packed, scales, zeros, group: int = 128) -> np.ndarray:
+        """-> Wdq [K,N] bfloat16 bit patterns, bf16((q - z) * s)."""
+        packed = np.ascontiguousarray(packed, dtype=np.uint32)
+        K, N = packed.shape[0] * 8, packed.shape[1]
+        Wdq = np.zeros((K, N), dtype=np.uint16)
+        _check(self.lib.oracle_dequant_bf16(_ptr(packed), _ptr(_as_u16(scales)),
+                                            _ptr(_as_u16(zeros)), K, N, group, _ptr(Wdq)),
+               "dequant_bf16")
+        return Wdq
+
+    def gemm_bf16(self, x_bits, packed, scales, zeros, group: int = 128) -> np.ndarray:
+        """x [M,K] bfloat16 bit patterns -> ref fp64 [M,N] = x @ bf16 dequant."""
+        xb = _as_u16(x_bits)
+        packed = np.ascontiguousarray(packed, dtype=np.uint32)
+        M, K = xb.shape
+        N = packed.shape[1]
+        ref = np.zeros((M, N), dtype=np.float64)
+        _check(self.lib.oracle_gemm_bf16(_ptr(xb), _ptr(packed), _ptr(_as_u16(scales)),
+                                         _ptr(_as_u16(zeros)), M, N, K, group, _ptr(ref)),
+               "gemm_bf16")
+        return ref
+
     # ------------------------------------------------- pre-permuted layout
     def permute(self, packed, scales, zeros, group: int = 128) -> np.ndarray:
         """natural (packed [K/8,N], scales, zeros) -> repacked uint32 words (the
@@ -177,6 +232,13 @@ def _as_half_bits(a) -> np.ndarray:
         a = a.view(np.uint16)
     if a.dtype != np.uint16:
         raise TypeError("expected float16 values or uint16 bit patterns, got %s" % a.dtype)
+    return np.ascontiguousarray(a)
+
+
+def _as_u16(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("expected uint16 bit patterns, got %s" % a.dtype)
     return np.ascontiguousarray(a)
 
 
@@ -220,6 +282,18 @@ def gemm(x, packed, scales, zeros, group: int = 128):
 
 def num_threads() -> int:
     return default().num_threads()
+
+
+def quantize_pack_bf16(W_bits, group: int = 128, return_codes: bool = False):
+    return default().quantize_pack_bf16(W_bits, group, return_codes)
+
+
+def dequant_bf16(packed, scales, zeros, group: int = 128):
+    return default().dequant_bf16(packed, scales, zeros, group)
+
+
+def gemm_bf16(x_bits, packed, scales, zeros, group: int = 128):
+    return default().gemm_bf16(x_bits, packed, scales, zeros, group)
 
 
 def permute(packed, scales, zeros, group: int = 128):

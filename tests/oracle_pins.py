@@ -371,6 +371,105 @@ def pin_permuted_layout_numpy(orc):
         assert np.array_equal(back[2].view(np.uint16), zeros)
 
 
+# ------------------------------------------------------------------ bfloat16
+def _bf16_from_f32_bits(u32: np.ndarray) -> np.ndarray:
+    """Independent bfloat16 rounding of float32 values: round to nearest even on
+    the integer bit pattern (the upper 16 bits, plus one when the dropped half
+    is above the midpoint or at it with an odd kept part)."""
+    u = u32.astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def pin_bf16_decode_exhaustive(orc):
+    """Every bfloat16 pattern decodes to the float32 whose upper 16 bits it is."""
+    bits = np.arange(65536, dtype=np.uint32)
+    ref = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = np.array([orc.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0])
+
+
+def pin_bf16_encode(orc):
+    """bfloat16 encoding, round to nearest even: finite patterns round-trip,
+    midpoints go to the even neighbour, and random float32 values (subnormal
+    to huge) match the integer rounding of their bit patterns."""
+    for b in list(range(0, 0x7f80, 7)) + [0x0001, 0x007f, 0x0080, 0x7f7f]:
+        v = float(np.array([b << 16], dtype=np.uint32).view(np.float32)[0])
+        assert orc.double_to_bf16(v) == b, hex(b)
+        assert orc.double_to_bf16(-v) == (b | 0x8000) or v == 0.0, hex(b)
+    for b in range(0, 0x7f7f, 13):
+        lo = float(np.array([b << 16], dtype=np.uint32).view(np.float32)[0])
+        hi = float(np.array([(b + 1) << 16], dtype=np.uint32).view(np.float32)[0])
+        mid = (lo + hi) / 2                     # exact in fp64
+        even = b if b % 2 == 0 else b + 1
+        assert orc.double_to_bf16(mid) == even, hex(b)
+    rng = np.random.Generator(np.random.PCG64(77))
+    u = rng.integers(0, 0x7f800000, size=20000, dtype=np.uint64).astype(np.uint32)
+    ref = _bf16_from_f32_bits(u)
+    vals = u.view(np.float32).astype(np.float64)
+    got = np.array([orc.double_to_bf16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    assert orc.double_to_bf16(3.5e38) == 0x7f80          # past the largest finite: inf
+
+
+def pin_golden_bf16_8x4(orc):
+    """The hand-worked bfloat16 example: codes, scales, zeros and every
+    dequantized weight (including a rounding tie) bit for bit."""
+    with open(os.path.join(GOLDEN, "hand_8x4_g8_bf16.json")) as f:
+        fx = json.load(f)
+    W = np.array([[int(v, 16) for v in r] for r in fx["w_bits"]], dtype=np.uint16)
+    packed, scales, zeros = orc.quantize_pack_bf16(W, fx["group"])
+    assert [int(v) for v in packed[0]] == [int(v, 16) for v in fx["packed"]]
+    assert [int(v) for v in scales[0]] == [int(v, 16) for v in fx["scales"]]
+    assert [int(v) for v in zeros[0]] == [int(v, 16) for v in fx["zeros"]]
+    wdq = orc.dequant_bf16(packed, scales, zeros, fx["group"])
+    assert np.array_equal(wdq, np.array([[int(v, 16) for v in r] for r in fx["wdq"]],
+                                        dtype=np.uint16))
+
+
+def pin_bf16_code_ties(orc):
+    """Codes at exact ties of w / s, worked by hand: the group [-1, 14, 0.5,
+    1.5, 2.5, -0.5, 0, 7.5] has s = 15 / 15 = 1 and z = rint(1 / 1) = 1, and
+    q = rint(w / s) + z rounds each half-integer w / s to the even integer
+    before the zero is added: codes [0, 15, 1, 3, 3, 1, 1, 9]."""
+    w = np.array([-1.0, 14.0, 0.5, 1.5, 2.5, -0.5, 0.0, 7.5], dtype=np.float32)
+    bits = (w.view(np.uint32) >> 16).astype(np.uint16).reshape(8, 1)
+    packed, scales, zeros = orc.quantize_pack_bf16(bits, 8)
+    assert int(scales[0, 0]) == 0x3F80 and int(zeros[0, 0]) == 0x3F80   # s = 1, z = 1
+    codes = [(int(packed[0, 0]) >> (4 * k)) & 15 for k in range(8)]
+    assert codes == [0, 15, 1, 3, 3, 1, 1, 9], codes
+
+
+def _bf16_values(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pin_bf16_gemm(orc):
+    """The bfloat16 GEMM: one-hot rows of x return the dequantized rows exactly,
+    and a random x agrees with numpy's matmul of the bf16 values; the quantizer
+    keeps |w - (q - z) s| <= s/2 for unclipped entries."""
+    K, N, M, g = 256, 24, 5, 64
+    W = synth.weight_bf16(K, N, seed=88)
+    packed, scales, zeros, q = orc.quantize_pack_bf16(W, g, return_codes=True)
+    s = np.repeat(_bf16_values(scales), g, axis=0)
+    z = np.repeat(_bf16_values(zeros), g, axis=0)
+    w = _bf16_values(W)
+    err = np.abs(w - (q.astype(np.float64) - z) * s)
+    inside = (q > 0) & (q < 15)
+    assert np.all(err[inside] <= s[inside] / 2 + 1e-12)
+    wdq = _bf16_values(orc.dequant_bf16(packed, scales, zeros, g))
+    ks = [0, 7, 100, 255, 64]
+    x = np.zeros((len(ks), K), dtype=np.uint16)
+    x[np.arange(len(ks)), ks] = 0x3F80                    # bfloat16 1.0
+    ref = orc.gemm_bf16(x, packed, scales, zeros, g)
+    assert np.array_equal(ref, wdq[ks])
+    xr = synth.activations_bf16(M, K, seed=89)
+    ref = orc.gemm_bf16(xr, packed, scales, zeros, g)
+    assert np.allclose(ref, _bf16_values(xr) @ wdq, rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [
     pin_half_decode_exhaustive,
     pin_half_encode,
@@ -387,4 +486,9 @@ ALL_PINS = [
     pin_brute_force,
     pin_golden_permuted_layout,
     pin_permuted_layout_numpy,
+    pin_bf16_decode_exhaustive,
+    pin_bf16_encode,
+    pin_golden_bf16_8x4,
+    pin_bf16_code_ties,
+    pin_bf16_gemm,
 ]

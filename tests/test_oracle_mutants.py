@@ -76,6 +76,39 @@ MUTANTS = [
     ("permute_group_row_ignores_block",
      "int j = 256 * kb / group + gi;\n                        int n = 32 * sn + 4 * g + c;\n                        int h = (gi * 8 + g) * 8 + c;\n                        sz[h]",
      "int j = gi;\n                        int n = 32 * sn + 4 * g + c;\n                        int h = (gi * 8 + g) * 8 + c;\n                        sz[h]"),
+    ("bf16_decode_bias",
+     "v = ldexp((double)(128 + frac), expo - 134);",
+     "v = ldexp((double)(128 + frac), expo - 133);"),
+    ("bf16_encode_truncates",
+     "double m = rint(ldexp(f, 8));",
+     "double m = floor(ldexp(f, 8));"),
+    ("bf16_subnormal_truncates",
+     "double q = rint(ldexp(a, 133));",
+     "double q = floor(ldexp(a, 133));"),
+    ("bf16_scale_divisor_16",
+     "uint16_t s_bits = oracle_double_to_bf16((mx - mn) / 15.0);",
+     "uint16_t s_bits = oracle_double_to_bf16((mx - mn) / 16.0);"),
+    ("bf16_degenerate_scale_fp16_pattern",
+     "s_bits = 0x3f80;     /* 1.0 */",
+     "s_bits = 0x3c00;     /* 1.0 */"),
+    ("bf16_dequant_sign",
+     "Wdq[(size_t)k * N + n] = oracle_double_to_bf16((q - z) * s);",
+     "Wdq[(size_t)k * N + n] = oracle_double_to_bf16((z - q) * s);"),
+    ("bf16_hqq_style_rounding",
+     "double qv = rint(w / s) + (double)z;",
+     "double qv = rint(w / s + (double)z);"),
+    ("bf16_half_away_rounding",
+     "double qv = rint(w / s) + (double)z;",
+     "double qv = round(w / s) + (double)z;"),
+    ("bf16_nibble_order_reversed",
+     "packed[(size_t)(k / 8) * N + n] |= q << (4 * (k & 7));",
+     "packed[(size_t)(k / 8) * N + n] |= q << (4 * (7 - (k & 7)));"),
+    ("bf16_zero_not_clamped",
+     "zq = zq < 0.0 ? 0.0 : (zq > 15.0 ? 15.0 : zq);",
+     "zq = zq < 0.0 ? 0.0 : zq;"),
+    ("bf16_gemm_drops_last_term",
+     "for (int k = 0; k < K; ++k) sum += xm[k] * w[k];",
+     "for (int k = 0; k < K - 1; ++k) sum += xm[k] * w[k];"),
     ("degenerate_scale_kept_zero",
      "s_bits = 0x3c00;     /* 1.0 */\n                s = 1.0;",
      "s_bits = 0x3c00;     /* 1.0 */\n                s = 1e-300;"),

@@ -6,8 +6,10 @@ and the fp64 oracle may take their inputs from it.
 
 Distributions (the workloads the pages measure on: decode-regime dense FFN,
 square projections and MoE-expert projections at group 128):
-  x ~ N(0, 1)      drawn as float32, rounded to fp16
+  x ~ N(0, 1)      drawn as float32, rounded to fp16 (or to bfloat16 for the
+                   bf16 variant: the same draws, stored as bfloat16)
   W ~ N(0, 0.02)   drawn as float32 (standard deviation 0.02), rounded to fp16
+                   (or bfloat16)
   outliers: each W entry independently with probability 0.001 is multiplied
             by 20 (in float32, before the fp16 rounding)
 
@@ -55,6 +57,37 @@ def weight(K: int, N: int, seed: int, outliers: bool = False, std: float = 0.02)
         mask = rng.random((K, N), dtype=np.float32) < np.float32(0.001)
         w[mask] *= np.float32(20.0)
     return w.astype(np.float16)
+
+
+def _draw_weight(K: int, N: int, seed: int, outliers: bool, std: float) -> np.ndarray:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    w = rng.standard_normal((K, N), dtype=np.float32)
+    w *= np.float32(std)
+    if outliers:
+        mask = rng.random((K, N), dtype=np.float32) < np.float32(0.001)
+        w[mask] *= np.float32(20.0)
+    return w
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 values -> bfloat16 bit patterns (uint16), round to nearest even
+    on the float32 bit pattern (finite inputs; these are the storage format of
+    the random draws, numpy having no bfloat16 type)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def weight_bf16(K: int, N: int, seed: int, outliers: bool = False,
+                std: float = 0.02) -> np.ndarray:
+    """bfloat16 [K, N] weight (bit patterns), the draws of weight() stored as bf16."""
+    return bf16_bits(_draw_weight(K, N, seed, outliers, std))
+
+
+def activations_bf16(M: int, K: int, seed: int) -> np.ndarray:
+    """bfloat16 [M, K] activations (bit patterns), the draws of activations()."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
 
 
 def activations(M: int, K: int, seed: int) -> np.ndarray:
