@@ -98,6 +98,23 @@ typedef enum w4a16_path {
 #define W4A16_PREFILL_A_TMEM 1    /* dequantized W^T operand in tensor memory (default) */
 #define W4A16_PREFILL_A_SMEM 2    /* dequantized W^T operand in shared memory */
 
+/* Element type of x, scales, zeros and out (w4a16_config.dtype).  The codes
+ * and their packing are the same for both. */
+#define W4A16_DTYPE_F16 0   /* binary16 (default) */
+#define W4A16_DTYPE_BF16 1  /* bfloat16: 1 sign, 8 exponent, 7 fraction bits.
+                               The pages name bf16 as the other model dtype
+                               (GemLite README, usage section; page "Beating
+                               FP16 with 4-bit Weights", section "What's
+                               next") but give no recipe; this library keeps
+                               the fp16 recipe with bfloat16 wherever a value
+                               is stored, and the kernels multiply x by the
+                               dequantized weight bf16((q - z) * s), one
+                               rounding of the exact product.  Decode path:
+                               registers variant only (W4A16_DECODE_AUTO
+                               selects it); prefill path: A in tensor memory
+                               only.  Other combinations return
+                               W4A16_ERR_UNSUPPORTED. */
+
 /*
  * Launch configuration of one GEMM call.  Zero in any field means "choose
  * automatically"; w4a16_plan() returns the choice for a shape.
@@ -119,6 +136,7 @@ typedef struct w4a16_config {
     int flags;      /* W4A16_FLAG_* */
     int variant;    /* decode: W4A16_DECODE_*; prefill: W4A16_PREFILL_* */
     int ctas;       /* decode, stream variant: CTAs in the grid (0: one per SM) */
+    int dtype;      /* W4A16_DTYPE_F16 (0) or W4A16_DTYPE_BF16 */
 } w4a16_config;
 
 /*
@@ -170,6 +188,23 @@ W4A16_API w4a16_status w4a16_dequantize(const uint32_t *packed, const uint16_t *
                               int K, int N, int group, cudaStream_t stream);
 
 /*
+ * bfloat16 counterparts of w4a16_quantize_pack and w4a16_dequantize (same
+ * layouts; W, scales, zeros and W_out hold bfloat16 bit patterns):
+ *     s = bf16((max - min) / 15)   fp64 arithmetic, one rounding; 1.0 if 0
+ *     z = clamp(rint(-min / s), 0, 15), stored as a bfloat16 integer
+ *     q = clamp(rint(W / s) + z, 0, 15)
+ *     W_out[k,n] = bf16((q - z) * s), one rounding of the exact product.
+ * Bit-exact with the oracle's bfloat16 variant.  Same argument checks and
+ * error returns as the fp16 entries.
+ */
+W4A16_API w4a16_status w4a16_quantize_pack_bf16(const uint16_t *W, int K, int N, int group,
+                                      uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                      cudaStream_t stream);
+W4A16_API w4a16_status w4a16_dequantize_bf16(const uint32_t *packed, const uint16_t *scales,
+                                   const uint16_t *zeros, uint16_t *W_out, int K, int N,
+                                   int group, cudaStream_t stream);
+
+/*
  * out[M,N] = x[M,K] . dequant(packed, scales, zeros), fp32 accumulation,
  * fp16 output (round to nearest even).  The weight is dequantized inside the
  * kernel and never materialized.  Automatic path selection.
@@ -179,8 +214,10 @@ W4A16_API w4a16_status w4a16_gemm(const uint16_t *x, const uint32_t *packed,
                         int M, int N, int K, int group, cudaStream_t stream);
 
 /* As w4a16_gemm, with an explicit (possibly partial) launch configuration;
- * cfg == NULL is the same as w4a16_gemm.  Unsupported combinations return
- * W4A16_ERR_UNSUPPORTED without enqueuing anything. */
+ * cfg == NULL is the same as w4a16_gemm.  cfg->dtype = W4A16_DTYPE_BF16
+ * makes x, scales, zeros and out bfloat16 (out rounded to nearest even).
+ * Unsupported combinations return W4A16_ERR_UNSUPPORTED without enqueuing
+ * anything. */
 W4A16_API w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed,
                            const uint16_t *scales, const uint16_t *zeros, uint16_t *out,
                            int M, int N, int K, int group, const w4a16_config *cfg,

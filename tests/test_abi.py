@@ -168,3 +168,30 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(native, "_PKG", str(tmp_path))
     with pytest.raises(native.W4A16Error):
         native.load_library()
+
+
+def test_bf16_planning():
+    """dtype = bf16: decode on the registers variant, prefill on A in tensor
+    memory; the other variants and unknown dtypes are refused on the host."""
+    for M in (1, 8, 16):
+        p = w4.plan(M, 4096, 4096, dtype="bf16")
+        assert (p["path"], p["variant"], p["dtype"]) == (1, 2, 1)
+        assert p["warps_k"] * p["steps"] * 4 * p["split_k"] >= 4096 // 8
+    p = w4.plan(1024, 14336, 4096, dtype="bf16")
+    assert (p["path"], p["dtype"]) == (2, 1) and p["variant"] == 1
+    for bad in (dict(path="decode", variant="tma"), dict(path="decode", variant="stream"),
+                dict(path="prefill", variant="smem", tile_m=64)):
+        with pytest.raises(native.W4A16Error) as e:
+            w4.plan(64 if bad["path"] == "prefill" else 4, 4096, 4096, dtype="bf16", **bad)
+        assert e.value.status == 2
+    with pytest.raises(native.W4A16Error) as e:
+        w4.plan(4, 4096, 4096, dtype=7)
+    assert e.value.status == 1
+    assert w4.plan(4, 4096, 4096)["dtype"] == 0
+
+
+def test_bf16_entries_validate_before_touching_the_gpu(lib):
+    assert lib.w4a16_quantize_pack_bf16(None, 512, 256, 128, None, None, None, None) == 1
+    assert lib.w4a16_quantize_pack_bf16(16, 500, 256, 128, 16, 16, 16, None) == 1   # K % group
+    assert lib.w4a16_dequantize_bf16(16, 16, 17, 16, 512, 256, 128, None) == 3     # misaligned
+    assert lib.w4a16_quantize_pack_bf16(16, 512, 0, 128, 16, 16, 16, None) == 0    # N == 0

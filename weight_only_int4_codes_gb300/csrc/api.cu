@@ -283,6 +283,9 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
     w4a16_status st = check_shape(M, N, K, group);
     if (st != W4A16_OK) return st;
     c = req ? *req : w4a16_config{};
+    if (c.dtype != W4A16_DTYPE_F16 && c.dtype != W4A16_DTYPE_BF16)
+        return fail(W4A16_ERR_INVALID_ARG, "unknown dtype %d", c.dtype);
+    const bool bf = c.dtype == W4A16_DTYPE_BF16;
     if (c.path == W4A16_PATH_AUTO) {
         c.path = W4A16_PATH_DECODE;
         if (M > kDecodeMaxM) {
@@ -293,6 +296,13 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
         }
     }
     if (c.path == W4A16_PATH_DECODE) {
+        // bfloat16 runs on the registers variant (the only decode kernel
+        // built for it); the measured table is for fp16
+        if (bf && c.variant == W4A16_DECODE_AUTO) c.variant = W4A16_DECODE_REGISTERS;
+        if (bf && c.variant != W4A16_DECODE_REGISTERS)
+            return fail(W4A16_ERR_UNSUPPORTED,
+                        "bfloat16 decode: registers variant only (variant %d requested)",
+                        c.variant);
         if (M <= 16) decode_from_table(M, N, K, group, c);
         if (c.variant == W4A16_DECODE_AUTO)
             c.variant = tma_variant_possible(N, group) ? W4A16_DECODE_TMA : W4A16_DECODE_REGISTERS;
@@ -406,6 +416,39 @@ w4a16_status w4a16_dequantize(const uint32_t *packed, const uint16_t *scales,
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "dequantize launch");
 }
 
+namespace {
+// Argument checks shared by the quantize / dequantize entries.
+w4a16_status check_quant_args(const void *W, int K, int N, int group, const void *packed,
+                              const void *scales, const void *zeros) {
+    w4a16_status st = check_shape(0, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if (!W || !packed || !scales || !zeros) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+    if (((uintptr_t)W & 1) || ((uintptr_t)packed & 3) || ((uintptr_t)scales & 1) ||
+        ((uintptr_t)zeros & 1))
+        return fail(W4A16_ERR_MISALIGNED, "pointer not aligned to its element size");
+    return W4A16_OK;
+}
+}  // namespace
+
+w4a16_status w4a16_quantize_pack_bf16(const uint16_t *W, int K, int N, int group,
+                                      uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                      cudaStream_t stream) {
+    w4a16_status st = check_quant_args(W, K, N, group, packed, scales, zeros);
+    if (st != W4A16_OK || N == 0) return st;
+    cudaError_t e = launch_quantize_pack_bf16(W, K, N, group, packed, scales, zeros, stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "quantize_pack_bf16 launch");
+}
+
+w4a16_status w4a16_dequantize_bf16(const uint32_t *packed, const uint16_t *scales,
+                                   const uint16_t *zeros, uint16_t *W_out, int K, int N,
+                                   int group, cudaStream_t stream) {
+    w4a16_status st = check_quant_args(W_out, K, N, group, packed, scales, zeros);
+    if (st != W4A16_OK || N == 0) return st;
+    cudaError_t e = launch_dequantize_bf16(packed, scales, zeros, W_out, K, N, group, stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "dequantize_bf16 launch");
+}
+
 w4a16_status w4a16_plan(int M, int N, int K, int group, const w4a16_config *request,
                         w4a16_config *plan_out) {
     if (!plan_out) return fail(W4A16_ERR_INVALID_ARG, "plan_out is null");
@@ -483,6 +526,8 @@ w4a16_status w4a16_gemm_grouped(int E, const uint16_t *const *x, const uint32_t 
                         "be 16-byte aligned", e);
     }
     if (M == 0 || N == 0) return W4A16_OK;
+    if (cfg && cfg->dtype != W4A16_DTYPE_F16 && M <= kDecodeMaxM)
+        return fail(W4A16_ERR_UNSUPPORTED, "grouped GEMM at M <= %d: fp16 only", kDecodeMaxM);
     if (M > kDecodeMaxM) {
         // prefill-sized experts: one launch each (the tensor-core path is
         // already compute-bound per expert)
@@ -590,6 +635,8 @@ w4a16_status plan_repacked(int M, int N, int K, int group, int experts, const w4
     if ((c.path != W4A16_PATH_AUTO && c.path != W4A16_PATH_DECODE) ||
         (c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_STREAM))
         return fail(W4A16_ERR_UNSUPPORTED, "repacked weights: decode path, stream variant only");
+    if (c.dtype != W4A16_DTYPE_F16)
+        return fail(W4A16_ERR_UNSUPPORTED, "repacked weights: fp16 only");
     c.path = W4A16_PATH_DECODE;
     c.variant = W4A16_DECODE_STREAM;
     const int m = M < 16 ? M : 16;

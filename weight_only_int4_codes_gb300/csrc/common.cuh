@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -66,6 +67,12 @@ cudaError_t launch_quantize_pack(const uint16_t *W, int K, int N, int group, boo
 cudaError_t launch_dequantize(const uint32_t *packed, const uint16_t *scales,
                               const uint16_t *zeros, uint16_t *W_out, int K, int N,
                               int group, cudaStream_t stream);
+cudaError_t launch_quantize_pack_bf16(const uint16_t *W, int K, int N, int group,
+                                      uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                      cudaStream_t stream);
+cudaError_t launch_dequantize_bf16(const uint32_t *packed, const uint16_t *scales,
+                                   const uint16_t *zeros, uint16_t *W_out, int K, int N,
+                                   int group, cudaStream_t stream);
 // The pre-permuted (repacked) weight layout: support check, size, and the
 // natural -> repacked transform (quant.cu).
 bool repack_supported(int K, int N, int group);
@@ -148,6 +155,25 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// The same three operations on bfloat16 pairs (round to nearest even).
+__device__ __forceinline__ uint32_t bsub2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t badd2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 

@@ -116,11 +116,14 @@ __device__ __forceinline__ void load_batch(Batch<U> &b, bool col_ok, const uint3
 
 // The MMA work of one batch (see decode_math.cuh for the fragment mapping):
 // thread (g, t) handles, in step u, packed row  row = krow_first + 4u + t.
-template <int NT, int U>
-__device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batch<U> &b,
-                                              const uint16_t *xrow0, const uint16_t *xrow1,
-                                              bool m0_ok, bool m1_ok, int krow_first,
-                                              int t) {
+// fp16: the batch's MMAs accumulate q - z, and the group scale is applied to
+// their sum (acc).  bfloat16 (BF): every weight is dequantized with its scale
+// first, and the MMAs accumulate into the running sums accb.
+template <int NT, int U, bool BF>
+__device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], float (&accb)[NT][2][2][4],
+                                              const Batch<U> &b, const uint16_t *xrow0,
+                                              const uint16_t *xrow1, bool m0_ok, bool m1_ok,
+                                              int krow_first, int t) {
     // x fragments of all U steps first (several loads in flight)
     uint4 xr[NT][U];
 #pragma unroll
@@ -129,22 +132,33 @@ __device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], const Batc
         xr[0][u] = m0_ok ? ld_nc_v4(xrow0 + koff) : make_uint4(0, 0, 0, 0);
         if (NT > 1) xr[NT - 1][u] = m1_ok ? ld_nc_v4(xrow1 + koff) : make_uint4(0, 0, 0, 0);
     }
-    const GroupConsts k = make_group_consts(b.z, b.s);
-    float gacc[NT][2][2][4];
+    if constexpr (BF) {
+        const GroupConstsBf k = make_group_consts_bf(b.z, b.s);
 #pragma unroll
-    for (int p = 0; p < NT; ++p)
+        for (int u = 0; u < U; ++u) {
+            uint32_t bx[NT][4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+            for (int p = 0; p < NT; ++p) x_fragments(xr[p][u], bx[p]);
+            step_mma_bf16<NT>(accb, b.w[u], k, bx);
+        }
+    } else {
+        const GroupConsts k = make_group_consts(b.z, b.s);
+        float gacc[NT][2][2][4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) gacc[p][j][0][r] = gacc[p][j][1][r] = 0.f;
+        for (int p = 0; p < NT; ++p)
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        uint32_t bx[NT][4];
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int p = 0; p < NT; ++p) x_fragments(xr[p][u], bx[p]);
-        step_mma_split<NT>(gacc, b.w[u], k, bx);
+                for (int r = 0; r < 4; ++r) gacc[p][j][0][r] = gacc[p][j][1][r] = 0.f;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint32_t bx[NT][4];
+#pragma unroll
+            for (int p = 0; p < NT; ++p) x_fragments(xr[p][u], bx[p]);
+            step_mma_split<NT>(gacc, b.w[u], k, bx);
+        }
+        flush_group_split<NT>(acc, gacc, k);
     }
-    flush_group_split<NT>(acc, gacc, k);
 }
 
 // The operands of one GEMM of a launch (one expert of a grouped launch).
@@ -163,9 +177,9 @@ struct ExpertTable {
 };
 
 // One CTA's share of one GEMM: column tile blockIdx.x, K slice blockIdx.y,
-// 16-row chunk `mchunk` of x.
+// 16-row chunk `mchunk` of x.  BF: x, scales, zeros and out are bfloat16.
 // Block: 32*WN*WK threads; dynamic shared memory (WK + 1) * 16 * 32*WN floats.
-template <int NT, int WN, int WK, int U>
+template <int NT, int WN, int WK, int U, bool BF>
 __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands &o, int mchunk)
 {
     extern __shared__ float smem[];
@@ -192,12 +206,13 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
     const int rows_per_group = a.group >> 3;
 
     float acc[NT][2][4];
+    float accb[NT][2][2][4];   // bfloat16 only (two k halves)
 #pragma unroll
     for (int p = 0; p < NT; ++p)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[p][j][r] = 0.f;
+            for (int r = 0; r < 4; ++r) acc[p][j][r] = accb[p][j][0][r] = accb[p][j][1][r] = 0.f;
 
     const int m0 = g, m1 = 8 + g;
     const bool m0_ok = m0 < Mc, m1_ok = m1 < Mc;
@@ -221,7 +236,7 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
             load_batch<U>(bb, col_ok, wptr + (size_t)(bi + 1) * U * wstride, wstride,
                           sptr + grow, zptr + grow, pol);
         }
-        compute_batch<NT, U>(acc, ba, xrow0, xrow1, m0_ok, m1_ok, row0 + 4 * U * bi, t);
+        compute_batch<NT, U, BF>(acc, accb, ba, xrow0, xrow1, m0_ok, m1_ok, row0 + 4 * U * bi, t);
         if (bi + 1 < nbatch) {
             if (bi + 2 < nbatch) {
                 const int r = row0 + 4 * U * (bi + 2);
@@ -229,9 +244,17 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
                 load_batch<U>(ba, col_ok, wptr + (size_t)(bi + 2) * U * wstride, wstride,
                               sptr + grow, zptr + grow, pol);
             }
-            compute_batch<NT, U>(acc, bb, xrow0, xrow1, m0_ok, m1_ok,
-                                 row0 + 4 * U * (bi + 1), t);
+            compute_batch<NT, U, BF>(acc, accb, bb, xrow0, xrow1, m0_ok, m1_ok,
+                                     row0 + 4 * U * (bi + 1), t);
         }
+    }
+    if constexpr (BF) {
+#pragma unroll
+        for (int p = 0; p < NT; ++p)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[p][j][r] = accb[p][j][0][r] + accb[p][j][1][r];
     }
 
     // ---- reduction 1: the WK warps of this CTA, through shared memory
@@ -257,7 +280,7 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
         if (a.split == 1) {
             const int col = blockIdx.x * BN + c;
             if (col < a.N)
-                o.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
+                o.out[(size_t)(m_base + m) * a.N + col] = to_out<BF>(v);
         } else {
             part[e] = v;
         }
@@ -277,18 +300,18 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
         const int m = e / BN, c = e - m * BN;
         const int col = blockIdx.x * BN + c;
         if (col < a.N)
-            o.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
+            o.out[(size_t)(m_base + m) * a.N + col] = to_out<BF>(v);
     }
     cluster.sync();   // keep this CTA's shared memory alive until all peers have read it
 }
 
 // Grid: (ceil(N / (32*WN)), split, ceil(M / 16)); cluster (1, split, 1).
-template <int NT, int WN, int WK, int U>
+template <int NT, int WN, int WK, int U, bool BF>
 __global__ void __launch_bounds__(32 * WN * WK)
 decode_kernel(const DecodeArgs a)
 {
     const Operands o{a.x, a.packed, a.scales, a.zeros, a.out};
-    decode_tile<NT, WN, WK, U>(a, o, blockIdx.z);
+    decode_tile<NT, WN, WK, U, BF>(a, o, blockIdx.z);
 }
 
 // Grouped launch of E GEMMs of one shape (MoE experts): grid z = E * ceil(M / 16),
@@ -299,10 +322,10 @@ decode_grouped_kernel(const DecodeArgs a, const ExpertTable tab)
 {
     const int mchunks = (a.M + 15) >> 4;
     const int e = blockIdx.z / mchunks;
-    decode_tile<NT, WN, WK, U>(a, tab.e[e], blockIdx.z - e * mchunks);
+    decode_tile<NT, WN, WK, U, false>(a, tab.e[e], blockIdx.z - e * mchunks);
 }
 
-template <int NT, int WN, int WK, int U>
+template <int NT, int WN, int WK, int U, bool BF>
 cudaError_t launch_one(const DecodeArgs &da, int strips, int mchunks, bool pdl,
                        cudaStream_t stream) {
     constexpr int BN = 32 * WN;
@@ -327,7 +350,7 @@ cudaError_t launch_one(const DecodeArgs &da, int strips, int mchunks, bool pdl,
     }
     lc.attrs = attrs;
     lc.numAttrs = na;
-    return cudaLaunchKernelEx(&lc, decode_kernel<NT, WN, WK, U>, da);
+    return cudaLaunchKernelEx(&lc, decode_kernel<NT, WN, WK, U, BF>, da);
 }
 
 template <int NT, int WN, int WK, int U>
@@ -369,14 +392,14 @@ cudaError_t launch_grouped_shape(const DecodeArgs &da, const ExpertTable &tab, i
     return cudaErrorNotSupported;
 }
 
-template <int NT, int U>
+template <int NT, int U, bool BF>
 cudaError_t launch_shape(const DecodeArgs &da, int wn, int wk, int strips, int mchunks,
                          bool pdl, cudaStream_t s) {
-    if (wn == 1 && wk == 4) return launch_one<NT, 1, 4, U>(da, strips, mchunks, pdl, s);
-    if (wn == 1 && wk == 8) return launch_one<NT, 1, 8, U>(da, strips, mchunks, pdl, s);
-    if (wn == 2 && wk == 4) return launch_one<NT, 2, 4, U>(da, strips, mchunks, pdl, s);
-    if (wn == 4 && wk == 2) return launch_one<NT, 4, 2, U>(da, strips, mchunks, pdl, s);
-    if (wn == 2 && wk == 2) return launch_one<NT, 2, 2, U>(da, strips, mchunks, pdl, s);
+    if (wn == 1 && wk == 4) return launch_one<NT, 1, 4, U, BF>(da, strips, mchunks, pdl, s);
+    if (wn == 1 && wk == 8) return launch_one<NT, 1, 8, U, BF>(da, strips, mchunks, pdl, s);
+    if (wn == 2 && wk == 4) return launch_one<NT, 2, 4, U, BF>(da, strips, mchunks, pdl, s);
+    if (wn == 4 && wk == 2) return launch_one<NT, 4, 2, U, BF>(da, strips, mchunks, pdl, s);
+    if (wn == 2 && wk == 2) return launch_one<NT, 2, 2, U, BF>(da, strips, mchunks, pdl, s);
     return cudaErrorNotSupported;
 }
 
@@ -390,11 +413,11 @@ int steps_per_batch(int group) {
 namespace {
 template <int NT, int U>
 const void *kernel_for(int wn, int wk) {
-    if (wn == 1 && wk == 4) return (const void *)decode_kernel<NT, 1, 4, U>;
-    if (wn == 1 && wk == 8) return (const void *)decode_kernel<NT, 1, 8, U>;
-    if (wn == 2 && wk == 4) return (const void *)decode_kernel<NT, 2, 4, U>;
-    if (wn == 4 && wk == 2) return (const void *)decode_kernel<NT, 4, 2, U>;
-    if (wn == 2 && wk == 2) return (const void *)decode_kernel<NT, 2, 2, U>;
+    if (wn == 1 && wk == 4) return (const void *)decode_kernel<NT, 1, 4, U, false>;
+    if (wn == 1 && wk == 8) return (const void *)decode_kernel<NT, 1, 8, U, false>;
+    if (wn == 2 && wk == 4) return (const void *)decode_kernel<NT, 2, 4, U, false>;
+    if (wn == 4 && wk == 2) return (const void *)decode_kernel<NT, 4, 2, U, false>;
+    if (wn == 2 && wk == 2) return (const void *)decode_kernel<NT, 2, 2, U, false>;
     return nullptr;
 }
 }  // namespace
@@ -440,6 +463,7 @@ bool decode_config_supported(const w4a16_config &cfg, int /*M*/) {
 
 cudaError_t launch_decode(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
     if (!decode_config_supported(cfg, a.M)) return cudaErrorNotSupported;
+    const bool bf = cfg.dtype == W4A16_DTYPE_BF16;
     const int U = steps_per_batch(a.group);
     if (cfg.steps % U != 0) return cudaErrorNotSupported;
     DecodeArgs da;
@@ -463,17 +487,15 @@ cudaError_t launch_decode(const GemmArgs &a, const w4a16_config &cfg, cudaStream
     if (mchunks > 65535) return cudaErrorInvalidValue;
     const bool pdl = (cfg.flags & W4A16_FLAG_PDL) != 0;
     const bool nt2 = a.M > 8;
+#define W4A16_DECODE(NT_, U_)                                                                   \
+    (bf ? launch_shape<NT_, U_, true>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream) \
+        : launch_shape<NT_, U_, false>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream))
     switch (U) {
-    case 4:
-        return nt2 ? launch_shape<2, 4>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream)
-                   : launch_shape<1, 4>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream);
-    case 2:
-        return nt2 ? launch_shape<2, 2>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream)
-                   : launch_shape<1, 2>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream);
-    default:
-        return nt2 ? launch_shape<2, 1>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream)
-                   : launch_shape<1, 1>(da, cfg.warps_n, cfg.warps_k, strips, mchunks, pdl, stream);
+    case 4: return nt2 ? W4A16_DECODE(2, 4) : W4A16_DECODE(1, 4);
+    case 2: return nt2 ? W4A16_DECODE(2, 2) : W4A16_DECODE(1, 2);
+    default: return nt2 ? W4A16_DECODE(2, 1) : W4A16_DECODE(1, 1);
     }
+#undef W4A16_DECODE
 }
 
 cudaError_t launch_decode_grouped(const GroupedGemmArgs &a, const w4a16_config &cfg,

@@ -122,4 +122,85 @@ __device__ __forceinline__ void flush_group_split(float (&acc)[NT][2][4],
             }
 }
 
+// ---------------------------------------------------------------- bfloat16
+// bfloat16 has 7 fraction bits, so only the low nibble of a half fits under
+// the magic exponent: 128.0 (0x4300) has its mantissa ulp at bit 0, and
+// 0x4300 | q is 128 + q exactly.  The other nibbles are shifted down first
+// (w >> 4, w >> 8, w >> 12 bring nibbles (1,5), (2,6), (3,7) to bits 0..3 and
+// 16..19), which keeps the fragment mapping above.  Each weight is then
+// ((128 + q) - (128 + z)) * s: the difference is exact, the product is one
+// bfloat16 rounding of (q - z) * s -- the dequantized bfloat16 weight bit for
+// bit, which the MMA multiplies by x exactly (products of two bfloat16 values
+// fit fp32) and accumulates in fp32.
+constexpr uint32_t kMagicBf = 0x43004300u;   // 128.0 | 128.0 (bfloat16)
+
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Per-group constants of the thread's four columns: (128 + z) and the scale,
+// each broadcast into both halves of a bfloat16 pair.
+struct GroupConstsBf {
+    uint32_t zA[4], s2[4];
+};
+
+__device__ __forceinline__ GroupConstsBf make_group_consts_bf(uint2 zraw, uint2 sraw) {
+    GroupConstsBf k;
+    const uint32_t z01 = badd2_u32(zraw.x, kMagicBf);   // (128+z0, 128+z1), exact
+    const uint32_t z23 = badd2_u32(zraw.y, kMagicBf);
+    k.zA[0] = __byte_perm(z01, 0, 0x1010);
+    k.zA[1] = __byte_perm(z01, 0, 0x3232);
+    k.zA[2] = __byte_perm(z23, 0, 0x1010);
+    k.zA[3] = __byte_perm(z23, 0, 0x3232);
+    k.s2[0] = __byte_perm(sraw.x, 0, 0x1010);
+    k.s2[1] = __byte_perm(sraw.x, 0, 0x3232);
+    k.s2[2] = __byte_perm(sraw.y, 0, 0x1010);
+    k.s2[3] = __byte_perm(sraw.y, 0, 0x3232);
+    return k;
+}
+
+// Two dequantized bfloat16 weights from bits 0..3 and 16..19 of v.
+__device__ __forceinline__ uint32_t dq_bf16(uint32_t v, uint32_t zA, uint32_t s2) {
+    return bmul2_u32(bsub2_u32(lop3_and_or(v, kMaskLo, kMagicBf), zA), s2);
+}
+
+// One 32-k step of one thread, bfloat16: as step_mma_split, with the scale
+// already inside each weight, so the MMAs accumulate straight into the
+// running sums acc[p][j][kk].
+template <int NT>
+__device__ __forceinline__ void step_mma_bf16(float (&acc)[NT][2][2][4], uint4 w,
+                                              const GroupConstsBf &k,
+                                              const uint32_t (&bx)[NT][4]) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t c0 = wv[2 * j], c1 = wv[2 * j + 1];
+        const uint32_t z0 = k.zA[2 * j], z1 = k.zA[2 * j + 1];
+        const uint32_t s0 = k.s2[2 * j], s1 = k.s2[2 * j + 1];
+        const uint32_t a0 = dq_bf16(c0, z0, s0), a1 = dq_bf16(c1, z1, s1);
+        const uint32_t a2 = dq_bf16(c0 >> 4, z0, s0), a3 = dq_bf16(c1 >> 4, z1, s1);
+        const uint32_t e0 = dq_bf16(c0 >> 8, z0, s0), e1 = dq_bf16(c1 >> 8, z1, s1);
+        const uint32_t e2 = dq_bf16(c0 >> 12, z0, s0), e3 = dq_bf16(c1 >> 12, z1, s1);
+#pragma unroll
+        for (int p = 0; p < NT; ++p) {
+            mma_16816_bf16(acc[p][j][0], a0, a1, a2, a3, bx[p][0], bx[p][1]);
+            mma_16816_bf16(acc[p][j][1], e0, e1, e2, e3, bx[p][2], bx[p][3]);
+        }
+    }
+}
+
+// fp32 -> the output element (fp16 or bfloat16, round to nearest even).
+template <bool BF>
+__device__ __forceinline__ uint16_t to_out(float v) {
+    if constexpr (BF)
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    else
+        return __half_as_ushort(__float2half_rn(v));
+}
+
 }  // namespace w4a16

@@ -2,7 +2,8 @@
 // (tcgen05.mma, accumulator in tensor memory).
 //
 // What it computes: out[m,n] = sum_k x[m,k] * Wdq[k,n], Wdq = fp16((q - z) * s),
-// fp32 accumulation, fp16 output (page "Beating FP16 with 4-bit Weights",
+// fp32 accumulation, fp16 output -- or, with bfloat16 data, Wdq = bf16((q - z)
+// * s), bf16 x bf16 MMAs and a bfloat16 output (page "Beating FP16 with 4-bit Weights",
 // section "The design": the packed tile is loaded, unpacked in registers,
 // dequantized and fed to a tensor-core dot product with fp32 accumulation;
 // section "Results": once M grows into prefill the unpack must hide under the
@@ -76,7 +77,8 @@ struct PrefillArgs {
 // stage then carries only x, the packed words and the scale/zero rows.
 // SPLIT: split-K across a cluster along z (a separate instantiation, so that
 // the kernel without it carries none of its code).
-template <int NDQ, bool ATMEM, bool SPLIT>
+// BF: x, scales, zeros and out are bfloat16 (MMA operands bf16 x bf16).
+template <int NDQ, bool ATMEM, bool SPLIT, bool BF>
 __global__ void __launch_bounds__(32 * (NDQ + 2), 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
@@ -165,7 +167,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         // ------------------------------------------------------ MMA issuer
         // Warp-wide loop, lane 0 issues the MMAs and the commits (a commit
         // tracks the MMAs of the thread that issues it).
-        const uint32_t idesc = idesc_f16(128, a.tile_m);
+        const uint32_t idesc = idesc_f16(128, a.tile_m, BF);
         const uint32_t tmem_u = __shfl_sync(0xffffffffu, tmem_d, 0);
         const uint32_t b_chunk16 = (uint32_t)a.b_chunk_bytes >> 4;
         const uint32_t ring_u = smem_u32(ring);
@@ -223,7 +225,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             for (int b0 = 0; b0 < kRowsPer; b0 += kBlk) {
                 const int c0 = part * kRowsPer + b0;              // first packed row of the block
                 uint32_t h[kBlk * 4];
-                dequant_words<kBlk>(st, a.p_off, a.s_off, a.z_off, c0, stage_zrow(k0, a.group, c0),
+                dequant_words<kBlk, BF>(st, a.p_off, a.s_off, a.z_off, c0, stage_zrow(k0, a.group, c0),
                                     n, h);
                 if (ATMEM) {
                     // A stage s: lane n, 32-bit columns a_col0 + 64 s + 4 c .. +3 (k = 8c .. 8c+7)
@@ -286,10 +288,10 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             // by one TMA copy (rows past M and columns past N are clipped by
             // the tensor map)
             if constexpr (SPLIT)
-                stage_accumulator(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart,
-                                  32 * kParts, smem_u32(ring + a.red_off), a.split - 1);
+                stage_accumulator<BF>(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart,
+                                      32 * kParts, smem_u32(ring + a.red_off), a.split - 1);
             else
-                stage_accumulator(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart,
+                stage_accumulator<BF>(taddr, smem_u32(ring), q * 32 + lane, a.tile_m, 32 * epart,
                                   32 * kParts);
             fence_proxy_async_smem();
             named_bar_sync(1, NDQ * 32);
@@ -393,11 +395,19 @@ __device__ __forceinline__ void store_pairs(const uint32_t (&hc)[16], int r0, in
     }
 }
 
+template <bool BF>
 __device__ __forceinline__ void pack_chunk(const uint32_t (&v)[32], uint32_t (&hc)[16]) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const __half2 p = __floats2half2_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-        hc[j] = *reinterpret_cast<const uint32_t *>(&p);
+        if constexpr (BF) {
+            const __nv_bfloat162 p =
+                __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            hc[j] = *reinterpret_cast<const uint32_t *>(&p);
+        } else {
+            const __half2 p =
+                __floats2half2_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            hc[j] = *reinterpret_cast<const uint32_t *>(&p);
+        }
     }
 }
 
@@ -406,7 +416,7 @@ __device__ __forceinline__ void pack_chunk(const uint32_t (&v)[32], uint32_t (&h
 // warps the thread's share (at most 64 pairs) is held in registers and the
 // accumulator is freed before any store; with 4 warps it is written chunk by
 // chunk and freed after.
-template <int NDQ>
+template <int NDQ, bool BF>
 __device__ __forceinline__ void split_epilogue(uint32_t lane_base, int lane, int n, int part,
                                                int m0, int n0, uint64_t *accum_full,
                                                uint64_t *accum_empty, uint32_t parity,
@@ -428,7 +438,7 @@ __device__ __forceinline__ void split_epilogue(uint32_t lane_base, int lane, int
             uint32_t v[32];
             tmem_ld_32x32b_x32(lane_base + (uint32_t)(first + c * kStep), v);
             tmem_ld_wait();
-            pack_chunk(v, h[c]);
+            pack_chunk<BF>(v, h[c]);
         }
         tc_fence_before();
         __syncwarp();
@@ -441,7 +451,7 @@ __device__ __forceinline__ void split_epilogue(uint32_t lane_base, int lane, int
             uint32_t v[32], hc[16];
             tmem_ld_32x32b_x32(lane_base + (uint32_t)(first + c * kStep), v);
             tmem_ld_wait();
-            pack_chunk(v, hc);
+            pack_chunk<BF>(v, hc);
             store_pairs(hc, first + c * kStep, lane, col, col_ok, m0, a.tile_m, a.M, a.N, a.out);
         }
         tc_fence_before();
@@ -450,7 +460,7 @@ __device__ __forceinline__ void split_epilogue(uint32_t lane_base, int lane, int
     }
 }
 
-template <int NDQ>
+template <int NDQ, bool BF>
 __global__ void __launch_bounds__(32 * (NDQ + 3), 1)
 prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
@@ -545,7 +555,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (lane 0 issues)
-        const uint32_t idesc = idesc_f16(128, a.tile_m);
+        const uint32_t idesc = idesc_f16(128, a.tile_m, BF);
         const uint32_t tmem_u = __shfl_sync(0xffffffffu, tmem_d, 0);
         const uint32_t ring_u = smem_u32(ring);
         const uint32_t chunk16 = (uint32_t)a.x_chunk_bytes >> 4;
@@ -607,7 +617,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
             for (int b0 = 0; b0 < kRowsPer; b0 += kBlk) {
                 const int c0 = part * kRowsPer + b0;
                 uint32_t h[kBlk * 4];
-                dequant_words<kBlk>(st, 0, a.s_off, a.z_off, c0, stage_zrow(k0, a.group, c0), n, h);
+                dequant_words<kBlk, BF>(st, 0, a.s_off, a.z_off, c0, stage_zrow(k0, a.group, c0), n, h);
                 tmem_st_32x32b<kBlk * 4>(
                     lane_base + (uint32_t)(a.a_col0 + s * (kStageK / 2) + c0 * 4), h);
             }
@@ -625,14 +635,14 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
             int kt = 0;
             if (it > 0) {
                 for (; kt < ep_at; ++kt) stage(kt);
-                split_epilogue<NDQ>(lane_base, lane, n, part, pm0, pn0, accum_full, accum_empty,
+                split_epilogue<NDQ, BF>(lane_base, lane, n, part, pm0, pn0, accum_full, accum_empty,
                                     (uint32_t)((it - 1) & 1), a);
             }
             for (; kt < KT; ++kt) stage(kt);
             split_tile(a, t, pm0, pn0);
         }
         if (it > 0)
-            split_epilogue<NDQ>(lane_base, lane, n, part, pm0, pn0, accum_full, accum_empty,
+            split_epilogue<NDQ, BF>(lane_base, lane, n, part, pm0, pn0, accum_full, accum_empty,
                                 (uint32_t)((it - 1) & 1), a);
     }
     tc_fence_before();
@@ -642,16 +652,16 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
-template <int NDQ, bool ATMEM>
+template <int NDQ, bool ATMEM, bool BF>
 cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                   const CUtensorMap &tx, const CUtensorMap &tw,
                                   const CUtensorMap &ts, const CUtensorMap &tz,
                                   const CUtensorMap &to, const PrefillArgs &pa) {
     if (pa.split <= 1) {
         const cudaError_t attr = ensure_dynamic_smem(
-            (const void *)prefill_tcgen05_kernel<NDQ, ATMEM, false>, 227 * 1024);
+            (const void *)prefill_tcgen05_kernel<NDQ, ATMEM, false, BF>, 227 * 1024);
         if (attr != cudaSuccess) return attr;
-        prefill_tcgen05_kernel<NDQ, ATMEM, false><<<grid, 32 * (NDQ + 2), smem, stream>>>(
+        prefill_tcgen05_kernel<NDQ, ATMEM, false, BF><<<grid, 32 * (NDQ + 2), smem, stream>>>(
             tx, tw, ts, tz, to, pa);
         return cudaGetLastError();
     }
@@ -659,7 +669,7 @@ cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
         return cudaErrorNotSupported;     // split-K is built for A in tensor memory only
     } else {
     const cudaError_t attr =
-        ensure_dynamic_smem((const void *)prefill_tcgen05_kernel<NDQ, ATMEM, true>, 227 * 1024);
+        ensure_dynamic_smem((const void *)prefill_tcgen05_kernel<NDQ, ATMEM, true, BF>, 227 * 1024);
     if (attr != cudaSuccess) return attr;
     // split-K: the CTAs of one output tile form a cluster along z
     cudaLaunchConfig_t lc = {};
@@ -674,18 +684,18 @@ cudaError_t launch_prefill_kernel(dim3 grid, size_t smem, cudaStream_t stream,
     attr1[0].val.clusterDim.z = (unsigned)pa.split;
     lc.attrs = attr1;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, prefill_tcgen05_kernel<NDQ, ATMEM, true>, tx, tw, ts, tz, to, pa);
+    return cudaLaunchKernelEx(&lc, prefill_tcgen05_kernel<NDQ, ATMEM, true, BF>, tx, tw, ts, tz, to, pa);
     }
 }
 
-template <int NDQ>
+template <int NDQ, bool BF>
 cudaError_t launch_split_kernel(dim3 grid, size_t smem, cudaStream_t stream,
                                 const CUtensorMap &tx, const CUtensorMap &tw,
                                 const CUtensorMap &ts, const CUtensorMap &tz, const SplitArgs &sa) {
     const cudaError_t attr =
-        ensure_dynamic_smem((const void *)prefill_split_kernel<NDQ>, 227 * 1024);
+        ensure_dynamic_smem((const void *)prefill_split_kernel<NDQ, BF>, 227 * 1024);
     if (attr != cudaSuccess) return attr;
-    prefill_split_kernel<NDQ><<<grid, 32 * (NDQ + 3), smem, stream>>>(tx, tw, ts, tz, sa);
+    prefill_split_kernel<NDQ, BF><<<grid, 32 * (NDQ + 3), smem, stream>>>(tx, tw, ts, tz, sa);
     return cudaGetLastError();
 }
 
@@ -761,6 +771,8 @@ bool ring_layout(const w4a16_config &cfg, int K, int group, PrefillArgs &pa) {
 bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int group) {
     if (cfg.split_k < 0 || cfg.split_k > kMaxPrefillSplit) return false;
     if (cfg.split_k > 1 && cfg.variant == W4A16_PREFILL_A_SMEM) return false;
+    if (cfg.dtype != W4A16_DTYPE_F16 && cfg.dtype != W4A16_DTYPE_BF16) return false;
+    if (cfg.dtype == W4A16_DTYPE_BF16 && cfg.variant == W4A16_PREFILL_A_SMEM) return false;
     if (cfg.variant != 0 && cfg.variant != W4A16_PREFILL_A_TMEM &&
         cfg.variant != W4A16_PREFILL_A_SMEM)
         return false;
@@ -822,15 +834,16 @@ cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cud
     const uint64_t x_dims[3] = {(uint64_t)kChunkK, (uint64_t)a.M, (uint64_t)(a.K / kChunkK)};
     const uint64_t x_strides[2] = {(uint64_t)a.K * 2, (uint64_t)kChunkK * 2};
     const uint32_t x_box[3] = {(uint32_t)kChunkK, (uint32_t)sa.tile_m, (uint32_t)kChunks};
+    const bool bf = cfg.dtype == W4A16_DTYPE_BF16;
+    const CUtensorMapDataType et = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tx, tw, ts, tz;
-    if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, x_dims, x_strides, x_box,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_tmap(&tx, et, 3, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, a.K / 8,
                       (uint64_t)a.N * 4, kTileN, kPackedRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
-                      (uint64_t)a.N * 2, kTileN, sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.zeros, a.N, a.K / a.group,
-                      (uint64_t)a.N * 2, kTileN, sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_tmap_2d(&ts, et, a.scales, a.N, a.K / a.group, (uint64_t)a.N * 2, kTileN,
+                      sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&tz, et, a.zeros, a.N, a.K / a.group, (uint64_t)a.N * 2, kTileN,
+                      sa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     // persistent: one CTA per SM (at most one per tile)
     sa.m_tiles = (a.M + sa.tile_m - 1) / sa.tile_m;
@@ -845,11 +858,15 @@ cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cud
     sa.tiles = (int)tiles;
     const int sms = device_info().sm_count;
     dim3 grid(sa.tiles < sms ? sa.tiles : sms, 1, 1);
+#define W4A16_SPLIT(NDQ_)                                                          \
+    (bf ? launch_split_kernel<NDQ_, true>(grid, smem, stream, tx, tw, ts, tz, sa) \
+        : launch_split_kernel<NDQ_, false>(grid, smem, stream, tx, tw, ts, tz, sa))
     switch (ndq) {
-    case 4: return launch_split_kernel<4>(grid, smem, stream, tx, tw, ts, tz, sa);
-    case 16: return launch_split_kernel<16>(grid, smem, stream, tx, tw, ts, tz, sa);
-    default: return launch_split_kernel<8>(grid, smem, stream, tx, tw, ts, tz, sa);
+    case 4: return W4A16_SPLIT(4);
+    case 16: return W4A16_SPLIT(16);
+    default: return W4A16_SPLIT(8);
     }
+#undef W4A16_SPLIT
 }
 
 cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
@@ -882,24 +899,35 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     const uint64_t x_dims[3] = {(uint64_t)kChunkK, (uint64_t)a.M, (uint64_t)(a.K / kChunkK)};
     const uint64_t x_strides[2] = {(uint64_t)a.K * 2, (uint64_t)kChunkK * 2};
     const uint32_t x_box[3] = {(uint32_t)kChunkK, (uint32_t)pa.tile_m, (uint32_t)kChunks};
+    const bool bf = cfg.dtype == W4A16_DTYPE_BF16;
+    if (bf && !atmem) return cudaErrorNotSupported;   // bfloat16: A in tensor memory only
+    const CUtensorMapDataType et = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tx, tw, ts, tz, to;
-    if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, x_dims, x_strides, x_box,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_2d(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.out, a.N, a.M, (uint64_t)a.N * 2,
-                      kTileN, pa.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!make_tmap(&tx, et, 3, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&to, et, a.out, a.N, a.M, (uint64_t)a.N * 2, kTileN, pa.tile_m,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.packed, a.N, a.K / 8,
                       (uint64_t)a.N * 4, kTileN, kPackedRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.scales, a.N, a.K / a.group,
-                      (uint64_t)a.N * 2, kTileN, pa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.zeros, a.N, a.K / a.group,
-                      (uint64_t)a.N * 2, kTileN, pa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_tmap_2d(&ts, et, a.scales, a.N, a.K / a.group, (uint64_t)a.N * 2, kTileN,
+                      pa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&tz, et, a.zeros, a.N, a.K / a.group, (uint64_t)a.N * 2, kTileN,
+                      pa.sz_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     const int mtiles = (a.M + pa.tile_m - 1) / pa.tile_m;
     if (mtiles > 65535) return cudaErrorInvalidValue;
     dim3 grid((a.N + kTileN - 1) / kTileN, mtiles, split);
 #define W4A16_PF(NDQ_, AT_) \
-    launch_prefill_kernel<NDQ_, AT_>(grid, smem, stream, tx, tw, ts, tz, to, pa)
+    launch_prefill_kernel<NDQ_, AT_, false>(grid, smem, stream, tx, tw, ts, tz, to, pa)
+#define W4A16_PF_BF(NDQ_) \
+    launch_prefill_kernel<NDQ_, true, true>(grid, smem, stream, tx, tw, ts, tz, to, pa)
+    if (bf) {
+        switch (ndq) {
+        case 4: return W4A16_PF_BF(4);
+        case 16: return W4A16_PF_BF(16);
+        default: return W4A16_PF_BF(8);
+        }
+    }
     if (atmem) {
         switch (ndq) {
         case 4: return W4A16_PF(4, true);
@@ -913,6 +941,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     default: return W4A16_PF(8, false);
     }
 #undef W4A16_PF
+#undef W4A16_PF_BF
 }
 
 }  // namespace w4a16

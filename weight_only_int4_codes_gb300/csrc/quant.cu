@@ -1,4 +1,5 @@
-// quant.cu -- group-wise int4 quantize + pack, and dequantize (test aid).
+// quant.cu -- group-wise int4 quantize + pack, and dequantize (test aid), for
+// fp16 and bfloat16 weights.
 //
 // Quantizer (page "Beating FP16 with 4-bit Weights: A Portable W4A16 GEMM in
 // Triton", section "The design": one scale and one zero-point per group of 128
@@ -95,6 +96,87 @@ dequantize_kernel(const uint32_t *__restrict__ packed, const __half *__restrict_
     }
 }
 
+// ---------------------------------------------------------------- bfloat16
+// double -> bfloat16, round to nearest even, in one rounding: first to float
+// with round-to-odd (round toward zero, then set the last bit if anything was
+// cut off), then float -> bfloat16 to nearest even.  An intermediate format
+// with at least two more bits than the target, rounded to odd, makes the
+// second rounding equal the direct one (S. Boldo and G. Melquiond, "When
+// double rounding is odd", 2005); float has 16 more bits than bfloat16 at
+// every exponent, subnormals included.
+__device__ __forceinline__ __nv_bfloat16 f64_to_bf16_rn(double v) {
+    float f = __double2float_rz(v);
+    if ((double)f != v) f = __uint_as_float(__float_as_uint(f) | 1u);
+    return __float2bfloat16_rn(f);
+}
+
+// The asymmetric recipe of quantize_pack_kernel with bfloat16 weights, scales
+// and zeros: s = bf16((max - min) / 15) from the fp64 quotient, z and q from
+// fp64 quotients by the rounded s.
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_pack_bf16_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N, int group,
+                          uint32_t *__restrict__ packed, __nv_bfloat16 *__restrict__ scales,
+                          __nv_bfloat16 *__restrict__ zeros)
+{
+    const int n = blockIdx.x * kQuantThreads + threadIdx.x;
+    if (n >= N) return;
+    for (int j = blockIdx.y; j < K / group; j += gridDim.y) {
+        const size_t k0 = (size_t)j * group;
+        float mn = __int_as_float(0x7f800000);
+        float mx = -mn;
+        for (int k = 0; k < group; ++k) {
+            const float v = __bfloat162float(W[(k0 + k) * N + n]);   // exact
+            mn = fminf(mn, v);
+            mx = fmaxf(mx, v);
+        }
+        __nv_bfloat16 sb = f64_to_bf16_rn(((double)mx - (double)mn) / 15.0);
+        double s = (double)__bfloat162float(sb);
+        if (s == 0.0) {                                 // degenerate group
+            sb = __float2bfloat16_rn(1.0f);
+            s = 1.0;
+        }
+        double zr = rint(-(double)mn / s);
+        zr = fmin(fmax(zr, 0.0), 15.0);
+        const int z = (int)zr;
+        scales[(size_t)j * N + n] = sb;
+        zeros[(size_t)j * N + n] = __float2bfloat16_rn((float)z);   // exact
+        for (int r = 0; r < group / 8; ++r) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const double v = (double)__bfloat162float(W[(k0 + 8 * r + i) * N + n]);
+                double qd = rint(v / s) + (double)z;
+                qd = fmin(fmax(qd, 0.0), 15.0);
+                word |= (uint32_t)qd << (4 * i);
+            }
+            packed[(k0 / 8 + r) * N + n] = word;
+        }
+    }
+}
+
+// W_out[k,n] = bf16((q - z) * s): (q - z) * s is exact in fp32 (a 4-bit
+// integer times an 8-bit significand), so one float -> bfloat16 rounding is
+// the rounding of the exact product.
+__global__ void __launch_bounds__(kDequantThreads)
+dequantize_bf16_kernel(const uint32_t *__restrict__ packed, const __nv_bfloat16 *__restrict__ scales,
+                       const __nv_bfloat16 *__restrict__ zeros, __nv_bfloat16 *__restrict__ W_out,
+                       int K, int N, int group)
+{
+    const int n = blockIdx.x * kDequantThreads + threadIdx.x;
+    if (n >= N) return;
+    for (int r = blockIdx.y; r < K / 8; r += gridDim.y) {
+        const int j = (8 * r) / group;
+        const uint32_t word = packed[(size_t)r * N + n];
+        const float s = __bfloat162float(scales[(size_t)j * N + n]);
+        const float z = __bfloat162float(zeros[(size_t)j * N + n]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q = (float)((word >> (4 * i)) & 15u);
+            W_out[(size_t)(8 * r + i) * N + n] = __float2bfloat16_rn((q - z) * s);
+        }
+    }
+}
+
 // Repack (the pre-permuted layout; page "Beating FP16 with 4-bit Weights",
 // section "What's next": permute the packed weights offline into the order the
 // MMA consumes them).  One CTA per block (32-column strip sn, 256-row block
@@ -156,6 +238,29 @@ cudaError_t launch_dequantize(const uint32_t *packed, const uint16_t *scales,
         packed, reinterpret_cast<const __half *>(scales),
         reinterpret_cast<const __half *>(zeros), reinterpret_cast<__half *>(W_out), K, N,
         group);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_pack_bf16(const uint16_t *W, int K, int N, int group,
+                                      uint32_t *packed, uint16_t *scales, uint16_t *zeros,
+                                      cudaStream_t stream)
+{
+    dim3 grid((N + kQuantThreads - 1) / kQuantThreads, K / group < 65535 ? K / group : 65535);
+    quantize_pack_bf16_kernel<<<grid, kQuantThreads, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16 *>(W), K, N, group, packed,
+        reinterpret_cast<__nv_bfloat16 *>(scales), reinterpret_cast<__nv_bfloat16 *>(zeros));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize_bf16(const uint32_t *packed, const uint16_t *scales,
+                                   const uint16_t *zeros, uint16_t *W_out, int K, int N,
+                                   int group, cudaStream_t stream)
+{
+    dim3 grid((N + kDequantThreads - 1) / kDequantThreads, K / 8 < 65535 ? K / 8 : 65535);
+    dequantize_bf16_kernel<<<grid, kDequantThreads, 0, stream>>>(
+        packed, reinterpret_cast<const __nv_bfloat16 *>(scales),
+        reinterpret_cast<const __nv_bfloat16 *>(zeros), reinterpret_cast<__nv_bfloat16 *>(W_out),
+        K, N, group);
     return cudaGetLastError();
 }
 

@@ -115,10 +115,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 D, fp16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_f16(int umma_m, int umma_n) {
+// Instruction descriptor, kind::f16: fp32 D, A and B both fp16 (bf = false)
+// or both bfloat16 (bf = true) -- one kind::f16 MMA takes one operand type --
+// both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int umma_m, int umma_n, bool bf = false) {
     return (1u << 4)                                  // D format: f32
-           | (0u << 7) | (0u << 10)                   // A, B format: f16
+           | ((bf ? 1u : 0u) << 7)                    // A format: f16 (0) / bf16 (1)
+           | ((bf ? 1u : 0u) << 10)                   // B format: f16 (0) / bf16 (1)
            | ((uint32_t)(umma_n >> 3) << 17)          // N / 8
            | ((uint32_t)(umma_m >> 4) << 24);         // M / 16
 }

@@ -24,6 +24,8 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4:
 PATHS = {"auto": 0, "decode": 1, "prefill": 2}
 VARIANTS = {"auto": 0, "tma": 1, "registers": 2, "stream": 3,   # decode path
             "tmem": 1, "smem": 2}                  # prefill path: A's home
+DTYPES = {"f16": 0, "fp16": 0, "float16": 0, "bf16": 1, "bfloat16": 1}
+DTYPE_F16, DTYPE_BF16 = 0, 1
 QUANT_ASYMMETRIC, QUANT_SYMMETRIC = 0, 1
 FLAG_PDL = 0x1
 FLAG_TEST_TIMEOUT = 0x100
@@ -38,7 +40,8 @@ class W4A16Error(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("warps_k", ctypes.c_int),
                 ("warps_n", ctypes.c_int), ("steps", ctypes.c_int), ("tile_m", ctypes.c_int),
-                ("flags", ctypes.c_int), ("variant", ctypes.c_int), ("ctas", ctypes.c_int)]
+                ("flags", ctypes.c_int), ("variant", ctypes.c_int), ("ctas", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
 
     @classmethod
     def make(cls, cfg):
@@ -66,6 +69,8 @@ class Config(ctypes.Structure):
                 v = PATHS[v]
             if k == "variant" and isinstance(v, str):
                 v = VARIANTS[v]
+            if k == "dtype" and isinstance(v, str):
+                v = DTYPES[v]
             if k == "pdl":
                 c.flags |= FLAG_PDL if v else 0
                 continue
@@ -101,6 +106,8 @@ def load_library():
             "w4a16_quantize_pack": [P, I, I, I, P, P, P, P],
             "w4a16_quantize_pack_ex": [P, I, I, I, I, P, P, P, P],
             "w4a16_dequantize": [P, P, P, P, I, I, I, P],
+            "w4a16_quantize_pack_bf16": [P, I, I, I, P, P, P, P],
+            "w4a16_dequantize_bf16": [P, P, P, P, I, I, I, P],
             "w4a16_gemm": [P, P, P, P, P, I, I, I, I, P],
             "w4a16_gemm_ex": [P, P, P, P, P, I, I, I, I, ctypes.POINTER(Config), P],
             "w4a16_plan": [I, I, I, I, ctypes.POINTER(Config), ctypes.POINTER(Config)],
@@ -188,19 +195,55 @@ def dequantize(packed, scales, zeros, group: int = 128, stream=None) -> torch.Te
     return W
 
 
+def quantize_pack_bf16(W: torch.Tensor, group: int = 128, stream=None):
+    """bfloat16 W [K,N] -> (packed int32 [K/8,N], scales bf16 [K/g,N], zeros bf16 [K/g,N])."""
+    K, N = W.shape
+    packed = torch.empty((K // 8, N), dtype=torch.int32, device=W.device)
+    scales = torch.empty((K // group, N), dtype=torch.bfloat16, device=W.device)
+    zeros = torch.empty((K // group, N), dtype=torch.bfloat16, device=W.device)
+    _check(load_library().w4a16_quantize_pack_bf16(
+        _dev(W, "W", torch.bfloat16), K, N, group, _dev(packed, "packed", torch.int32),
+        _dev(scales, "scales", torch.bfloat16), _dev(zeros, "zeros", torch.bfloat16),
+        _stream_handle(stream)))
+    return packed, scales, zeros
+
+
+def dequantize_bf16(packed, scales, zeros, group: int = 128, stream=None) -> torch.Tensor:
+    """-> bfloat16 W [K,N] = bf16((q - z) * s)."""
+    K, N = packed.shape[0] * 8, packed.shape[1]
+    W = torch.empty((K, N), dtype=torch.bfloat16, device=packed.device)
+    _check(load_library().w4a16_dequantize_bf16(
+        _dev(packed, "packed", torch.int32), _dev(scales, "scales", torch.bfloat16),
+        _dev(zeros, "zeros", torch.bfloat16), _dev(W, "W_out", torch.bfloat16), K, N, group,
+        _stream_handle(stream)))
+    return W
+
+
+def _bf16_config(config):
+    """``config`` with dtype = bfloat16 (a new Config; the caller's is not changed)."""
+    c = Config()
+    base = Config.make(config)
+    if base is not None:
+        ctypes.memmove(ctypes.byref(c), ctypes.byref(base), ctypes.sizeof(Config))
+    c.dtype = DTYPE_BF16
+    return c
+
+
 def gemm_ex(x, packed, scales, zeros, group: int = 128, out=None, config=None, stream=None):
-    """out [M,N] fp16 = x [M,K] @ dequant(packed, scales, zeros); ``config`` is a
+    """out [M,N] = x [M,K] @ dequant(packed, scales, zeros); ``config`` is a
     dict of w4a16_config fields (path may be 'auto' | 'decode' | 'prefill',
-    pdl=True sets W4A16_FLAG_PDL)."""
+    pdl=True sets W4A16_FLAG_PDL).  x, scales, zeros and out are all fp16, or
+    all bfloat16 (then the call runs with dtype = W4A16_DTYPE_BF16)."""
     M, K = x.shape
     N = packed.shape[1]
+    et = torch.bfloat16 if x.dtype is torch.bfloat16 else torch.float16
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
-    cfg = Config.make(config)
+        out = torch.empty((M, N), dtype=et, device=x.device)
+    cfg = _bf16_config(config) if et is torch.bfloat16 else Config.make(config)
     _check(_lib_fast().w4a16_gemm_ex(
-        _dev(x, "x", torch.float16), _dev(packed, "packed", torch.int32),
-        _dev(scales, "scales", torch.float16), _dev(zeros, "zeros", torch.float16),
-        _dev(out, "out", torch.float16), M, N, K, group,
+        _dev(x, "x", et), _dev(packed, "packed", torch.int32),
+        _dev(scales, "scales", et), _dev(zeros, "zeros", et),
+        _dev(out, "out", et), M, N, K, group,
         ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
     return out
 
