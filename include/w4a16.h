@@ -224,6 +224,27 @@ W4A16_API w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed,
                            cudaStream_t stream);
 
 /*
+ * The arguments of one w4a16_gemm_ex call in one block, for callers that
+ * repeat the same call (a decode loop: same buffers, new contents): the
+ * caller fills the block once and passes its address each time, which keeps
+ * the per-call marshalling of a foreign-function binding to two arguments.
+ * The pages have no counterpart (they call a Triton kernel from Python).
+ * Same meaning, checks, errors and result as w4a16_gemm_ex; `cfg` may be
+ * NULL (automatic).  The block and the configuration it points to are read
+ * during the call only.
+ */
+typedef struct w4a16_gemm_args {
+    const uint16_t *x;
+    const uint32_t *packed;
+    const uint16_t *scales;
+    const uint16_t *zeros;
+    uint16_t *out;
+    int M, N, K, group;
+    const w4a16_config *cfg;
+} w4a16_gemm_args;
+W4A16_API w4a16_status w4a16_gemm_call(const w4a16_gemm_args *args, cudaStream_t stream);
+
+/*
  * Grouped GEMM: E independent products of one shape, out_e = x_e . W_e
  * (the experts of a mixture-of-experts layer, each with its own weights and
  * its own rows of x), in ONE kernel launch instead of E.  The pages measure

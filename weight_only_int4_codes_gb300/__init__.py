@@ -15,7 +15,7 @@ _NATIVE_NAMES = {
     "W4A16Error", "gemm", "gemm_ex", "gemm_grouped", "dequantize", "quantize_pack",
     "kernel_status", "library_path", "load_library", "plan", "native", "repack",
     "repacked_bytes", "gemm_repacked", "gemm_grouped_repacked", "gemm_noalloc",
-    "quantize_pack_bf16", "dequantize_bf16",
+    "quantize_pack_bf16", "dequantize_bf16", "prepare_gemm", "PreparedGemm",
 }
 
 

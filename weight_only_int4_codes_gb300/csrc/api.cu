@@ -1,10 +1,12 @@
 // api.cu -- the extern "C" boundary of libw4a16.so: argument validation,
 // launch planning (dispatch), error reporting.  Every compute step runs in the
 // kernels of quant.cu, decode.cu and prefill.cu.
+#include <atomic>
 #include <mutex>
 #include <set>
 #include <stdarg.h>
 #include <stdio.h>
+#include <string.h>
 #include <string>
 
 #include "common.cuh"
@@ -349,26 +351,115 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
     return W4A16_OK;
 }
 
+// Thread-private cache of resolved plans.  A decode loop repeats a handful of
+// (shape, request) pairs; planning (table lookup, the planners' searches,
+// occupancy queries) then runs once per pair instead of once per call.  Only
+// successful plans are kept; a plan depends on the device, the shape and the
+// request, which together form the key.
+struct PlanKey {
+    int dev, M, N, K, group, has_req;
+    w4a16_config req;
+};
+
+w4a16_status cached_plan(int M, int N, int K, int group, const w4a16_config *req,
+                         w4a16_config &c) {
+    PlanKey key;
+    memset(&key, 0, sizeof key);
+    if (cudaGetDevice(&key.dev) != cudaSuccess) {
+        cudaGetLastError();
+        key.dev = -1;
+    }
+    key.M = M;
+    key.N = N;
+    key.K = K;
+    key.group = group;
+    key.has_req = req != nullptr;
+    if (req) key.req = *req;
+    struct Entry {
+        PlanKey key;
+        w4a16_config plan;
+        bool valid;
+    };
+    constexpr int kEntries = 64;
+    static thread_local Entry cache[kEntries];
+    uint64_t h = 0xCBF29CE484222325ull;
+    const unsigned char *b = reinterpret_cast<const unsigned char *>(&key);
+    for (size_t i = 0; i < sizeof key; ++i) h = (h ^ b[i]) * 0x100000001B3ull;
+    Entry &e = cache[(h >> 29) & (kEntries - 1)];
+    if (e.valid && memcmp(&e.key, &key, sizeof key) == 0) {
+        c = e.plan;
+        return W4A16_OK;
+    }
+    const w4a16_status st = make_plan(M, N, K, group, req, c);
+    if (st == W4A16_OK) {
+        e.key = key;
+        e.plan = c;
+        e.valid = true;
+    }
+    return st;
+}
+
 }  // namespace
 
 cudaError_t ensure_dynamic_smem(const void *kernel, int bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    // thread-private record of the (device, kernel) pairs already set up
+    constexpr int kFront = 16;
+    static thread_local std::pair<int, const void *> front[kFront];
+    static thread_local int front_next = 0;
+    for (const auto &f : front)
+        if (f.second == kernel && f.first == dev) return cudaSuccess;
     static std::mutex mu;
     static std::set<std::pair<int, const void *>> done;
     std::lock_guard<std::mutex> lock(mu);
-    if (done.count({dev, kernel})) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.insert({dev, kernel});
-    return e;
+    if (!done.count({dev, kernel})) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        done.insert({dev, kernel});
+    }
+    front[front_next] = {dev, kernel};
+    front_next = (front_next + 1) % kFront;
+    return cudaSuccess;
 }
 
 const DeviceInfo &device_info() {
-    static DeviceInfo info;
+    constexpr int kMaxDev = 64;
+    static DeviceInfo infos[kMaxDev + 1];
+    static std::atomic<bool> ready[kMaxDev + 1];
+    static std::mutex mu;
+    static int ndev = -1;
     static std::once_flag once;
-    std::call_once(once, [] { info = query_device(); });
-    return info;
+    std::call_once(once, [] {
+        if (cudaGetDeviceCount(&ndev) != cudaSuccess) ndev = 0;
+        cudaGetLastError();
+    });
+    int dev = 0;
+    // no GPU (host-only planning) uses the last slot
+    if (ndev <= 0 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        cudaGetLastError();
+        dev = kMaxDev;
+    }
+    if (!ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!ready[dev].load(std::memory_order_relaxed)) {
+            infos[dev] = query_device();
+            ready[dev].store(true, std::memory_order_release);
+        }
+    }
+    return infos[dev];
+}
+
+int *device_status_word() {
+    static std::atomic<int *> ptrs[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    int *p = ptrs[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    if (kernel_status_address(&p) != cudaSuccess) return nullptr;
+    ptrs[dev].store(p, std::memory_order_release);
+    return p;
 }
 
 }  // namespace w4a16
@@ -471,7 +562,7 @@ w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed, const uint
         return fail(W4A16_ERR_MISALIGNED, "x, packed, scales, zeros and out must be 16-byte "
                     "aligned");
     w4a16_config c;
-    st = make_plan(M, N, K, group, cfg, c);
+    st = cached_plan(M, N, K, group, cfg, c);
     if (st != W4A16_OK) return st;
     GemmArgs a{x, packed, scales, zeros, out, M, N, K, group};
     cudaError_t e;
@@ -498,6 +589,12 @@ w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed, const uint
     if (e == cudaErrorNotSupported)
         return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "gemm launch");
+}
+
+w4a16_status w4a16_gemm_call(const w4a16_gemm_args *args, cudaStream_t stream) {
+    if (!args) return fail(W4A16_ERR_INVALID_ARG, "args is null");
+    return w4a16_gemm_ex(args->x, args->packed, args->scales, args->zeros, args->out, args->M,
+                         args->N, args->K, args->group, args->cfg, stream);
 }
 
 w4a16_status w4a16_gemm(const uint16_t *x, const uint32_t *packed, const uint16_t *scales,

@@ -130,7 +130,10 @@ struct DeviceInfo {
     int sm_count;
     int cc_major, cc_minor;
 };
-const DeviceInfo &device_info();   // host; falls back to GB300 numbers when no GPU
+const DeviceInfo &device_info();   // host, current device (queried once per device);
+                                   // falls back to GB300 numbers when no GPU
+int *device_status_word();         // the status word's device address on the
+                                   // current device (looked up once per device)
 
 // ------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t bits) {

@@ -781,19 +781,6 @@ bool scratch_for(cudaStream_t stream, float **partials, int **counters) {
     return true;
 }
 
-int *stream_status_word() {
-    static int *ptrs[64] = {};
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
-        int *p = nullptr;
-        if (kernel_status_address(&p) != cudaSuccess) return nullptr;
-        ptrs[dev] = p;
-    }
-    return ptrs[dev];
-}
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
@@ -975,7 +962,7 @@ NoAllocResult launch_decode_stream_noalloc(const StreamCall &call, int bns, bool
     sa.blk_bytes = L.blk_bytes;
     sa.red_off = L.red_off;
     sa.bar_off = L.bar_off;
-    sa.status = stream_status_word();
+    sa.status = device_status_word();
     if (!sa.status) return NoAllocResult{cudaErrorInvalidDevice, 0, 0};
     sa.timeout_ns = 1000000000ull;
     const bool og = group >= 32 * kSPW;
@@ -1049,7 +1036,7 @@ cudaError_t launch_decode_stream(const StreamCall &call, const w4a16_config &cfg
     sa.blk_bytes = L.blk_bytes;
     sa.red_off = L.red_off;
     sa.bar_off = L.bar_off;
-    sa.status = stream_status_word();
+    sa.status = device_status_word();
     if (!sa.status) return cudaErrorInvalidDevice;
     const bool test_timeout = (cfg.flags & W4A16_FLAG_TEST_TIMEOUT) != 0;
     sa.timeout_ns = test_timeout ? 5000000ull : 1000000000ull;

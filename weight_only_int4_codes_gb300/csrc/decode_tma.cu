@@ -390,19 +390,6 @@ cudaError_t launch_tma(const CUtensorMap &w, const CUtensorMap &s, const CUtenso
     return cudaLaunchKernelEx(&lc, decode_tma_kernel<NT, BNS, CW, OG>, w, s, z, x, da);
 }
 
-int *status_word() {
-    static int *ptrs[64] = {};
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
-        int *p = nullptr;
-        if (kernel_status_address(&p) != cudaSuccess) return nullptr;
-        ptrs[dev] = p;
-    }
-    return ptrs[dev];
-}
 
 }  // namespace
 
@@ -463,7 +450,7 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
         return cudaErrorInvalidValue;
     TmaDecodeArgs da;
     da.out = a.out;
-    da.status = status_word();
+    da.status = device_status_word();
     if (!da.status) return cudaErrorInvalidDevice;
     da.M = a.M;
     da.N = a.N;

@@ -699,10 +699,6 @@ cudaError_t launch_split_kernel(dim3 grid, size_t smem, cudaStream_t stream,
     return cudaGetLastError();
 }
 
-int *status_word() {
-    int *p = nullptr;
-    return kernel_status_address(&p) == cudaSuccess ? p : nullptr;
-}
 
 // Shared-memory and tensor-memory layout of the one-ring kernel for `cfg`
 // (tile_m, variant, split_k) and K; false when it does not fit.
@@ -792,7 +788,7 @@ bool prefill_config_supported(const w4a16_config &cfg, int M, int N, int K, int 
 // Default variant (A in tensor memory) for wide tiles: the split-ring kernel.
 cudaError_t launch_prefill_split(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
     SplitArgs sa;
-    sa.status = status_word();
+    sa.status = device_status_word();
     if (!sa.status) return cudaErrorInvalidDevice;
     sa.M = a.M;
     sa.N = a.N;
@@ -882,7 +878,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const w4a16_config &cfg, cudaStrea
     PrefillArgs pa;
     if (!ring_layout(cfg, a.K, a.group, pa)) return cudaErrorNotSupported;
     pa.out = a.out;
-    pa.status = status_word();
+    pa.status = device_status_word();
     if (!pa.status) return cudaErrorInvalidDevice;
     pa.M = a.M;
     pa.N = a.N;

@@ -4,7 +4,9 @@
 // so the library does not link libcuda directly.  Encoded maps are cached by
 // their full description (base address, shape, strides, box, swizzle): a
 // decode loop that calls the GEMM with the same weights and activation buffers
-// pays the encoding once.
+// pays the encoding once.  Lookups go first to a small direct-mapped cache
+// private to the calling thread (no lock, one hash and one key compare), then
+// to the process-wide map under its lock.
 #include <array>
 #include <map>
 #include <mutex>
@@ -50,6 +52,21 @@ bool make_tmap(CUtensorMap *out, CUtensorMapDataType dtype, int rank, const void
         key[5 + i] = box[i];
         if (i + 1 < rank) key[8 + i] = strides_bytes[i];
     }
+    // thread-private direct-mapped front cache
+    struct Front {
+        std::array<uint64_t, 13> key;
+        CUtensorMap map;
+        bool valid;
+    };
+    constexpr int kFront = 64;
+    static thread_local Front front[kFront];
+    uint64_t h = 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : key) h = (h ^ v) * 0x100000001B3ull;
+    Front &f = front[(h >> 32) & (kFront - 1)];
+    if (f.valid && f.key == key) {
+        *out = f.map;
+        return true;
+    }
     static std::mutex mu;
     static std::map<std::array<uint64_t, 13>, CUtensorMap> cache;
     {
@@ -57,6 +74,9 @@ bool make_tmap(CUtensorMap *out, CUtensorMapDataType dtype, int rank, const void
         auto it = cache.find(key);
         if (it != cache.end()) {
             *out = it->second;
+            f.key = key;
+            f.map = it->second;
+            f.valid = true;
             return true;
         }
     }
@@ -75,9 +95,14 @@ bool make_tmap(CUtensorMap *out, CUtensorMapDataType dtype, int rank, const void
                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
-    std::lock_guard<std::mutex> lock(mu);
-    if (cache.size() > 4096) cache.clear();
-    cache[key] = m;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache.size() > 4096) cache.clear();
+        cache[key] = m;
+    }
+    f.key = key;
+    f.map = m;
+    f.valid = true;
     *out = m;
     return true;
 }

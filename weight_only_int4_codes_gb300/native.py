@@ -81,6 +81,14 @@ class Config(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class GemmArgs(ctypes.Structure):
+    """w4a16_gemm_args: the argument block of w4a16_gemm_call."""
+    _fields_ = [("x", ctypes.c_void_p), ("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p), ("out", ctypes.c_void_p), ("M", ctypes.c_int),
+                ("N", ctypes.c_int), ("K", ctypes.c_int), ("group", ctypes.c_int),
+                ("cfg", ctypes.POINTER(Config))]
+
+
 _lock = threading.Lock()
 _lib = None
 _cfg_cache = {}       # config dict items -> Config (read-only once built)
@@ -118,6 +126,7 @@ def load_library():
             "w4a16_get_kernel_status": [P],
             "w4a16_stream_read": [P, ctypes.c_size_t, P, I, P],
             "w4a16_gemm_noalloc": [P, P, P, P, P, I, I, I, I, P],
+            "w4a16_gemm_call": [ctypes.POINTER(GemmArgs), P],
             "w4a16_last_error": [],
             "w4a16_version": [],
         }
@@ -221,10 +230,8 @@ def dequantize_bf16(packed, scales, zeros, group: int = 128, stream=None) -> tor
 
 def _bf16_config(config):
     """``config`` with dtype = bfloat16 (a new Config; the caller's is not changed)."""
-    c = Config()
     base = Config.make(config)
-    if base is not None:
-        ctypes.memmove(ctypes.byref(c), ctypes.byref(base), ctypes.sizeof(Config))
+    c = _copy_config(base) if base is not None else Config()
     c.dtype = DTYPE_BF16
     return c
 
@@ -246,6 +253,58 @@ def gemm_ex(x, packed, scales, zeros, group: int = 128, out=None, config=None, s
         _dev(out, "out", et), M, N, K, group,
         ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream)))
     return out
+
+
+class PreparedGemm:
+    """One GEMM call with its arguments checked and marshalled once.
+
+    ``prepare_gemm`` validates the tensors (device, dtype, contiguity), takes
+    their data pointers and builds the argument block of ``w4a16_gemm_call``;
+    each call passes that block and the current (or the given) CUDA stream,
+    so a loop that repeats the same product with new contents in x pays only
+    a two-argument C call.  The tensors are referenced by the object and must
+    keep their storage (no resize) while it is used; ``out`` is the result.
+    """
+    __slots__ = ("_fn", "_ref", "_block", "_cfg", "_keep", "_dev", "out")
+
+    def __init__(self, fn, block, cfg, keep, dev, out):
+        self._fn, self._block, self._cfg, self._keep, self._dev = fn, block, cfg, keep, dev
+        self._ref = ctypes.byref(block)
+        self.out = out
+
+    def __call__(self, stream=None):
+        if stream is None and _raw_stream is not None:
+            h = _raw_stream(self._dev)
+        else:
+            h = _stream_handle(stream)
+        st = self._fn(self._ref, h)
+        if st != 0:
+            _check(st)
+        return self.out
+
+
+def prepare_gemm(x, packed, scales, zeros, group: int = 128, out=None, config=None):
+    """A reusable call of ``gemm_ex(x, packed, scales, zeros, group, out, config)``;
+    see ``PreparedGemm``."""
+    M, K = x.shape
+    N = packed.shape[1]
+    et = torch.bfloat16 if x.dtype is torch.bfloat16 else torch.float16
+    if out is None:
+        out = torch.empty((M, N), dtype=et, device=x.device)
+    cfg = _bf16_config(config) if et is torch.bfloat16 else Config.make(config)
+    if cfg is not None:
+        cfg = _copy_config(cfg)            # private: the caller may change theirs later
+    block = GemmArgs(_dev(x, "x", et), _dev(packed, "packed", torch.int32),
+                     _dev(scales, "scales", et), _dev(zeros, "zeros", et), _dev(out, "out", et),
+                     M, N, K, group, ctypes.pointer(cfg) if cfg is not None else None)
+    return PreparedGemm(_lib_fast().w4a16_gemm_call, block, cfg, (x, packed, scales, zeros),
+                        x.device.index if x.device.index is not None else 0, out)
+
+
+def _copy_config(c):
+    d = Config()
+    ctypes.memmove(ctypes.byref(d), ctypes.byref(c), ctypes.sizeof(Config))
+    return d
 
 
 def gemm(x, packed, scales, zeros, group: int = 128, out=None, stream=None):
