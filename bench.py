@@ -99,7 +99,7 @@ def load_peaks():
 # summary is used only while these are unchanged.
 KERNEL_SOURCES = {
     "decode": ["api.cu", "common.cuh", "decode.cu", "decode_math.cuh", "decode_tma.cu",
-               "sm100_ptx.cuh", "tmap.cu", "tmap.cuh"],
+               "decode_warp.cu", "sm100_ptx.cuh", "tmap.cu", "tmap.cuh"],
     "prefill": ["api.cu", "common.cuh", "prefill.cu", "prefill_tile.cuh", "sm100_ptx.cuh",
                 "tcgen05.cuh", "tmap.cu", "tmap.cuh"],
 }

@@ -150,10 +150,11 @@ def test_prefill_split_k_requests():
 def test_auto_path_small_m_is_decode():
     for M in (1, 2, 4, 8, 16):
         p = w4.plan(M, 4096, 4096)
-        assert p["path"] == 1 and p["variant"] in (1, 2)
+        assert p["path"] == 1 and p["variant"] in (1, 2, 4)
     # measured dispatch table rows
-    t = w4.plan(1, 4096, 4096)                            # TMA variant, split 8, at M <= 2
-    assert (t["variant"], t["split_k"], t["steps"]) == (1, 8, 2)
+    assert w4.plan(1, 4096, 4096)["variant"] == 4         # warp-stream variant at M <= 4
+    assert w4.plan(4, 4096, 4096)["variant"] == 4
+    assert w4.plan(8, 4096, 4096)["variant"] == 2         # registers variant at M = 8
     assert w4.plan(16, 4096, 4096)["variant"] == 2         # registers variant at M = 16
     t = w4.plan(4, 14336, 4096)
     assert (t["variant"], t["warps_n"], t["warps_k"], t["split_k"], t["steps"]) == (1, 2, 4, 2, 8)

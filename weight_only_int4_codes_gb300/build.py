@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libw4a16.so")
-SOURCES = ["api.cu", "quant.cu", "decode.cu", "decode_tma.cu", "decode_stream.cu", "tmap.cu",
+SOURCES = ["api.cu", "quant.cu", "decode.cu", "decode_tma.cu", "decode_stream.cu", "decode_warp.cu", "tmap.cu",
            "prefill.cu", "read_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -205,14 +205,16 @@ void plan_decode_stream(int M, int N, int K, int group, int experts, bool perm, 
 
 // Measured dispatch table (GB300, group 128, one call per distinct weight copy
 // in a CUDA graph with programmatic dependent launch): the fastest decode
-// configuration for the projection shapes of the benchmark workloads.
+// configuration for the projection shapes of the benchmark workloads.  The
+// warp-stream row (4096 x 4096, M <= 4) was 2-6% ahead of the TMA variant in
+// interleaved runs of both in one process.
 struct TableEntry {
     int K, N, m_max;        // shape and the largest M the row covers
     w4a16_config cfg;
 };
 constexpr TableEntry kDecodeTable[] = {
     // K      N      M<=   path split warps_k warps_n steps tile flags variant
-    {4096, 4096, 4, {1, 8, 4, 2, 2, 0, 0, W4A16_DECODE_TMA}},
+    {4096, 4096, 4, {1, 0, 0, 0, 0, 0, 0, W4A16_DECODE_WARP}},
     {4096, 4096, 8, {1, 2, 8, 1, 8, 0, 0, W4A16_DECODE_REGISTERS}},
     {4096, 4096, 16, {1, 1, 8, 1, 16, 0, 0, W4A16_DECODE_REGISTERS}},
     {4096, 14336, 16, {1, 2, 4, 2, 8, 0, 0, W4A16_DECODE_TMA}},
@@ -324,6 +326,11 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
                             "stream decode configuration not available (M=%d warps_n=%d "
                             "split_k=%d ctas=%d, group=%d, N=%d)",
                             M, c.warps_n, c.split_k, c.ctas, group, N);
+        } else if (c.variant == W4A16_DECODE_WARP) {
+            if (!decode_warp_supported(M, N, K, group, c.ctas) || c.ctas < 0)
+                return fail(W4A16_ERR_UNSUPPORTED,
+                            "warp-stream decode not available (M=%d N=%d K=%d group=%d)", M, N,
+                            K, group);
         } else if (c.variant == W4A16_DECODE_REGISTERS) {
             plan_decode(M, N, K, group, device_info().sm_count, c);
             if (!decode_config_supported(c, M) || c.steps % decode_steps_per_batch(group) != 0 ||
@@ -580,6 +587,8 @@ w4a16_status w4a16_gemm_ex(const uint16_t *x, const uint32_t *packed, const uint
         sc.group = group;
         sc.permuted = false;
         e = launch_decode_stream(sc, c, stream);
+    } else if (c.path == W4A16_PATH_DECODE && c.variant == W4A16_DECODE_WARP) {
+        e = launch_decode_warp(a, c, stream);
     } else if (c.path == W4A16_PATH_DECODE) {
         e = c.variant == W4A16_DECODE_TMA ? launch_decode_tma(a, c, stream)
                                           : launch_decode(a, c, stream);

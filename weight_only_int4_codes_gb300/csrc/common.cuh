@@ -97,6 +97,10 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
 // Decode path, stream variant (decode_stream.cu): cfg.warps_n strips per
 // tile (1, 2 or 4), cfg.split_k 1 (whole tiles per CTA) or 2 (stream-K
 // shares), cfg.ctas CTAs (0: one per SM).
+// The warp-stream decode kernel (decode_warp.cu, M <= 4): every warp streams
+// its own run of 32-column x 512-k units through a private ring.
+bool decode_warp_supported(int M, int N, int K, int group, int ctas);
+cudaError_t launch_decode_warp(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 bool decode_stream_supported(int M, int N, int K, int group, int bns, bool perm);
 int decode_stream_stage_k(int bns);   // k per stage of a tile of bns strips
 cudaError_t launch_decode_stream(const StreamCall &call, const w4a16_config &cfg,

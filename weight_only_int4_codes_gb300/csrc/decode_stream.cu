@@ -141,19 +141,6 @@ __device__ __forceinline__ int cta_of(long long u, int G, int U) {
     return (int)(((u + 1) * G + U - 1) / U - 1);
 }
 
-// D = A * B (+ C): FIRST starts the accumulator from zero inside the MMA.
-template <bool FIRST>
-__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-    if (FIRST)
-        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
-    else
-        mma_16816(d, a0, a1, a2, a3, b0, b1);
-}
-
 // One 32-k step (decode_math.cuh's fragment mapping): the thread's four words
 // become the A operands of two MMA tiles x two k halves; KH = 2 keeps the k
 // halves in separate accumulators, KH = 1 adds them into one.
@@ -208,73 +195,7 @@ __device__ __forceinline__ void flush(float (&acc)[NT][2][4], const float (&g)[N
                                     acc[p][j][r]);
 }
 
-// ---- zero-free form of a step (M <= 8).  A nibble masked into the low bits of
-// an fp16 half with a zero exponent is the exact subnormal q * 2^-24 (bits 0..3)
-// or q * 2^-20 (bits 4..7): the codes enter the MMA with no bias to remove.
-// The low-position codes of a step go to one MMA (D_lo), the high-position ones
-// to another (D_hi), and one more pair of MMAs with an all-ones A operand sums
-// the step's x (D_x), so that per group
-//     sum_k x (q - z) s = s 2^24 (D_lo + D_hi / 16) - s z D_x,
-// with every product exact and no large term to cancel.
-constexpr bool kZeroFree = true;
-constexpr uint32_t kLoMask = 0x000F000Fu;     // nibbles 0 and 4 -> q * 2^-24
-constexpr uint32_t kHiMask = 0x00F000F0u;     // nibbles 1 and 5 -> q * 2^-20
-constexpr uint32_t kOnes = 0x3C003C00u;       // fp16 (1.0, 1.0)
-
-struct ZfConsts {
-    float s24[4], sz[4];      // s * 2^24 and s * z of the thread's four columns
-};
-
-__device__ __forceinline__ ZfConsts make_zf_consts(uint2 zraw, uint2 sraw) {
-    ZfConsts k;
-    const __half2 s01 = *reinterpret_cast<const __half2 *>(&sraw.x);
-    const __half2 s23 = *reinterpret_cast<const __half2 *>(&sraw.y);
-    const __half2 z01 = *reinterpret_cast<const __half2 *>(&zraw.x);
-    const __half2 z23 = *reinterpret_cast<const __half2 *>(&zraw.y);
-    const float sv[4] = {__low2float(s01), __high2float(s01), __low2float(s23), __high2float(s23)};
-    const float zv[4] = {__low2float(z01), __high2float(z01), __low2float(z23), __high2float(z23)};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        k.s24[c] = sv[c] * 16777216.f;
-        k.sz[c] = sv[c] * zv[c];
-    }
-    return k;
-}
-
-// One 32-k step, M <= 8: blo / bhi are the x fragments of the low / high
-// nibble positions (two registers each).
-template <bool FIRST>
-__device__ __forceinline__ void zf_step(float (&dlo)[2][4], float (&dhi)[2][4], float (&dx)[4],
-                                        uint4 w, const uint32_t (&blo)[2],
-                                        const uint32_t (&bhi)[2]) {
-    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const uint32_t c0 = wv[2 * j], c1 = wv[2 * j + 1];
-        const uint32_t d0 = c0 >> 8, d1 = c1 >> 8;
-        mma_acc<FIRST>(dlo[j], c0 & kLoMask, c1 & kLoMask, d0 & kLoMask, d1 & kLoMask, blo[0],
-                       blo[1]);
-        mma_acc<FIRST>(dhi[j], c0 & kHiMask, c1 & kHiMask, d0 & kHiMask, d1 & kHiMask, bhi[0],
-                       bhi[1]);
-    }
-    mma_acc<FIRST>(dx, kOnes, kOnes, kOnes, kOnes, blo[0], blo[1]);
-    mma_16816(dx, kOnes, kOnes, kOnes, kOnes, bhi[0], bhi[1]);
-}
-
-// acc += s 2^24 (D_lo + D_hi / 16) - s z D_x for the thread's 8 outputs
-// (D_x element r & 1 holds the x sum of batch row 2t + (r & 1)).
-__device__ __forceinline__ void zf_flush(float (&acc)[1][2][4], const float (&dlo)[2][4],
-                                         const float (&dhi)[2][4], const float (&dx)[4],
-                                         const ZfConsts &k) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int c = 2 * j + (r >> 1);
-            const float g = fmaf(0.0625f, dhi[j][r], dlo[j][r]);
-            acc[0][j][r] = fmaf(-k.sz[c], dx[r & 1], fmaf(k.s24[c], g, acc[0][j][r]));
-        }
-}
+constexpr bool kZeroFree = true;   // M <= 8: the zero-free step of decode_math.cuh
 
 template <int NT, int BNS, int LAY, bool OG, int MAXE>
 __global__ void __launch_bounds__(kThreads, 2)

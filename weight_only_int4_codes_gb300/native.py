@@ -22,7 +22,7 @@ _LIB_NAME = "libw4a16.so"
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA",
                 5: "TIMEOUT"}
 PATHS = {"auto": 0, "decode": 1, "prefill": 2}
-VARIANTS = {"auto": 0, "tma": 1, "registers": 2, "stream": 3,   # decode path
+VARIANTS = {"auto": 0, "tma": 1, "registers": 2, "stream": 3, "warp": 4,   # decode path
             "tmem": 1, "smem": 2}                  # prefill path: A's home
 DTYPES = {"f16": 0, "fp16": 0, "float16": 0, "bf16": 1, "bfloat16": 1}
 DTYPE_F16, DTYPE_BF16 = 0, 1
