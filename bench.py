@@ -17,8 +17,9 @@ Printed: one JSON line (rank 0).  `value` is the weight-stream bandwidth of the
 whole job (packed words + scales + zeros of every call, all ranks) over the
 timed region.  Beside it: per-shape microseconds per call (CUDA graph and eager
 launches), GB/s and roofline fractions, a cuBLAS fp16 reference (torch.matmul on
-the dequantized weight), the same GEMMs on the repacked weight layout, the 64
-experts of a MoE shape in one grouped launch (natural and repacked weights),
+the dequantized weight), the same GEMMs in bfloat16, with groups of 64 and 256
+rows (M = 1), and on the repacked weight layout, the 64 experts of a MoE shape in
+one grouped launch (natural and repacked weights),
 the streaming-read ceiling of a launch of the same size in the same launch
 chain, the fp64 oracle on the host cores (`cpu_baseline`), and `e2e`: the step
 through the public API (prepared calls) with all of its activations copied
@@ -449,9 +450,19 @@ def run_ours(args, rank, local, world, pg):
         Wd = torch.from_numpy(W).to(dev)
         base = w4.quantize_pack(Wd, GROUP)
         wdq = w4.dequantize(*base, group=GROUP) if args.cublas else None
-        del Wd
         R = max(2, math.ceil(3 * l2 / weight_bytes(K, N)) + 1)
         copies = [tuple(t.clone() for t in base) for _ in range(R)]
+        # extras: the same weight quantized in bfloat16, and (decode) with
+        # groups of 64 and 256 rows, R copies each
+        bf16_copies, group_copies = None, {}
+        if not args.no_extras:
+            base_b = w4.quantize_pack_bf16(Wd.bfloat16(), GROUP)
+            bf16_copies = [tuple(t.clone() for t in base_b) for _ in range(R)]
+            if workload_kind(args.workload) == "decode":
+                for gsz in (64, 256):
+                    bg = w4.quantize_pack(Wd, gsz)
+                    group_copies[gsz] = [tuple(t.clone() for t in bg) for _ in range(R)]
+        del Wd
         rep_ok = decode and w4.repacked_bytes(K, N, GROUP) > 0 and not args.no_extras
         repacked = [w4.repack(*c, group=GROUP) for c in copies] if rep_ok else None
         dq = None
@@ -466,7 +477,8 @@ def run_ours(args, rank, local, world, pg):
                                                           shape_index=sh["si"]))
                 for e in range(E)])).to(dev)
             outs[M] = torch.empty((E, M, N), dtype=torch.float16, device=dev)
-        shapes.append(dict(sh, copies=copies, repacked=repacked, dq=dq, xs=xs, outs=outs))
+        shapes.append(dict(sh, copies=copies, repacked=repacked, dq=dq, xs=xs, outs=outs,
+                           bf16_copies=bf16_copies, group_copies=group_copies))
     # the activations and outputs of every (shape, M) live in two flat arenas,
     # so that the end-to-end step moves all of its inputs with one
     # host->device copy and all of its results with one device->host copy
@@ -629,6 +641,24 @@ def run_ours(args, rank, local, world, pg):
                                    for i in range(Rq)], Rq)
                 rec["cublas_fp16_us_per_call"] = round(tq, 3)
                 rec["speedup_vs_cublas"] = round(tq / us, 3)
+            if s["bf16_copies"] is not None:
+                # the bfloat16 variant: bf16 x, scales, zeros and out
+                xb = x.bfloat16()
+                ob = torch.empty(o.shape, dtype=torch.bfloat16, device=dev)
+                ub16 = one_graph_us([lambda i=i: w4.gemm_ex(
+                    xb, *s["bf16_copies"][i], group=GROUP, out=ob, config=gemm_cfg)
+                    for i in range(R)], R)
+                rec["bf16_us_per_call"] = round(ub16, 3)
+                rec["bf16_roofline_frac"] = round(frac(M, ub16), 4)
+            if decode and M == 1 and s["group_copies"]:
+                # other group sizes (same weight, M = 1)
+                for gsz, cps in s["group_copies"].items():
+                    wb_g = K * N // 2 + 4 * (K // gsz) * N + 2 * K + 2 * N
+                    ug = one_graph_us([lambda i=i, cps=cps, gsz=gsz: w4.gemm_ex(
+                        x, *cps[i], group=gsz, out=o, config=gemm_cfg) for i in range(R)], R)
+                    rec["group%d_us_per_call" % gsz] = round(ug, 3)
+                    rec["group%d_roofline_frac" % gsz] = round(
+                        wb_g / (peaks["hbm_gbs"] * 1e9) / (ug * 1e-6), 4)
             if decode and not args.no_extras:
                 if s["repacked"] is not None:
                     ur = one_graph_us([lambda i=i: w4.gemm_repacked(

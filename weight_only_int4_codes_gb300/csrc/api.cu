@@ -179,28 +179,22 @@ void plan_decode_tma(int M, int N, int K, int group, int sm_count, w4a16_config 
 
 // Decode path, stream variant: tiles of 32*warps_n columns cut into 16 KB
 // stages; split_k = 1 gives every CTA whole tiles (no shared tile, no
-// scratch), 2 gives every CTA an equal share of all stages (stream-K).  The
-// choice compares the busiest CTA's stages, counting one more stage for the
-// cross-CTA sum of a shared tile.  Narrow tiles (long stages along K) at small
-// M, wide ones when the x rows of a stage would crowd the ring.
+// scratch), 2 gives every CTA an equal share of all stages (stream-K).
+// Measured on GB300 (repacked weights, CUDA graph + PDL; 4096 x 4096,
+// 4096 x 14336 and 2048 x 768 at M = 1..16): the narrowest tiles that fit
+// (32 columns up to M = 8, 64 above) and whole tiles per CTA were the fastest
+// at every shape and M -- stream-K shares were 1.5-2x slower, even where
+// whole tiles leave SMs idle.
 void plan_decode_stream(int M, int N, int K, int group, int experts, bool perm, int sm_count,
                         w4a16_config &c) {
+    (void)experts;
+    (void)sm_count;
     if (c.warps_n <= 0) {
-        c.warps_n = M <= 2 ? 1 : (M <= 8 ? 2 : 4);
+        c.warps_n = M <= 8 ? 1 : 2;
         while (c.warps_n < 4 && !decode_stream_supported(M, N, K, group, c.warps_n, perm))
             c.warps_n *= 2;
     }
-    if (c.split_k <= 0 && c.warps_n >= 1 && c.warps_n <= 4) {
-        const int BN = 32 * c.warps_n, SK = decode_stream_stage_k(c.warps_n);
-        const long long T = (long long)experts * ((N + BN - 1) / BN);
-        const long long KS = (K + SK - 1) / SK, U = T * KS;
-        const long long G = c.ctas > 0 ? c.ctas : sm_count;
-        const long long ga = G < T ? G : T;
-        const long long gs = G < U ? G : U;
-        const long long load_align = (T + ga - 1) / ga * KS;
-        const long long load_shared = (U + gs - 1) / gs + 1;
-        c.split_k = load_align <= load_shared ? 1 : 2;
-    }
+    if (c.split_k <= 0) c.split_k = 1;
 }
 
 // Measured dispatch table (GB300, group 128, one call per distinct weight copy
