@@ -172,15 +172,18 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 
 def test_bf16_planning():
-    """dtype = bf16: decode on the registers variant, prefill on A in tensor
-    memory; the other variants and unknown dtypes are refused on the host."""
+    """dtype = bf16: decode on the registers or TMA variant (a measured table
+    row for another variant falls back to the TMA planner), prefill on A in
+    tensor memory; the other variants and unknown dtypes are refused."""
     for M in (1, 8, 16):
         p = w4.plan(M, 4096, 4096, dtype="bf16")
-        assert (p["path"], p["variant"], p["dtype"]) == (1, 2, 1)
-        assert p["warps_k"] * p["steps"] * 4 * p["split_k"] >= 4096 // 8
+        assert (p["path"], p["dtype"]) == (1, 1) and p["variant"] in (1, 2)
+    assert w4.plan(1, 4096, 4096, dtype="bf16")["variant"] == 1     # the fp16 row is warp-stream
+    assert w4.plan(8, 4096, 4096, dtype="bf16")["variant"] == 2     # the table's registers row
+    assert w4.plan(4, 4096, 14336, dtype="bf16")["variant"] == 1    # the table's TMA row
     p = w4.plan(1024, 14336, 4096, dtype="bf16")
     assert (p["path"], p["dtype"]) == (2, 1) and p["variant"] == 1
-    for bad in (dict(path="decode", variant="tma"), dict(path="decode", variant="stream"),
+    for bad in (dict(path="decode", variant="warp"), dict(path="decode", variant="stream"),
                 dict(path="prefill", variant="smem", tile_m=64)):
         with pytest.raises(native.W4A16Error) as e:
             w4.plan(64 if bad["path"] == "prefill" else 4, 4096, 4096, dtype="bf16", **bad)

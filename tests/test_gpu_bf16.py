@@ -161,6 +161,31 @@ def test_gemm_bf16_decode_launch_shapes(cfg, M):
     check_gemm(xb, dev_w, ref_w, 128, config=cfg)
 
 
+@pytest.mark.parametrize("cfg", [
+    dict(path="decode", variant="tma", warps_k=4, warps_n=2),
+    dict(path="decode", variant="tma", warps_k=8, warps_n=4, split_k=3),
+    dict(path="decode", variant="tma", warps_k=16, warps_n=2, split_k=8),
+    dict(path="decode", variant="tma", warps_k=4, warps_n=4, split_k=2, pdl=True),
+])
+@pytest.mark.parametrize("M", [1, 5, 9, 16])
+def test_gemm_bf16_decode_tma(cfg, M):
+    """The TMA decode kernel's bfloat16 instantiations: every consumer count,
+    tile width and several cluster sizes; a ragged last column tile."""
+    K, N = 2048, 776
+    dev_w, ref_w = quantized(K, N, 128, 71, True)
+    xb = synth.activations_bf16(M, K, seed=76 + M)
+    check_gemm(xb, dev_w, ref_w, 128, config=cfg)
+
+
+@pytest.mark.parametrize("group", [32, 64, 256])
+@pytest.mark.parametrize("M", [1, 12])
+def test_gemm_bf16_tma_groups(group, M):
+    K, N = 2048, 512
+    dev_w, ref_w = quantized(K, N, group, 81 + group, False)
+    xb = synth.activations_bf16(M, K, seed=83 + M)
+    check_gemm(xb, dev_w, ref_w, group, config=dict(path="decode", variant="tma"))
+
+
 @pytest.mark.parametrize("group", [32, 64, 256, 512])
 @pytest.mark.parametrize("M", [1, 12])
 def test_gemm_bf16_other_groups(group, M):
@@ -228,6 +253,7 @@ def test_gemm_bf16_random_encodings():
 
 @pytest.mark.parametrize("M,config", [
     (1, None), (16, None), (9, dict(path="decode", variant="registers", warps_n=2, warps_k=4)),
+    (3, dict(path="decode", variant="tma")), (12, dict(path="decode", variant="tma", warps_k=16)),
     (64, dict(path="prefill", tile_m=64)), (128, dict(path="prefill", tile_m=128)),
     (300, dict(path="prefill", tile_m=256)),
 ])
@@ -270,7 +296,7 @@ def test_bf16_rejected_where_not_built():
     """The variants without a bfloat16 kernel refuse it (nothing enqueued)."""
     dev_w, _ = quantized(512, 256, 128, 181, False)
     x = bf_dev(synth.activations_bf16(4, 512, seed=182))
-    for cfg in (dict(path="decode", variant="tma"), dict(path="decode", variant="stream"),
+    for cfg in (dict(path="decode", variant="warp"), dict(path="decode", variant="stream"),
                 dict(path="prefill", variant="smem", tile_m=64)):
         with pytest.raises(w4.W4A16Error) as e:
             w4.gemm_ex(x, *dev_w, group=128, config=cfg)

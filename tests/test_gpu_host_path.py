@@ -112,7 +112,7 @@ def test_prepared_call_bf16_and_errors(weights):
     torch.cuda.synchronize()
     assert out.dtype == torch.bfloat16 and torch.equal(out.view(torch.int16), ref.view(torch.int16))
     # a request the library refuses is reported when the prepared call runs
-    bad = w4.prepare_gemm(x, packed, scales, zeros, group=128, config=dict(variant="tma",
+    bad = w4.prepare_gemm(x, packed, scales, zeros, group=128, config=dict(variant="warp",
                                                                            path="decode"))
     with pytest.raises(w4.W4A16Error) as e:
         bad()

@@ -250,9 +250,10 @@ bool decode_from_table(int M, int N, int K, int group, w4a16_config &c) {
         return false;
     for (const TableEntry &e : kDecodeTable)
         if (e.K == K && e.N == N && M <= e.m_max) {
-            const int flags = c.flags;
+            const int flags = c.flags, dtype = c.dtype;
             c = e.cfg;
             c.flags = flags;
+            c.dtype = dtype;
             return true;
         }
     return false;
@@ -294,14 +295,21 @@ w4a16_status make_plan(int M, int N, int K, int group, const w4a16_config *req,
         }
     }
     if (c.path == W4A16_PATH_DECODE) {
-        // bfloat16 runs on the registers variant (the only decode kernel
-        // built for it); the measured table is for fp16
-        if (bf && c.variant == W4A16_DECODE_AUTO) c.variant = W4A16_DECODE_REGISTERS;
-        if (bf && c.variant != W4A16_DECODE_REGISTERS)
-            return fail(W4A16_ERR_UNSUPPORTED,
-                        "bfloat16 decode: registers variant only (variant %d requested)",
-                        c.variant);
         if (M <= 16) decode_from_table(M, N, K, group, c);
+        // bfloat16 runs on the registers and TMA variants; a table row for
+        // another variant falls back to the TMA planner
+        if (bf && c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_REGISTERS &&
+            c.variant != W4A16_DECODE_TMA) {
+            if (req && req->variant == c.variant)
+                return fail(W4A16_ERR_UNSUPPORTED,
+                            "bfloat16 decode: registers or TMA variant (variant %d requested)",
+                            c.variant);
+            const int flags = c.flags;
+            c = w4a16_config{};
+            c.path = W4A16_PATH_DECODE;
+            c.flags = flags;
+            c.dtype = W4A16_DTYPE_BF16;
+        }
         if (c.variant == W4A16_DECODE_AUTO)
             c.variant = tma_variant_possible(N, group) ? W4A16_DECODE_TMA : W4A16_DECODE_REGISTERS;
         if (c.variant == W4A16_DECODE_TMA) {

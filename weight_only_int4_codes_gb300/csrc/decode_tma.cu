@@ -64,7 +64,10 @@ __device__ __forceinline__ int perm8(int g) { return (g >> 1) + ((g & 1) << 2); 
 // ONE_GROUP: a warp's share of a stage (8*BNS*... k rows) lies inside one
 // quantization group (group >= 32 * steps per warp), so the group constants
 // are formed once per stage and the step loop has no branches.
-template <int NT, int BNS, int CW, bool ONE_GROUP>
+// BF: x, scales, zeros and out are bfloat16; every weight is dequantized with
+// its scale (one bf16 multiply) and the MMAs accumulate straight into running
+// sums (decode_math.cuh, bfloat16 section).
+template <int NT, int BNS, int CW, bool ONE_GROUP, bool BF>
 __global__ void __launch_bounds__(32 * (CW + 1), CW == 4 ? 3 : (CW == 8 ? 2 : 1))
 decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_x,
@@ -120,12 +123,13 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     if (a.split > 1) cluster_arrive();
 
     float acc[NT][2][4];
+    float accb[NT][2][2][4];   // bfloat16 only: running sums of the two k halves
 #pragma unroll
     for (int p = 0; p < NT; ++p)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[p][j][r] = 0.f;
+            for (int r = 0; r < 4; ++r) acc[p][j][r] = accb[p][j][0][r] = accb[p][j][1][r] = 0.f;
 
     const int g = lane >> 2, t = lane & 3;
     const int wn = warp % BNS, wk = warp / BNS;
@@ -241,6 +245,17 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);   // operands are in registers
             if (++slot == a.stages) { slot = 0; phase ^= 1; }
+            if constexpr (BF) {
+                GroupConstsBf kb = make_group_consts_bf(zraw[0], sraw[0]);
+#pragma unroll
+                for (int u = 0; u < SPW; ++u) {
+                    if (!ONE_GROUP && u > 0) kb = make_group_consts_bf(zraw[u], sraw[u]);
+                    uint32_t bx[NT][4];
+#pragma unroll
+                    for (int p = 0; p < NT; ++p) x_fragments(xv[p][u], bx[p]);
+                    step_mma_bf16<NT>(accb, wv[u], kb, bx);
+                }
+            } else {
             GroupConsts k = make_group_consts(zraw[0], sraw[0]);
             // one group per warp-stage: the warp's steps accumulate together
             // and the scale is applied once; otherwise once per step
@@ -261,6 +276,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                 if (!ONE_GROUP) flush_group_split<NT>(acc, gs, k);
             }
             if (ONE_GROUP) flush_group_split<NT>(acc, gs, k);
+            }
+        }
+        if constexpr (BF) {
+#pragma unroll
+            for (int p = 0; p < NT; ++p)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) acc[p][j][r] = accb[p][j][0][r] + accb[p][j][1][r];
         }
     }
 
@@ -324,7 +348,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         const int m = e / BN, c = e - m * BN;
         const int col = col_base + c;
         if (col < a.N)
-            a.out[(size_t)(m_base + m) * a.N + col] = __half_as_ushort(__float2half_rn(v));
+            a.out[(size_t)(m_base + m) * a.N + col] = to_out<BF>(v);
     }
 }
 
@@ -359,12 +383,12 @@ Layout layout_for(int group, int bns, int nt, int n_st, int split, int cw) {
     return L;
 }
 
-template <int NT, int BNS, int CW, bool OG>
+template <int NT, int BNS, int CW, bool OG, bool BF>
 cudaError_t launch_tma(const CUtensorMap &w, const CUtensorMap &s, const CUtensorMap &z,
                        const CUtensorMap &x, const TmaDecodeArgs &da, int tiles, int mchunks,
                        int smem, bool pdl, cudaStream_t stream) {
     const cudaError_t attr_err =
-        ensure_dynamic_smem((const void *)decode_tma_kernel<NT, BNS, CW, OG>, kSmemMax);
+        ensure_dynamic_smem((const void *)decode_tma_kernel<NT, BNS, CW, OG, BF>, kSmemMax);
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(tiles, da.split, mchunks);
@@ -387,7 +411,7 @@ cudaError_t launch_tma(const CUtensorMap &w, const CUtensorMap &s, const CUtenso
     }
     lc.attrs = attrs;
     lc.numAttrs = na;
-    return cudaLaunchKernelEx(&lc, decode_tma_kernel<NT, BNS, CW, OG>, w, s, z, x, da);
+    return cudaLaunchKernelEx(&lc, decode_tma_kernel<NT, BNS, CW, OG, BF>, w, s, z, x, da);
 }
 
 
@@ -415,6 +439,7 @@ bool decode_tma_supported(const w4a16_config &cfg, int group) {
 // along K, steps = 256-k stages per CTA.
 cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream) {
     if (!decode_tma_supported(cfg, a.group)) return cudaErrorNotSupported;
+    const bool bf = cfg.dtype == W4A16_DTYPE_BF16;
     const int bns = cfg.warps_n;
     const int nt = a.M > 8 ? 2 : 1;
     const int KB = a.K / 8;
@@ -476,11 +501,13 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     // steps per warp per stage: 8 * bns / cw; one group per warp-stage if the
     // group spans at least that many 32-k steps
     const bool one_group = a.group >= 32 * (8 * bns / cw);
-#define W4A16_TMA_LAUNCH(NT_, BNS_, CW_)                                                         \
-    (one_group ? launch_tma<NT_, BNS_, CW_, true>(tw, ts, tz, tx, da, tiles, mchunks,          \
-                                                  L.smem_bytes, pdl, stream)                   \
-               : launch_tma<NT_, BNS_, CW_, false>(tw, ts, tz, tx, da, tiles, mchunks,         \
-                                                   L.smem_bytes, pdl, stream))
+#define W4A16_TMA_LAUNCH1(NT_, BNS_, CW_, BF_)                                                   \
+    (one_group ? launch_tma<NT_, BNS_, CW_, true, BF_>(tw, ts, tz, tx, da, tiles, mchunks,     \
+                                                       L.smem_bytes, pdl, stream)              \
+               : launch_tma<NT_, BNS_, CW_, false, BF_>(tw, ts, tz, tx, da, tiles, mchunks,    \
+                                                        L.smem_bytes, pdl, stream))
+#define W4A16_TMA_LAUNCH(NT_, BNS_, CW_) \
+    (bf ? W4A16_TMA_LAUNCH1(NT_, BNS_, CW_, true) : W4A16_TMA_LAUNCH1(NT_, BNS_, CW_, false))
     if (cw == 8) {
         if (nt == 1) return bns == 4 ? W4A16_TMA_LAUNCH(1, 4, 8) : W4A16_TMA_LAUNCH(1, 2, 8);
         return bns == 4 ? W4A16_TMA_LAUNCH(2, 4, 8) : W4A16_TMA_LAUNCH(2, 2, 8);
@@ -492,6 +519,7 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
     if (nt == 1) return bns == 4 ? W4A16_TMA_LAUNCH(1, 4, 16) : W4A16_TMA_LAUNCH(1, 2, 16);
     return bns == 4 ? W4A16_TMA_LAUNCH(2, 4, 16) : W4A16_TMA_LAUNCH(2, 2, 16);
 #undef W4A16_TMA_LAUNCH
+#undef W4A16_TMA_LAUNCH1
 }
 
 }  // namespace w4a16
