@@ -117,3 +117,51 @@ def test_prepared_call_bf16_and_errors(weights):
     with pytest.raises(w4.W4A16Error) as e:
         bad()
     assert e.value.status == 2
+
+
+def test_concurrent_host_threads(weights):
+    """Four host threads, each with its own stream, issue GEMMs of different
+    shapes and variants at once (ctypes releases the interpreter lock during
+    the C call, so the plan, tensor-map and scratch caches are exercised
+    concurrently); every result equals the single-threaded one bit for bit."""
+    import threading
+    _, dev_w, _ = weights
+    K = dev_w[0].shape[0] * 8
+    cases = [(1, dict(path="decode", variant="tma", pdl=True)),
+             (3, dict(path="decode", variant="registers")),
+             (2, dict(path="decode", variant="warp")),
+             (8, dict(path="decode", variant="stream")),
+             (64, None)]
+    xs = {M: to_dev(synth.activations(M, K, seed=240 + M)) for M, _ in cases}
+    ref = {}
+    for M, cfg in cases:
+        ref[M] = w4.gemm_ex(xs[M], *dev_w, group=128, config=cfg).clone()
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(tid):
+        try:
+            s = torch.cuda.Stream()
+            outs = {M: torch.empty_like(ref[M]) for M, _ in cases}
+            calls = [w4.prepare_gemm(xs[M], *dev_w, group=128, out=outs[M], config=cfg)
+                     for M, cfg in cases]
+            with torch.cuda.stream(s):
+                for it in range(40):
+                    for c in calls[tid % len(calls):] + calls[:tid % len(calls)]:
+                        c(s)
+                    if it % 10 == 9:
+                        s.synchronize()
+                        for M, _ in cases:
+                            if not torch.equal(outs[M].view(torch.int16), ref[M].view(torch.int16)):
+                                errors.append((tid, it, M))
+            s.synchronize()
+        except Exception as e:        # reported below, on the main thread
+            errors.append((tid, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors[:5]
+    assert w4.kernel_status() == 0
