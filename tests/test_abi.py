@@ -194,6 +194,16 @@ def test_bf16_planning():
     assert w4.plan(4, 4096, 4096)["dtype"] == 0
 
 
+def test_gemm_call_validates(lib):
+    """The argument-block entry: a null block is refused; a block with a bad
+    shape returns the same status as w4a16_gemm_ex."""
+    assert lib.w4a16_gemm_call(None, None) == 1
+    blk = native.GemmArgs(16, 16, 16, 16, 16, 1, 4096, 4000, 128, None)   # K % group != 0
+    assert lib.w4a16_gemm_call(ctypes.byref(blk), None) == 1
+    blk = native.GemmArgs(16, 16, 16, 16, 16, 1, 4094, 4096, 128, None)   # N % 4 != 0
+    assert lib.w4a16_gemm_call(ctypes.byref(blk), None) == 3
+
+
 def test_bf16_entries_validate_before_touching_the_gpu(lib):
     assert lib.w4a16_quantize_pack_bf16(None, 512, 256, 128, None, None, None, None) == 1
     assert lib.w4a16_quantize_pack_bf16(16, 500, 256, 128, 16, 16, 16, None) == 1   # K % group
