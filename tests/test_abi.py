@@ -178,9 +178,13 @@ def test_bf16_planning():
     for M in (1, 8, 16):
         p = w4.plan(M, 4096, 4096, dtype="bf16")
         assert (p["path"], p["dtype"]) == (1, 1) and p["variant"] in (1, 2)
-    assert w4.plan(1, 4096, 4096, dtype="bf16")["variant"] == 1     # the fp16 row is warp-stream
-    assert w4.plan(8, 4096, 4096, dtype="bf16")["variant"] == 2     # the table's registers row
-    assert w4.plan(4, 4096, 14336, dtype="bf16")["variant"] == 1    # the table's TMA row
+    # the bf16 dispatch table (measured on bf16 data)
+    t = w4.plan(1, 4096, 4096, dtype="bf16")
+    assert (t["variant"], t["split_k"], t["warps_k"], t["warps_n"], t["steps"]) == (1, 8, 4, 2, 2)
+    assert w4.plan(16, 2048, 768, dtype="bf16")["variant"] == 2
+    assert w4.plan(4, 4096, 14336, dtype="bf16")["variant"] == 1
+    # off the table: the TMA planner
+    assert w4.plan(1, 8192, 8192, dtype="bf16")["variant"] == 1
     p = w4.plan(1024, 14336, 4096, dtype="bf16")
     assert (p["path"], p["dtype"]) == (2, 1) and p["variant"] == 1
     for bad in (dict(path="decode", variant="warp"), dict(path="decode", variant="stream"),

@@ -220,6 +220,21 @@ constexpr TableEntry kDecodeTable[] = {
     {768, 2048, 16, {1, 1, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
 };
 
+// The same for bfloat16 (registers and TMA variants only; measured the same
+// way on bf16 weights and activations).
+constexpr TableEntry kDecodeTableBf16[] = {
+    // K      N      M<=   path split warps_k warps_n steps tile flags variant
+    {4096, 4096, 4, {1, 8, 4, 2, 2, 0, 0, W4A16_DECODE_TMA}},
+    {4096, 4096, 8, {1, 4, 16, 4, 4, 0, 0, W4A16_DECODE_TMA}},
+    {4096, 4096, 16, {1, 2, 16, 2, 8, 0, 0, W4A16_DECODE_TMA}},
+    {4096, 14336, 16, {1, 2, 4, 2, 8, 0, 0, W4A16_DECODE_TMA}},
+    {14336, 4096, 8, {1, 8, 8, 4, 7, 0, 0, W4A16_DECODE_TMA}},
+    {14336, 4096, 16, {1, 4, 16, 4, 14, 0, 0, W4A16_DECODE_TMA}},
+    {2048, 768, 4, {1, 8, 8, 2, 1, 0, 0, W4A16_DECODE_TMA}},
+    {2048, 768, 16, {1, 2, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+    {768, 2048, 16, {1, 1, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+};
+
 // Grouped launches of 64 experts (measured the same way, one grouped launch
 // per 64 distinct weight copies): registers variant, no split -- the experts
 // already give thousands of CTAs.
@@ -243,12 +258,18 @@ bool grouped_from_table(int M, int N, int K, int group, w4a16_config &c) {
     return false;
 }
 
-// Fill an all-automatic decode request from the table; false if no row fits.
+// Fill an all-automatic decode request from the table of its dtype; false if
+// no row fits.
 bool decode_from_table(int M, int N, int K, int group, w4a16_config &c) {
     if (group != 128 || c.variant != W4A16_DECODE_AUTO || c.split_k || c.warps_k || c.warps_n ||
         c.steps)
         return false;
-    for (const TableEntry &e : kDecodeTable)
+    const bool bf = c.dtype == W4A16_DTYPE_BF16;
+    const TableEntry *rows = bf ? kDecodeTableBf16 : kDecodeTable;
+    const size_t n = bf ? sizeof(kDecodeTableBf16) / sizeof(TableEntry)
+                        : sizeof(kDecodeTable) / sizeof(TableEntry);
+    for (size_t i = 0; i < n; ++i) {
+        const TableEntry &e = rows[i];
         if (e.K == K && e.N == N && M <= e.m_max) {
             const int flags = c.flags, dtype = c.dtype;
             c = e.cfg;
@@ -256,6 +277,7 @@ bool decode_from_table(int M, int N, int K, int group, w4a16_config &c) {
             c.dtype = dtype;
             return true;
         }
+    }
     return false;
 }
 
