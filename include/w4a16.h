@@ -318,22 +318,31 @@ W4A16_API w4a16_status w4a16_repack(const uint32_t *packed, const uint16_t *scal
                           cudaStream_t stream);
 
 /*
- * out[M,N] = x[M,K] . W, with W given in the repacked form: the stream decode
- * kernel (W4A16_DECODE_STREAM) reading one contiguous block per strip and
- * stage.  cfg NULL or a stream-variant configuration (warps_n, split_k, ctas,
- * flags).  M up to 16 per launch; larger M runs ceil(M/16) launches in
- * stream order.  Same x / out layouts and alignment rules as w4a16_gemm;
- * `repacked` 16-byte aligned.  The result equals w4a16_gemm on the natural
- * weights within the GEMM tolerance (the MMAs see the same values; only the
- * summation order of the k-permutation differs).
+ * out[M,N] = x[M,K] . W, with W given in the repacked form, reading one
+ * contiguous block per strip and 256-k stage with one bulk copy.  Two kernels:
+ *   W4A16_DECODE_WARP    M <= 4: every warp streams its own run of blocks
+ *                        through a private ring (the design of the natural-
+ *                        layout warp-stream kernel); at most 64 32-column
+ *                        tiles per CTA (over all experts of a grouped call).
+ *   W4A16_DECODE_STREAM  M up to 16 per launch; larger M runs ceil(M/16)
+ *                        launches in stream order.
+ * cfg NULL (or variant AUTO with warps_n and split_k 0) takes the warp kernel
+ * where it serves the call and the call has at least four 256-k blocks per SM
+ * (over all experts), else the stream kernel; a stream-variant
+ * configuration (warps_n, split_k, ctas, flags) or the warp variant (ctas,
+ * flags) may be requested, and a warp request it cannot serve returns
+ * W4A16_ERR_UNSUPPORTED.  Same x / out layouts and alignment rules as
+ * w4a16_gemm; `repacked` 16-byte aligned.  The result equals w4a16_gemm on the
+ * natural weights within the GEMM tolerance (the MMAs see the same values;
+ * only the summation order of the k-permutation differs).
  */
 W4A16_API w4a16_status w4a16_gemm_repacked(const uint16_t *x, const void *repacked, uint16_t *out,
                                  int M, int N, int K, int group, const w4a16_config *cfg,
                                  cudaStream_t stream);
 
 /* Grouped form of w4a16_gemm_repacked: E <= W4A16_MAX_EXPERTS experts of one
- * shape in one launch, M <= 16; host arrays of E device pointers as in
- * w4a16_gemm_grouped. */
+ * shape in one launch, M <= 16 (the warp kernel at M <= 4, as above); host
+ * arrays of E device pointers as in w4a16_gemm_grouped. */
 W4A16_API w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const *x,
                                          const void *const *repacked, uint16_t *const *out,
                                          int M, int N, int K, int group,

@@ -308,7 +308,7 @@ def test_repack_rejects_unsupported_shapes():
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("cfg", [dict(), dict(split_k=1), dict(split_k=2),
+@pytest.mark.parametrize("cfg", [dict(), dict(variant="stream"), dict(split_k=1), dict(split_k=2),
                                  dict(warps_n=1, split_k=2), dict(warps_n=4, split_k=1),
                                  dict(split_k=2, ctas=45), dict(pdl=True)],
                          ids=lambda c: "-".join("%s%s" % (k, v) for k, v in c.items()) or "auto")

@@ -763,11 +763,32 @@ w4a16_status plan_repacked(int M, int N, int K, int group, int experts, const w4
                     K, N, group);
     c = cfg ? *cfg : w4a16_config{};
     if ((c.path != W4A16_PATH_AUTO && c.path != W4A16_PATH_DECODE) ||
-        (c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_STREAM))
-        return fail(W4A16_ERR_UNSUPPORTED, "repacked weights: decode path, stream variant only");
+        (c.variant != W4A16_DECODE_AUTO && c.variant != W4A16_DECODE_STREAM &&
+         c.variant != W4A16_DECODE_WARP))
+        return fail(W4A16_ERR_UNSUPPORTED, "repacked weights: decode path, stream or warp "
+                    "variant only");
     if (c.dtype != W4A16_DTYPE_F16)
         return fail(W4A16_ERR_UNSUPPORTED, "repacked weights: fp16 only");
     c.path = W4A16_PATH_DECODE;
+    // the warp-stream kernel serves M <= 4 (every row in one launch); the
+    // stream kernel the rest.  By default the warp kernel takes calls of at
+    // least four 256-k blocks per SM: below that too few warps have work, and
+    // the stream kernel (more CTAs per tile) was measured faster
+    const bool warp_ok = M <= 4 && decode_warp_perm_supported(M > 0 ? M : 1, N, K, group,
+                                                              experts, c.ctas);
+    const long long blocks = (long long)experts * (N / 32) * (K / 256);
+    if (c.variant == W4A16_DECODE_WARP) {
+        if (!warp_ok)
+            return fail(W4A16_ERR_UNSUPPORTED, "repacked warp-stream kernel: M <= 4 and at "
+                        "most 64 tiles per CTA (M=%d N=%d K=%d group=%d E=%d ctas=%d)",
+                        M, N, K, group, experts, c.ctas);
+        return W4A16_OK;
+    }
+    if (c.variant == W4A16_DECODE_AUTO && warp_ok && c.warps_n == 0 && c.split_k == 0 &&
+        blocks >= 4LL * device_info().sm_count) {
+        c.variant = W4A16_DECODE_WARP;
+        return W4A16_OK;
+    }
     c.variant = W4A16_DECODE_STREAM;
     const int m = M < 16 ? M : 16;
     plan_decode_stream(m > 0 ? m : 1, N, K, group, experts, true, device_info().sm_count, c);
@@ -797,6 +818,15 @@ w4a16_status w4a16_gemm_repacked(const uint16_t *x, const void *repacked, uint16
     sc.K = K;
     sc.group = group;
     sc.permuted = true;
+    if (c.variant == W4A16_DECODE_WARP) {
+        sc.M = M;
+        sc.x[0] = x;
+        sc.out[0] = out;
+        cudaError_t e = launch_decode_warp_perm(sc, c, stream);
+        if (e == cudaErrorNotSupported)
+            return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
+        return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "gemm launch");
+    }
     // 16 rows of x per launch (the decode kernel's batch); larger M runs
     // several launches in stream order
     for (int m0 = 0; m0 < M; m0 += 16) {
@@ -850,7 +880,8 @@ w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const *x,
     sc.K = K;
     sc.group = group;
     sc.permuted = true;
-    cudaError_t err = launch_decode_stream(sc, c, stream);
+    cudaError_t err = c.variant == W4A16_DECODE_WARP ? launch_decode_warp_perm(sc, c, stream)
+                                                     : launch_decode_stream(sc, c, stream);
     if (err == cudaErrorNotSupported)
         return fail(W4A16_ERR_UNSUPPORTED, "no kernel for this configuration");
     return err == cudaSuccess ? W4A16_OK : cuda_fail(err, "grouped gemm launch");

@@ -101,6 +101,12 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
 // its own run of 32-column x 512-k units through a private ring.
 bool decode_warp_supported(int M, int N, int K, int group, int ctas);
 cudaError_t launch_decode_warp(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
+// The same design on repacked blocks (one bulk copy per unit), for one or up
+// to kMaxExperts GEMMs of one shape (M <= 4).
+bool decode_warp_perm_supported(int M, int N, int K, int group, int experts, int ctas);
+struct StreamCall;
+cudaError_t launch_decode_warp_perm(const StreamCall &call, const w4a16_config &cfg,
+                                    cudaStream_t stream);
 bool decode_stream_supported(int M, int N, int K, int group, int bns, bool perm);
 int decode_stream_stage_k(int bns);   // k per stage of a tile of bns strips
 cudaError_t launch_decode_stream(const StreamCall &call, const w4a16_config &cfg,

@@ -385,4 +385,348 @@ cudaError_t launch_decode_warp(const GemmArgs &g, const w4a16_config &cfg, cudaS
     }
 }
 
+
+// ------------------------------------------------------------ repacked weights
+// The same warp-stream design on the pre-permuted layout (quant.cu's repack):
+// a unit is UB consecutive repacked blocks of one strip -- a block is 32
+// columns x 256 k, 1024 words in lane order, then its scales and zeros; the
+// blocks of a strip are contiguous -- fetched with ONE 1-D bulk copy (no
+// tensor map), and x's rows of the unit by one bulk copy each.  The last unit
+// of a strip may hold fewer blocks.  Each
+// lane's 128-bit read of a step is its MMA fragment, and x enters the MMA as
+// it sits in memory.  Up to kMaxExperts GEMMs of one shape per launch: the
+// units of all experts' tiles are split between the CTAs as above.
+namespace {
+
+constexpr int kPermK = 256;                 // k per repacked block
+constexpr int kPermSteps = kPermK / 32;
+constexpr int kPermWordBytes = 4096;        // the block's packed words
+
+struct PermArgs {
+    int *status;
+    int M, N, K, group, E;
+    int T;                   // 32-column strips per expert
+    int KB;                  // 256-k blocks per strip
+    int UB, U;               // blocks per unit, units per strip (ceil(KB / UB))
+    int blk_bytes;           // 4096 + 128 * groups per block
+    int G, D;                // CTAs, ring slots per warp
+    int slot_bytes, x_off;   // per slot: UB blocks, then M rows of UB * 256 k of x
+    int part_off, cnt_off, bar_off;
+    unsigned long long timeout_ns;
+};
+
+struct PermTable {
+    const uint16_t *x[kMaxExperts];
+    const uint8_t *w[kMaxExperts];
+    uint16_t *out[kMaxExperts];
+};
+
+// SG: 32-k steps per scale group inside a block (8 when a group spans it).
+template <int SG>
+__global__ void __launch_bounds__(32 * kW, 1)
+decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constant__ PermTable tab)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    int *cnt = reinterpret_cast<int *>(smem + a.cnt_off);
+    float *part = reinterpret_cast<float *>(smem + a.part_off);   // [kW][2][kMaxM][32]
+
+    pdl_launch_dependents();
+    // this CTA's tiles (over all experts: tile = expert * T + strip) and the
+    // runs of its warps, as in decode_warp_kernel
+    const int TT = a.E * a.T;
+    const int tc0 = (int)((long long)TT * blockIdx.x / a.G);
+    const int tc1 = (int)((long long)TT * (blockIdx.x + 1) / a.G);
+    const int ucta = (tc1 - tc0) * a.U;
+    const int weff = ucta < kW ? ucta : kW;
+    const int q = ucta / weff, r = ucta - q * weff;
+    auto begin_of = [&](int w) { return w * q + (w < r ? w : r); };
+    auto warp_of = [&](int u) {
+        const int lim = r * (q + 1);
+        return u < lim ? u / (q + 1) : r + (u - lim) / q;
+    };
+    if (threadIdx.x < kMaxTilesPerCta) cnt[threadIdx.x] = 0;
+    __syncthreads();   // counters are zero before any warp counts
+    if (warp >= weff) return;
+
+    const int ub = begin_of(warp), ue = begin_of(warp + 1), n = ue - ub;
+    uint8_t *ring = smem + warp * a.D * a.slot_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.bar_off) + warp * a.D;
+    if (lane == 0) {
+        for (int i = 0; i < a.D; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const uint64_t pol_w = l2_evict_first_policy();
+    const uint64_t pol_x = l2_evict_last_policy();
+    const int xrow = a.UB * kPermK * 2;   // bytes per row of x in a slot
+    auto blocks_of = [&](int iu) {
+        const int b = a.KB - iu * a.UB;
+        return b < a.UB ? b : a.UB;
+    };
+    // lane 0: the blocks of (tile it, unit iu) into slot sl, with the barrier
+    // armed for the whole unit, x included; x follows separately
+    auto issue_w = [&](int sl, int it, int iu) {
+        const int e = it / a.T, sn = it - e * a.T, nb = blocks_of(iu);
+        mbar_arrive_expect_tx(&full[sl], (uint32_t)(nb * (a.blk_bytes + a.M * kPermK * 2)));
+        bulk_load(smem_u32(ring + sl * a.slot_bytes),
+                  tab.w[e] + ((size_t)sn * a.KB + (size_t)iu * a.UB) * a.blk_bytes,
+                  (uint32_t)(nb * a.blk_bytes), smem_u32(&full[sl]), pol_w);
+    };
+    auto issue_x = [&](int sl, int it, int iu) {
+        const int e = it / a.T, nb = blocks_of(iu);
+        for (int m = 0; m < a.M; ++m)
+            bulk_load(smem_u32(ring + sl * a.slot_bytes + a.x_off + m * xrow),
+                      tab.x[e] + (size_t)m * a.K + (size_t)iu * a.UB * kPermK,
+                      (uint32_t)(nb * kPermK * 2), smem_u32(&full[sl]), pol_x);
+    };
+    int tl = ub / a.U, kc = ub - (ub / a.U) * a.U;   // the unit being computed (local tile)
+    int itl = tl, ikc = kc;                              // the next unit to request
+    const int first = n < a.D ? n : a.D;
+    for (int i = 0; i < first; ++i) {
+        if (lane == 0) issue_w(i, tc0 + itl, ikc);
+        if (++ikc == a.U) { ikc = 0; ++itl; }
+    }
+    pdl_wait();   // x and out may belong to the previous kernel
+    if (lane == 0) {
+        int xt = tl, xk = kc;
+        for (int i = 0; i < first; ++i) {
+            issue_x(i, tc0 + xt, xk);
+            if (++xk == a.U) { xk = 0; ++xt; }
+        }
+    }
+
+    const bool x_ok = g < a.M;
+    const uint32_t x_row = (uint32_t)(a.x_off + (x_ok ? g : 0) * xrow + t * 16);
+
+    float acc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+
+    const int first_tl = tl;
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < n; ++i) {
+        if (!mbar_wait_bounded(&full[slot], phase, a.timeout_ns))
+            report_status(a.status, W4A16_ERR_TIMEOUT);
+        const uint32_t s0 = smem_u32(ring) + slot * a.slot_bytes;
+        const int nb = blocks_of(kc);
+        for (int b = 0; b < nb; ++b) {
+            const uint32_t sb = s0 + b * a.blk_bytes;        // the block
+            const uint32_t xb = s0 + x_row + b * (kPermK * 2);   // its x, this thread's row
+            float dlo[2][4], dhi[2][4], dx[4];
+            ZfConsts zk;
+#pragma unroll
+            for (int sc = 0; sc < kPermSteps / 4; ++sc) {
+                uint4 wv[4], xv[4];
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const int u = 4 * sc + s4;
+                    wv[s4] = lds128(sb + u * 512 + lane * 16);     // the lane's fragment
+                    const uint4 v = lds128(xb + u * 64);
+                    xv[s4] = x_ok ? v : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const int u = 4 * sc + s4;
+                    if (u % SG == 0) {
+                        // four scales then four zeros of the thread's columns
+                        const uint4 v = lds128(sb + kPermWordBytes + ((u / SG) * 8 + g) * 16);
+                        zk = make_zf_consts(make_uint2(v.z, v.w), make_uint2(v.x, v.y));
+                    }
+                    // repacked nibble order: nibbles (0,4) / (2,6) hold k (0,1) /
+                    // (4,5), nibbles (1,5) / (3,7) hold k (2,3) / (6,7)
+                    const uint32_t blo[2] = {xv[s4].x, xv[s4].z};
+                    const uint32_t bhi[2] = {xv[s4].y, xv[s4].w};
+                    if (u % SG == 0)
+                        zf_step<true>(dlo, dhi, dx, wv[s4], blo, bhi);
+                    else
+                        zf_step<false>(dlo, dhi, dx, wv[s4], blo, bhi);
+                    if (u % SG == SG - 1)
+                        zf_flush(reinterpret_cast<float (&)[1][2][4]>(acc), dlo, dhi, dx, zk);
+                }
+            }
+        }
+        // every read of the slot is done: refill it with the unit D ahead
+        if (i + a.D < n) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                issue_w(slot, tc0 + itl, ikc);
+                issue_x(slot, tc0 + itl, ikc);
+            }
+            if (++ikc == a.U) { ikc = 0; ++itl; }
+        }
+        if (++slot == a.D) {
+            slot = 0;
+            phase ^= 1;
+        }
+
+        // ------------------------------------------------ end of a tile segment
+        if (++kc == a.U || i + 1 == n) {
+            const int t_first = tl * a.U, t_last = t_first + a.U - 1;   // local units
+            const int tg = tc0 + tl, e = tg / a.T, col0 = (tg - e * a.T) * 32;
+            uint16_t *out = tab.out[e];
+            if (t_first >= ub && t_last < ue) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) {
+                        const int m = 2 * t + (k2 & 1);
+                        const int c = col0 + 4 * g + 2 * j + (k2 >> 1);
+                        if (m < a.M)
+                            out[(size_t)m * a.N + c] = __half_as_ushort(__float2half_rn(acc[j][k2]));
+                    }
+            } else {
+                float *mine = part + (warp * 2 + (tl == first_tl ? 0 : 1)) * kMaxM * 32;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) {
+                        const int m = 2 * t + (k2 & 1);
+                        if (m < kMaxM) mine[m * 32 + 4 * g + 2 * j + (k2 >> 1)] = acc[j][k2];
+                    }
+                __syncwarp();
+                const int w_lo = warp_of(t_first), w_hi = warp_of(t_last);
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence_block();
+                    last = atomicAdd(&cnt[tl], 1) == w_hi - w_lo;
+                    __threadfence_block();
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    float v[kMaxM];
+#pragma unroll
+                    for (int m = 0; m < kMaxM; ++m) v[m] = 0.f;
+                    for (int w = w_lo; w <= w_hi; ++w) {
+                        const int sel = begin_of(w) / a.U == tl ? 0 : 1;
+                        const float *src = part + (w * 2 + sel) * kMaxM * 32 + lane;
+#pragma unroll
+                        for (int m = 0; m < kMaxM; ++m) v[m] += src[m * 32];
+                    }
+#pragma unroll
+                    for (int m = 0; m < kMaxM; ++m)
+                        if (m < a.M)
+                            out[(size_t)m * a.N + col0 + lane] = __half_as_ushort(__float2half_rn(v[m]));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) acc[j][k2] = 0.f;
+            ++tl;
+            kc = 0;
+        }
+    }
+}
+
+bool perm_layout(int M, int group, int ub, PermArgs &a, int &smem);
+
+constexpr int kPermUnitBlocks = 2;
+
+// Blocks per unit: kPermUnitBlocks where two ring slots per warp still fit,
+// else fewer.
+int perm_unit_blocks(int M, int group) {
+    for (int ub = kPermUnitBlocks; ub > 1; --ub) {
+        PermArgs a;
+        int smem = 0;
+        if (perm_layout(M, group, ub, a, smem)) return ub;
+    }
+    return 1;
+}
+
+bool perm_layout(int M, int group, int ub, PermArgs &a, int &smem) {
+    const int gps = group < kPermK ? kPermK / group : 1;
+    a.UB = ub;
+    a.blk_bytes = kPermWordBytes + 128 * gps;
+    a.x_off = round_up(ub * a.blk_bytes, 128);
+    a.slot_bytes = round_up(a.x_off + M * ub * kPermK * 2, 128);
+    const int fixed = 128 + kW * 2 * kMaxM * 32 * 4 + kMaxTilesPerCta * 4 + kW * kMaxDepth * 8 + 64;
+    int d = (kBudget - fixed) / (kW * a.slot_bytes);
+    if (d > kMaxDepth) d = kMaxDepth;
+    if (d < 2) return false;
+    a.D = d;
+    a.part_off = kW * d * a.slot_bytes;
+    a.cnt_off = a.part_off + kW * 2 * kMaxM * 32 * 4;
+    a.bar_off = round_up(a.cnt_off + kMaxTilesPerCta * 4, 16);
+    smem = 128 + a.bar_off + kW * d * 8;
+    return smem <= kBudget;
+}
+
+template <int SG>
+cudaError_t launch_perm_kernel(const PermArgs &a, const PermTable &tab, int smem, bool pdl,
+                               cudaStream_t stream) {
+    auto kern = decode_warp_perm_kernel<SG>;
+    cudaError_t e = ensure_dynamic_smem((const void *)kern, kBudget);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(a.G, 1, 1);
+    lc.blockDim = dim3(32 * kW, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = &attr;
+    lc.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, kern, a, tab);
+}
+
+}  // namespace
+
+bool decode_warp_perm_supported(int M, int N, int K, int group, int experts, int ctas) {
+    if (!(M >= 1 && M <= kMaxM && experts >= 1 && experts <= kMaxExperts &&
+          repack_supported(K, N, group)))
+        return false;
+    const long long TT = (long long)experts * (N / 32);
+    const int G = grid_for((int)(TT < 0x7fffffff ? TT : 0x7fffffff), ctas);
+    if (G < 1 || (TT + G - 1) / G > kMaxTilesPerCta) return false;
+    PermArgs a;
+    int smem = 0;
+    return perm_layout(M, group, perm_unit_blocks(M, group), a, smem);
+}
+
+cudaError_t launch_decode_warp_perm(const StreamCall &call, const w4a16_config &cfg,
+                                    cudaStream_t stream) {
+    if (!decode_warp_perm_supported(call.M, call.N, call.K, call.group, call.E, cfg.ctas))
+        return cudaErrorNotSupported;
+    PermArgs a = {};
+    int smem = 0;
+    if (!perm_layout(call.M, call.group, perm_unit_blocks(call.M, call.group), a, smem))
+        return cudaErrorNotSupported;
+    a.M = call.M;
+    a.N = call.N;
+    a.K = call.K;
+    a.group = call.group;
+    a.E = call.E;
+    a.T = call.N / 32;
+    a.KB = call.K / kPermK;
+    a.U = (a.KB + a.UB - 1) / a.UB;
+    a.G = grid_for(a.E * a.T, cfg.ctas);
+    a.status = device_status_word();
+    if (!a.status) return cudaErrorInvalidDevice;
+    a.timeout_ns = 1000000000ull;
+    PermTable tab = {};
+    for (int e = 0; e < call.E; ++e) {
+        tab.x[e] = call.x[e];
+        tab.w[e] = reinterpret_cast<const uint8_t *>(call.w[e]);
+        tab.out[e] = call.out[e];
+    }
+    const bool pdl = (cfg.flags & W4A16_FLAG_PDL) != 0;
+    const int sg = call.group >= kPermK ? kPermSteps : call.group / 32;
+    switch (sg) {
+    case 1: return launch_perm_kernel<1>(a, tab, smem, pdl, stream);
+    case 2: return launch_perm_kernel<2>(a, tab, smem, pdl, stream);
+    case 4: return launch_perm_kernel<4>(a, tab, smem, pdl, stream);
+    default: return launch_perm_kernel<8>(a, tab, smem, pdl, stream);
+    }
+}
+
 }  // namespace w4a16
