@@ -398,6 +398,7 @@ cudaError_t launch_decode_warp(const GemmArgs &g, const w4a16_config &cfg, cudaS
 // units of all experts' tiles are split between the CTAs as above.
 namespace {
 
+constexpr int kPermW = 8;                   // warps per CTA
 constexpr int kPermK = 256;                 // k per repacked block
 constexpr int kPermSteps = kPermK / 32;
 constexpr int kPermWordBytes = 4096;        // the block's packed words
@@ -423,7 +424,7 @@ struct PermTable {
 
 // SG: 32-k steps per scale group inside a block (8 when a group spans it).
 template <int SG>
-__global__ void __launch_bounds__(32 * kW, 1)
+__global__ void __launch_bounds__(32 * kPermW, 1)
 decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constant__ PermTable tab)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -432,7 +433,7 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     int *cnt = reinterpret_cast<int *>(smem + a.cnt_off);
-    float *part = reinterpret_cast<float *>(smem + a.part_off);   // [kW][2][kMaxM][32]
+    float *part = reinterpret_cast<float *>(smem + a.part_off);   // [kPermW][2][kMaxM][32]
 
     pdl_launch_dependents();
     // this CTA's tiles (over all experts: tile = expert * T + strip) and the
@@ -441,7 +442,7 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
     const int tc0 = (int)((long long)TT * blockIdx.x / a.G);
     const int tc1 = (int)((long long)TT * (blockIdx.x + 1) / a.G);
     const int ucta = (tc1 - tc0) * a.U;
-    const int weff = ucta < kW ? ucta : kW;
+    const int weff = ucta < kPermW ? ucta : kPermW;
     const int q = ucta / weff, r = ucta - q * weff;
     auto begin_of = [&](int w) { return w * q + (w < r ? w : r); };
     auto warp_of = [&](int u) {
@@ -648,15 +649,15 @@ bool perm_layout(int M, int group, int ub, PermArgs &a, int &smem) {
     a.blk_bytes = kPermWordBytes + 128 * gps;
     a.x_off = round_up(ub * a.blk_bytes, 128);
     a.slot_bytes = round_up(a.x_off + M * ub * kPermK * 2, 128);
-    const int fixed = 128 + kW * 2 * kMaxM * 32 * 4 + kMaxTilesPerCta * 4 + kW * kMaxDepth * 8 + 64;
-    int d = (kBudget - fixed) / (kW * a.slot_bytes);
+    const int fixed = 128 + kPermW * 2 * kMaxM * 32 * 4 + kMaxTilesPerCta * 4 + kPermW * kMaxDepth * 8 + 64;
+    int d = (kBudget - fixed) / (kPermW * a.slot_bytes);
     if (d > kMaxDepth) d = kMaxDepth;
     if (d < 2) return false;
     a.D = d;
-    a.part_off = kW * d * a.slot_bytes;
-    a.cnt_off = a.part_off + kW * 2 * kMaxM * 32 * 4;
+    a.part_off = kPermW * d * a.slot_bytes;
+    a.cnt_off = a.part_off + kPermW * 2 * kMaxM * 32 * 4;
     a.bar_off = round_up(a.cnt_off + kMaxTilesPerCta * 4, 16);
-    smem = 128 + a.bar_off + kW * d * 8;
+    smem = 128 + a.bar_off + kPermW * d * 8;
     return smem <= kBudget;
 }
 
@@ -668,7 +669,7 @@ cudaError_t launch_perm_kernel(const PermArgs &a, const PermTable &tab, int smem
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(a.G, 1, 1);
-    lc.blockDim = dim3(32 * kW, 1, 1);
+    lc.blockDim = dim3(32 * kPermW, 1, 1);
     lc.dynamicSmemBytes = smem;
     lc.stream = stream;
     cudaLaunchAttribute attr;
