@@ -320,7 +320,7 @@ W4A16_API w4a16_status w4a16_repack(const uint32_t *packed, const uint16_t *scal
 /*
  * out[M,N] = x[M,K] . W, with W given in the repacked form, reading one
  * contiguous block per strip and 256-k stage with one bulk copy.  Two kernels:
- *   W4A16_DECODE_WARP    M <= 4: every warp streams its own run of blocks
+ *   W4A16_DECODE_WARP    M <= 8: every warp streams its own run of blocks
  *                        through a private ring (the design of the natural-
  *                        layout warp-stream kernel); at most 64 32-column
  *                        tiles per CTA (over all experts of a grouped call).
@@ -341,7 +341,7 @@ W4A16_API w4a16_status w4a16_gemm_repacked(const uint16_t *x, const void *repack
                                  cudaStream_t stream);
 
 /* Grouped form of w4a16_gemm_repacked: E <= W4A16_MAX_EXPERTS experts of one
- * shape in one launch, M <= 16 (the warp kernel at M <= 4, as above); host
+ * shape in one launch, M <= 16 (the warp kernel at M <= 8, as above); host
  * arrays of E device pointers as in w4a16_gemm_grouped. */
 W4A16_API w4a16_status w4a16_gemm_grouped_repacked(int E, const uint16_t *const *x,
                                          const void *const *repacked, uint16_t *const *out,

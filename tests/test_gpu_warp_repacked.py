@@ -1,6 +1,6 @@
 """Parity of the warp-stream decode kernel on repacked weights
 (w4a16_gemm_repacked / w4a16_gemm_grouped_repacked with W4A16_DECODE_WARP,
-M <= 4) with the fp64 oracle: the decode workload shapes, every repacked group
+M <= 8) with the fp64 oracle: the decode workload shapes, every repacked group
 size, grid sizes that give different runs per warp and split tiles, grouped
 calls over many experts, one-hot exactness, dirty outputs, PDL chains and
 run-to-run determinism; requests it cannot serve are refused."""
@@ -50,7 +50,7 @@ def check(out, x, ref_w, group, what):
     assert err <= TOL, "rel err %.3g > %g (%s)" % (err, TOL, what)
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("K,N,outliers", [
     (256, 32, False), (512, 256, False), (4096, 4096, False), (2048, 768, False),
     (768, 2048, False), (4096, 14336, True), (14336, 4096, True),
@@ -69,7 +69,7 @@ def test_warp_repacked_decode_configs(K, N, outliers, M):
 
 
 @pytest.mark.parametrize("group", [32, 64, 256, 512, 1024])
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 8])
 def test_warp_repacked_groups(group, M):
     K, N = 2048, 384
     rep, ref_w = repacked(K, N, group, 31 + group, True)
@@ -79,7 +79,7 @@ def test_warp_repacked_groups(group, M):
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7, 19, 152, 300])
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 7])
 def test_warp_repacked_grid_sizes(ctas, M):
     """Different grids give different tiles per CTA, runs per warp and split
     tiles (a run of blocks may cross a tile and a tile's blocks may be split
@@ -96,7 +96,7 @@ def test_warp_repacked_grid_sizes(ctas, M):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("M", [1, 2, 4])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_warp_repacked_one_hot_is_exact(M):
     K, N = 1024, 768
     W = synth.weight(K, N, seed=61, outliers=True)
@@ -121,7 +121,7 @@ def expert_set(E, K, N, group, seed):
     return reps, refs
 
 
-@pytest.mark.parametrize("E,M", [(64, 1), (64, 4), (3, 3), (1, 2)])
+@pytest.mark.parametrize("E,M", [(64, 1), (64, 4), (64, 8), (3, 3), (5, 6), (1, 2)])
 @pytest.mark.parametrize("K,N", [(2048, 768), (768, 2048)])
 def test_warp_repacked_grouped(E, M, K, N):
     """Tiles of all experts are split between the CTAs in one launch; every
@@ -145,12 +145,12 @@ def test_warp_repacked_grouped(E, M, K, N):
 def test_warp_repacked_dirty_output_zero_input_and_chains():
     K, N = 4096, 2048
     rep, ref_w = repacked(K, N, 128, 331, False)
-    x = to_dev(synth.activations(4, K, seed=332))
-    out = torch.full((4, N), 5.0, dtype=torch.float16, device=DEV)
+    x = to_dev(synth.activations(8, K, seed=332))
+    out = torch.full((8, N), 5.0, dtype=torch.float16, device=DEV)
     w4.gemm_repacked(torch.zeros_like(x), rep, N, group=128, out=out, config=WARP)
     torch.cuda.synchronize()
     assert torch.all(out.view(torch.int16) == 0)
-    outs = [torch.full((4, N), 9.0, dtype=torch.float16, device=DEV) for _ in range(6)]
+    outs = [torch.full((8, N), 9.0, dtype=torch.float16, device=DEV) for _ in range(6)]
     for o in outs:
         w4.gemm_repacked(x, rep, N, group=128, out=o, config=dict(WARP, pdl=True))
     torch.cuda.synchronize()
@@ -164,15 +164,15 @@ def test_warp_repacked_dirty_output_zero_input_and_chains():
 def test_warp_repacked_refusals():
     K, N = 1024, 4096
     rep, _ = repacked(K, N, 128, 341, False)
-    x5 = to_dev(synth.activations(5, K, seed=342))
-    with pytest.raises(w4.W4A16Error) as e:              # M > 4
-        w4.gemm_repacked(x5, rep, N, group=128, config=WARP)
+    x9 = to_dev(synth.activations(9, K, seed=342))
+    with pytest.raises(w4.W4A16Error) as e:              # M > 8
+        w4.gemm_repacked(x9, rep, N, group=128, config=WARP)
     assert e.value.status == 2
     x1 = to_dev(synth.activations(1, K, seed=343))
     with pytest.raises(w4.W4A16Error) as e:              # 128 tiles on one CTA
         w4.gemm_repacked(x1, rep, N, group=128, config=dict(WARP, ctas=1))
     assert e.value.status == 2
-    # the default request at M = 5 takes the stream kernel and still answers
-    out = w4.gemm_repacked(x5, rep, N, group=128)
+    # the default request at M = 9 takes the stream kernel and still answers
+    out = w4.gemm_repacked(x9, rep, N, group=128)
     torch.cuda.synchronize()
-    assert w4.kernel_status() == 0 and out.shape == (5, N)
+    assert w4.kernel_status() == 0 and out.shape == (9, N)

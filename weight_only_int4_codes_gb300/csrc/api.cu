@@ -770,16 +770,16 @@ w4a16_status plan_repacked(int M, int N, int K, int group, int experts, const w4
     if (c.dtype != W4A16_DTYPE_F16)
         return fail(W4A16_ERR_UNSUPPORTED, "repacked weights: fp16 only");
     c.path = W4A16_PATH_DECODE;
-    // the warp-stream kernel serves M <= 4 (every row in one launch); the
+    // the warp-stream kernel serves M <= 8 (every row in one launch); the
     // stream kernel the rest.  By default the warp kernel takes calls of at
     // least four 256-k blocks per SM: below that too few warps have work, and
     // the stream kernel (more CTAs per tile) was measured faster
-    const bool warp_ok = M <= 4 && decode_warp_perm_supported(M > 0 ? M : 1, N, K, group,
+    const bool warp_ok = M <= 8 && decode_warp_perm_supported(M > 0 ? M : 1, N, K, group,
                                                               experts, c.ctas);
     const long long blocks = (long long)experts * (N / 32) * (K / 256);
     if (c.variant == W4A16_DECODE_WARP) {
         if (!warp_ok)
-            return fail(W4A16_ERR_UNSUPPORTED, "repacked warp-stream kernel: M <= 4 and at "
+            return fail(W4A16_ERR_UNSUPPORTED, "repacked warp-stream kernel: M <= 8 and at "
                         "most 64 tiles per CTA (M=%d N=%d K=%d group=%d E=%d ctas=%d)",
                         M, N, K, group, experts, c.ctas);
         return W4A16_OK;

@@ -102,7 +102,7 @@ cudaError_t launch_decode_tma(const GemmArgs &a, const w4a16_config &cfg, cudaSt
 bool decode_warp_supported(int M, int N, int K, int group, int ctas);
 cudaError_t launch_decode_warp(const GemmArgs &a, const w4a16_config &cfg, cudaStream_t stream);
 // The same design on repacked blocks (one bulk copy per unit), for one or up
-// to kMaxExperts GEMMs of one shape (M <= 4).
+// to kMaxExperts GEMMs of one shape (M <= 8).
 bool decode_warp_perm_supported(int M, int N, int K, int group, int experts, int ctas);
 struct StreamCall;
 cudaError_t launch_decode_warp_perm(const StreamCall &call, const w4a16_config &cfg,

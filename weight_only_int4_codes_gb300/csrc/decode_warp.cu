@@ -399,6 +399,7 @@ cudaError_t launch_decode_warp(const GemmArgs &g, const w4a16_config &cfg, cudaS
 namespace {
 
 constexpr int kPermW = 8;                   // warps per CTA
+constexpr int kPermMaxM = 8;                // rows of x: the MMA's 8 batch columns
 constexpr int kPermK = 256;                 // k per repacked block
 constexpr int kPermSteps = kPermK / 32;
 constexpr int kPermWordBytes = 4096;        // the block's packed words
@@ -433,7 +434,7 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     int *cnt = reinterpret_cast<int *>(smem + a.cnt_off);
-    float *part = reinterpret_cast<float *>(smem + a.part_off);   // [kPermW][2][kMaxM][32]
+    float *part = reinterpret_cast<float *>(smem + a.part_off);   // [kPermW][2][M][32]
 
     pdl_launch_dependents();
     // this CTA's tiles (over all experts: tile = expert * T + strip) and the
@@ -585,13 +586,13 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
                             out[(size_t)m * a.N + c] = __half_as_ushort(__float2half_rn(acc[j][k2]));
                     }
             } else {
-                float *mine = part + (warp * 2 + (tl == first_tl ? 0 : 1)) * kMaxM * 32;
+                float *mine = part + (warp * 2 + (tl == first_tl ? 0 : 1)) * a.M * 32;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int k2 = 0; k2 < 4; ++k2) {
                         const int m = 2 * t + (k2 & 1);
-                        if (m < kMaxM) mine[m * 32 + 4 * g + 2 * j + (k2 >> 1)] = acc[j][k2];
+                        if (m < a.M) mine[m * 32 + 4 * g + 2 * j + (k2 >> 1)] = acc[j][k2];
                     }
                 __syncwarp();
                 const int w_lo = warp_of(t_first), w_hi = warp_of(t_last);
@@ -603,17 +604,18 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
                 }
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
-                    float v[kMaxM];
+                    float v[kPermMaxM];
 #pragma unroll
-                    for (int m = 0; m < kMaxM; ++m) v[m] = 0.f;
+                    for (int m = 0; m < kPermMaxM; ++m) v[m] = 0.f;
                     for (int w = w_lo; w <= w_hi; ++w) {
                         const int sel = begin_of(w) / a.U == tl ? 0 : 1;
-                        const float *src = part + (w * 2 + sel) * kMaxM * 32 + lane;
+                        const float *src = part + (w * 2 + sel) * a.M * 32 + lane;
 #pragma unroll
-                        for (int m = 0; m < kMaxM; ++m) v[m] += src[m * 32];
+                        for (int m = 0; m < kPermMaxM; ++m)
+                            if (m < a.M) v[m] += src[m * 32];
                     }
 #pragma unroll
-                    for (int m = 0; m < kMaxM; ++m)
+                    for (int m = 0; m < kPermMaxM; ++m)
                         if (m < a.M)
                             out[(size_t)m * a.N + col0 + lane] = __half_as_ushort(__float2half_rn(v[m]));
                 }
@@ -628,37 +630,30 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
     }
 }
 
-bool perm_layout(int M, int group, int ub, PermArgs &a, int &smem);
-
-constexpr int kPermUnitBlocks = 2;
-
-// Blocks per unit: kPermUnitBlocks where two ring slots per warp still fit,
-// else fewer.
-int perm_unit_blocks(int M, int group) {
-    for (int ub = kPermUnitBlocks; ub > 1; --ub) {
-        PermArgs a;
-        int smem = 0;
-        if (perm_layout(M, group, ub, a, smem)) return ub;
-    }
-    return 1;
-}
-
 bool perm_layout(int M, int group, int ub, PermArgs &a, int &smem) {
+    const int w = kPermW;
     const int gps = group < kPermK ? kPermK / group : 1;
     a.UB = ub;
     a.blk_bytes = kPermWordBytes + 128 * gps;
     a.x_off = round_up(ub * a.blk_bytes, 128);
     a.slot_bytes = round_up(a.x_off + M * ub * kPermK * 2, 128);
-    const int fixed = 128 + kPermW * 2 * kMaxM * 32 * 4 + kMaxTilesPerCta * 4 + kPermW * kMaxDepth * 8 + 64;
-    int d = (kBudget - fixed) / (kPermW * a.slot_bytes);
+    const int fixed = 128 + w * 2 * M * 32 * 4 + kMaxTilesPerCta * 4 + w * kMaxDepth * 8 + 64;
+    int d = (kBudget - fixed) / (w * a.slot_bytes);
     if (d > kMaxDepth) d = kMaxDepth;
     if (d < 2) return false;
     a.D = d;
-    a.part_off = kPermW * d * a.slot_bytes;
-    a.cnt_off = a.part_off + kPermW * 2 * kMaxM * 32 * 4;
+    a.part_off = w * d * a.slot_bytes;
+    a.cnt_off = a.part_off + w * 2 * M * 32 * 4;
     a.bar_off = round_up(a.cnt_off + kMaxTilesPerCta * 4, 16);
-    smem = 128 + a.bar_off + kPermW * d * 8;
+    smem = 128 + a.bar_off + w * d * 8;
     return smem <= kBudget;
+}
+
+// Units of two blocks where two ring slots per warp fit (M <= 4 at group 128),
+// else single blocks.  (Six warps with units of two blocks at M = 5..8 were
+// measured: faster on some shapes, slower on others, the same on average.)
+bool perm_shape(int M, int group, PermArgs &a, int &smem) {
+    return perm_layout(M, group, 2, a, smem) || perm_layout(M, group, 1, a, smem);
 }
 
 template <int SG>
@@ -683,7 +678,7 @@ cudaError_t launch_perm_kernel(const PermArgs &a, const PermTable &tab, int smem
 }  // namespace
 
 bool decode_warp_perm_supported(int M, int N, int K, int group, int experts, int ctas) {
-    if (!(M >= 1 && M <= kMaxM && experts >= 1 && experts <= kMaxExperts &&
+    if (!(M >= 1 && M <= kPermMaxM && experts >= 1 && experts <= kMaxExperts &&
           repack_supported(K, N, group)))
         return false;
     const long long TT = (long long)experts * (N / 32);
@@ -691,7 +686,7 @@ bool decode_warp_perm_supported(int M, int N, int K, int group, int experts, int
     if (G < 1 || (TT + G - 1) / G > kMaxTilesPerCta) return false;
     PermArgs a;
     int smem = 0;
-    return perm_layout(M, group, perm_unit_blocks(M, group), a, smem);
+    return perm_shape(M, group, a, smem);
 }
 
 cudaError_t launch_decode_warp_perm(const StreamCall &call, const w4a16_config &cfg,
@@ -700,8 +695,7 @@ cudaError_t launch_decode_warp_perm(const StreamCall &call, const w4a16_config &
         return cudaErrorNotSupported;
     PermArgs a = {};
     int smem = 0;
-    if (!perm_layout(call.M, call.group, perm_unit_blocks(call.M, call.group), a, smem))
-        return cudaErrorNotSupported;
+    if (!perm_shape(call.M, call.group, a, smem)) return cudaErrorNotSupported;
     a.M = call.M;
     a.N = call.N;
     a.K = call.K;
