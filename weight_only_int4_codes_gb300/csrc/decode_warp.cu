@@ -423,8 +423,9 @@ struct PermTable {
     uint16_t *out[kMaxExperts];
 };
 
-// SG: 32-k steps per scale group inside a block (8 when a group spans it).
-template <int SG>
+// SG: 32-k steps per scale group inside a block (8 when a group spans it);
+// MAXM: 4 or 8, the rows of x the partial sums are laid out for (M <= MAXM).
+template <int SG, int MAXM>
 __global__ void __launch_bounds__(32 * kPermW, 1)
 decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constant__ PermTable tab)
 {
@@ -434,7 +435,7 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     int *cnt = reinterpret_cast<int *>(smem + a.cnt_off);
-    float *part = reinterpret_cast<float *>(smem + a.part_off);   // [kPermW][2][M][32]
+    float *part = reinterpret_cast<float *>(smem + a.part_off);   // [kPermW][2][MAXM][32]
 
     pdl_launch_dependents();
     // this CTA's tiles (over all experts: tile = expert * T + strip) and the
@@ -586,13 +587,13 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
                             out[(size_t)m * a.N + c] = __half_as_ushort(__float2half_rn(acc[j][k2]));
                     }
             } else {
-                float *mine = part + (warp * 2 + (tl == first_tl ? 0 : 1)) * a.M * 32;
+                float *mine = part + (warp * 2 + (tl == first_tl ? 0 : 1)) * MAXM * 32;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int k2 = 0; k2 < 4; ++k2) {
                         const int m = 2 * t + (k2 & 1);
-                        if (m < a.M) mine[m * 32 + 4 * g + 2 * j + (k2 >> 1)] = acc[j][k2];
+                        if (m < MAXM) mine[m * 32 + 4 * g + 2 * j + (k2 >> 1)] = acc[j][k2];
                     }
                 __syncwarp();
                 const int w_lo = warp_of(t_first), w_hi = warp_of(t_last);
@@ -604,18 +605,18 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
                 }
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
-                    float v[kPermMaxM];
+                    // rows M..MAXM-1 hold zeros (their x rows are zero)
+                    float v[MAXM];
 #pragma unroll
-                    for (int m = 0; m < kPermMaxM; ++m) v[m] = 0.f;
+                    for (int m = 0; m < MAXM; ++m) v[m] = 0.f;
                     for (int w = w_lo; w <= w_hi; ++w) {
                         const int sel = begin_of(w) / a.U == tl ? 0 : 1;
-                        const float *src = part + (w * 2 + sel) * a.M * 32 + lane;
+                        const float *src = part + (w * 2 + sel) * MAXM * 32 + lane;
 #pragma unroll
-                        for (int m = 0; m < kPermMaxM; ++m)
-                            if (m < a.M) v[m] += src[m * 32];
+                        for (int m = 0; m < MAXM; ++m) v[m] += src[m * 32];
                     }
 #pragma unroll
-                    for (int m = 0; m < kPermMaxM; ++m)
+                    for (int m = 0; m < MAXM; ++m)
                         if (m < a.M)
                             out[(size_t)m * a.N + col0 + lane] = __half_as_ushort(__float2half_rn(v[m]));
                 }
@@ -630,20 +631,22 @@ decode_warp_perm_kernel(const __grid_constant__ PermArgs a, const __grid_constan
     }
 }
 
+int perm_max_m(int M) { return M <= 4 ? 4 : kPermMaxM; }
+
 bool perm_layout(int M, int group, int ub, PermArgs &a, int &smem) {
-    const int w = kPermW;
+    const int w = kPermW, maxm = perm_max_m(M);
     const int gps = group < kPermK ? kPermK / group : 1;
     a.UB = ub;
     a.blk_bytes = kPermWordBytes + 128 * gps;
     a.x_off = round_up(ub * a.blk_bytes, 128);
     a.slot_bytes = round_up(a.x_off + M * ub * kPermK * 2, 128);
-    const int fixed = 128 + w * 2 * M * 32 * 4 + kMaxTilesPerCta * 4 + w * kMaxDepth * 8 + 64;
+    const int fixed = 128 + w * 2 * maxm * 32 * 4 + kMaxTilesPerCta * 4 + w * kMaxDepth * 8 + 64;
     int d = (kBudget - fixed) / (w * a.slot_bytes);
     if (d > kMaxDepth) d = kMaxDepth;
     if (d < 2) return false;
     a.D = d;
     a.part_off = w * d * a.slot_bytes;
-    a.cnt_off = a.part_off + w * 2 * M * 32 * 4;
+    a.cnt_off = a.part_off + w * 2 * maxm * 32 * 4;
     a.bar_off = round_up(a.cnt_off + kMaxTilesPerCta * 4, 16);
     smem = 128 + a.bar_off + w * d * 8;
     return smem <= kBudget;
@@ -659,7 +662,8 @@ bool perm_shape(int M, int group, PermArgs &a, int &smem) {
 template <int SG>
 cudaError_t launch_perm_kernel(const PermArgs &a, const PermTable &tab, int smem, bool pdl,
                                cudaStream_t stream) {
-    auto kern = decode_warp_perm_kernel<SG>;
+    auto kern = perm_max_m(a.M) == 4 ? decode_warp_perm_kernel<SG, 4>
+                                     : decode_warp_perm_kernel<SG, kPermMaxM>;
     cudaError_t e = ensure_dynamic_smem((const void *)kern, kBudget);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t lc = {};
