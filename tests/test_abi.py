@@ -152,8 +152,8 @@ def test_auto_path_small_m_is_decode():
         p = w4.plan(M, 4096, 4096)
         assert p["path"] == 1 and p["variant"] in (1, 2, 4)
     # measured dispatch table rows
-    assert w4.plan(1, 4096, 4096)["variant"] == 4         # warp-stream variant at M <= 4
-    assert w4.plan(4, 4096, 4096)["variant"] == 4
+    assert w4.plan(1, 4096, 4096)["variant"] == 1         # TMA variant at M <= 2
+    assert w4.plan(4, 4096, 4096)["variant"] == 4         # warp-stream variant at M = 3..4
     assert w4.plan(8, 4096, 4096)["variant"] == 2         # registers variant at M = 8
     assert w4.plan(16, 4096, 4096)["variant"] == 2         # registers variant at M = 16
     t = w4.plan(4, 14336, 4096)

@@ -199,23 +199,24 @@ void plan_decode_stream(int M, int N, int K, int group, int experts, bool perm, 
 
 // Measured dispatch table (GB300, group 128, one call per distinct weight copy
 // in a CUDA graph with programmatic dependent launch): the fastest decode
-// configuration for the projection shapes of the benchmark workloads.  The
-// warp-stream row (4096 x 4096, M <= 4) was 2-6% ahead of the TMA variant in
-// interleaved runs of both in one process.
+// configuration for the projection shapes of the benchmark workloads (the TMA
+// variant with the zero-free step at M <= 8).  Interleaved runs in one process
+// decided the close rows: 4096 x 4096 takes the TMA variant at M <= 2 (1-2%
+// ahead) and the warp-stream variant at M = 3..4 (2% ahead).
 struct TableEntry {
     int K, N, m_max;        // shape and the largest M the row covers
     w4a16_config cfg;
 };
 constexpr TableEntry kDecodeTable[] = {
     // K      N      M<=   path split warps_k warps_n steps tile flags variant
+    {4096, 4096, 2, {1, 8, 4, 2, 2, 0, 0, W4A16_DECODE_TMA}},
     {4096, 4096, 4, {1, 0, 0, 0, 0, 0, 0, W4A16_DECODE_WARP}},
     {4096, 4096, 8, {1, 2, 8, 1, 8, 0, 0, W4A16_DECODE_REGISTERS}},
     {4096, 4096, 16, {1, 1, 8, 1, 16, 0, 0, W4A16_DECODE_REGISTERS}},
     {4096, 14336, 16, {1, 2, 4, 2, 8, 0, 0, W4A16_DECODE_TMA}},
     {14336, 4096, 8, {1, 8, 8, 4, 7, 0, 0, W4A16_DECODE_TMA}},
     {14336, 4096, 16, {1, 6, 4, 2, 10, 0, 0, W4A16_DECODE_TMA}},
-    {2048, 768, 2, {1, 8, 8, 2, 1, 0, 0, W4A16_DECODE_TMA}},
-    {2048, 768, 8, {1, 8, 2, 2, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+    {2048, 768, 8, {1, 4, 4, 2, 4, 0, 0, W4A16_DECODE_REGISTERS}},
     {2048, 768, 16, {1, 4, 4, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
     {768, 2048, 16, {1, 1, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
 };

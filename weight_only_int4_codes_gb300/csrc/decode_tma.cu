@@ -35,6 +35,8 @@ namespace w4a16 {
 
 namespace {
 
+constexpr bool kTmaZeroFree = true;   // M <= 8: decode_math.cuh's zero-free step
+
 constexpr int kStageRows = 32;                 // packed rows per stage
 constexpr int kStageK = 8 * kStageRows;        // 256 k per stage
 // ring + slots per CTA: about half an SM with 8 or 16 consumer warps, about a
@@ -255,6 +257,28 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
                     for (int p = 0; p < NT; ++p) x_fragments(xv[p][u], bx[p]);
                     step_mma_bf16<NT>(accb, wv[u], kb, bx);
                 }
+            } else if constexpr (NT == 1 && kTmaZeroFree) {
+                // M <= 8: the zero-free step (codes as fp16 subnormals, the
+                // zero removed per group through the x sums)
+                float dlo[2][4], dhi[2][4], dx[4];
+                ZfConsts zk = make_zf_consts(zraw[0], sraw[0]);
+#pragma unroll
+                for (int u = 0; u < SPW; ++u) {
+                    if (!ONE_GROUP && u > 0) zk = make_zf_consts(zraw[u], sraw[u]);
+                    uint32_t blo[2], bhi[2];
+                    blo[0] = __byte_perm(xv[0][u].x, xv[0][u].z, 0x5410);   // (x0, x4)
+                    blo[1] = __byte_perm(xv[0][u].y, xv[0][u].w, 0x5410);   // (x2, x6)
+                    bhi[0] = __byte_perm(xv[0][u].x, xv[0][u].z, 0x7632);   // (x1, x5)
+                    bhi[1] = __byte_perm(xv[0][u].y, xv[0][u].w, 0x7632);   // (x3, x7)
+                    if (!ONE_GROUP || u == 0)
+                        zf_step<true>(dlo, dhi, dx, wv[u], blo, bhi);
+                    else
+                        zf_step<false>(dlo, dhi, dx, wv[u], blo, bhi);
+                    if (!ONE_GROUP)
+                        zf_flush(reinterpret_cast<float (&)[1][2][4]>(acc), dlo, dhi, dx, zk);
+                }
+                if (ONE_GROUP)
+                    zf_flush(reinterpret_cast<float (&)[1][2][4]>(acc), dlo, dhi, dx, zk);
             } else {
             GroupConsts k = make_group_consts(zraw[0], sraw[0]);
             // one group per warp-stage: the warp's steps accumulate together
