@@ -44,6 +44,8 @@ namespace cg = cooperative_groups;
 namespace w4a16 {
 namespace {
 
+constexpr bool kRegZeroFree = true;   // M <= 8: decode_math.cuh's zero-free step
+
 struct DecodeArgs {
     const uint16_t *x;
     const uint32_t *packed;
@@ -141,6 +143,24 @@ __device__ __forceinline__ void compute_batch(float (&acc)[NT][2][4], float (&ac
             for (int p = 0; p < NT; ++p) x_fragments(xr[p][u], bx[p]);
             step_mma_bf16<NT>(accb, b.w[u], k, bx);
         }
+    } else if constexpr (NT == 1 && kRegZeroFree) {
+        // M <= 8: the zero-free step (codes as fp16 subnormals, the zero
+        // removed per group through the x sums)
+        const ZfConsts zk = make_zf_consts(b.z, b.s);
+        float dlo[2][4], dhi[2][4], dx[4];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint32_t blo[2], bhi[2];
+            blo[0] = __byte_perm(xr[0][u].x, xr[0][u].z, 0x5410);   // (x0, x4)
+            blo[1] = __byte_perm(xr[0][u].y, xr[0][u].w, 0x5410);   // (x2, x6)
+            bhi[0] = __byte_perm(xr[0][u].x, xr[0][u].z, 0x7632);   // (x1, x5)
+            bhi[1] = __byte_perm(xr[0][u].y, xr[0][u].w, 0x7632);   // (x3, x7)
+            if (u == 0)
+                zf_step<true>(dlo, dhi, dx, b.w[u], blo, bhi);
+            else
+                zf_step<false>(dlo, dhi, dx, b.w[u], blo, bhi);
+        }
+        zf_flush(acc, dlo, dhi, dx, zk);
     } else {
         const GroupConsts k = make_group_consts(b.z, b.s);
         float gacc[NT][2][2][4];
