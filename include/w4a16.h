@@ -94,9 +94,9 @@ typedef enum w4a16_path {
                                      contiguous run of (column tile, stage) units
                                      through a ring of bulk copies */
 #define W4A16_DECODE_WARP 4       /* every warp streams its own run of 32-column x
-                                     128-k units through a private TMA ring; no
-                                     barrier between warps (N % 8 == 0, power-of-two
-                                     groups 32..1024) */
+                                     512-k units through a private TMA ring; no
+                                     barrier between warps (M <= 4, N % 8 == 0,
+                                     power-of-two groups 32..1024) */
 
 /* Prefill kernel variants (w4a16_config.variant on the prefill path). */
 #define W4A16_PREFILL_A_TMEM 1    /* dequantized W^T operand in tensor memory (default) */
