@@ -56,7 +56,7 @@ extern "C" {
 typedef enum w4a16_status {
     W4A16_OK = 0,
     W4A16_ERR_INVALID_ARG = 1,   /* bad shape, group or null pointer */
-    W4A16_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+    W4A16_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement */
     W4A16_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
     W4A16_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
     W4A16_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (see

@@ -55,7 +55,7 @@ def test_version(lib):
 @pytest.mark.parametrize("M,N,K,group,status", [
     (1, 4096, 4000, 128, 1),    # K not a multiple of group
     (1, 4096, 4096, 100, 1),    # group not a multiple of 8
-    (1, 4096, 4096, 8, 2),      # valid format, group below this build's minimum
+    (1, 4096, 4096, 8, 2),      # valid format, group below the library's minimum
     (1, 4094, 4096, 128, 3),    # N % 4 != 0
     (-1, 4096, 4096, 128, 1),   # negative size
     (1, 4096, 0, 128, 1),       # K == 0
