@@ -449,6 +449,29 @@ def test_zero_input_and_dirty_output_and_determinism():
     assert ((out2.float() - 2 * first.float()).abs() <= 2.0 ** -24)[~normal].all()
 
 
+@pytest.mark.parametrize("cfg", [
+    dict(path="decode", variant="registers", split_k=4, warps_k=4, warps_n=2),
+    dict(path="decode", variant="registers", split_k=7, warps_k=8, warps_n=1, steps=4),
+    dict(path="decode", variant="tma", warps_n=4, split_k=8),
+    dict(path="decode", variant="tma", warps_n=2, split_k=3),
+], ids=lambda c: "-".join("%s%s" % (k, v) for k, v in c.items()))
+def test_split_sums_are_reproducible(cfg):
+    """The cluster's partials are summed in rank order whatever the arrival
+    order: repeated calls (chained with PDL) give the same bits."""
+    K, N, M = 4096, 2048, 5
+    W = synth.weight(K, N, seed=91)
+    dev_w, ref_w = quantize_both(W, 128)
+    x = to_dev(synth.activations(M, K, seed=92))
+    outs = [torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV) for _ in range(6)]
+    for o in outs:
+        w4.gemm_ex(x, *dev_w, group=128, out=o, config=dict(cfg, pdl=True))
+    torch.cuda.synchronize()
+    assert w4.kernel_status() == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert oracle.rel_err(outs[0].cpu().numpy(), oracle.gemm(x.cpu().numpy(), *ref_w)) <= TOL
+
+
 def test_matches_cublas_on_dequantized_weight():
     """A library cross-check: cuBLAS fp16 on the dequantized weight agrees with
     both the oracle and the fused kernel within the tolerance."""

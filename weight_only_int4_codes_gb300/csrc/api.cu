@@ -216,7 +216,7 @@ constexpr TableEntry kDecodeTable[] = {
     {4096, 14336, 16, {1, 2, 4, 2, 8, 0, 0, W4A16_DECODE_TMA}},
     {14336, 4096, 8, {1, 8, 8, 4, 7, 0, 0, W4A16_DECODE_TMA}},
     {14336, 4096, 16, {1, 6, 4, 2, 10, 0, 0, W4A16_DECODE_TMA}},
-    {2048, 768, 8, {1, 4, 4, 2, 4, 0, 0, W4A16_DECODE_REGISTERS}},
+    {2048, 768, 4, {1, 4, 4, 2, 4, 0, 0, W4A16_DECODE_REGISTERS}},
     {2048, 768, 16, {1, 4, 4, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
     {768, 2048, 16, {1, 1, 8, 1, 4, 0, 0, W4A16_DECODE_REGISTERS}},
 };

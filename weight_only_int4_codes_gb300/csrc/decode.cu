@@ -28,18 +28,17 @@
 //   * Split-K: a column tile's K range is split across the warps of a CTA and
 //     across the CTAs of one thread-block cluster.  Partials are reduced in a
 //     FIXED order: warps through shared memory, then CTAs through distributed
-//     shared memory after a cluster barrier.  No atomics, no global workspace,
-//     no spin-waits, bitwise reproducible.  (The pages merge split-K partials
+//     shared memory -- every CTA finalizes a slice of the tile, its peers push
+//     their partials of that slice into its shared memory, one cluster barrier.
+//     No atomics, no global workspace, no spin-waits, bitwise reproducible.  (The pages merge split-K partials
 //     with fp32 atomics; the second page names a second-stage reduction as the
 //     alternative, which this is.)
-#include <cooperative_groups.h>
 #include <map>
 #include <mutex>
 
 #include "common.cuh"
 #include "decode_math.cuh"
-
-namespace cg = cooperative_groups;
+#include "sm100_ptx.cuh"
 
 namespace w4a16 {
 namespace {
@@ -198,7 +197,7 @@ struct ExpertTable {
 
 // One CTA's share of one GEMM: column tile blockIdx.x, K slice blockIdx.y,
 // 16-row chunk `mchunk` of x.  BF: x, scales, zeros and out are bfloat16.
-// Block: 32*WN*WK threads; dynamic shared memory (WK + 1) * 16 * 32*WN floats.
+// Block: 32*WN*WK threads; dynamic shared memory (WK + 1) * 16 * 32*WN + 8 floats.
 template <int NT, int WN, int WK, int U, bool BF>
 __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands &o, int mchunk)
 {
@@ -212,6 +211,9 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
     const int col0 = blockIdx.x * BN + wn * 32 + 4 * g;
     const bool col_ok = col0 < a.N;                 // N % 4 == 0: all 4 columns valid
     const int KB = a.K >> 3;                        // packed rows
+    // first half of a split cluster barrier: once every CTA has arrived, each
+    // one's shared memory exists and may receive its peers' partials
+    if (a.split > 1) cluster_arrive();
     const int row0 = blockIdx.y * a.rows_per_cta + wk * a.steps * 4;
     // warp-uniform trip count (independent of col_ok)
     const int nsteps = max(0, min(a.steps, (KB - row0) >> 2));
@@ -279,7 +281,6 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
 
     // ---- reduction 1: the WK warps of this CTA, through shared memory
     float *red = smem;                    // [WK][16][BN]
-    float *part = smem + WK * 16 * BN;    // [16][BN] this CTA's partial
 #pragma unroll
     for (int p = 0; p < NT; ++p)
 #pragma unroll
@@ -292,37 +293,45 @@ __device__ __forceinline__ void decode_tile(const DecodeArgs &a, const Operands 
             }
     __syncthreads();
     const int E = Mc * BN;
+    if (a.split > 1) {
+        // ---- reduction 2: every CTA pushes its partial of output e into the
+        // slot [rank][e - q*per] of the CTA q that finalizes e; one cluster
+        // barrier; each CTA sums its slots in rank order (fixed: bitwise
+        // reproducible).  No CTA reads another's shared memory.
+        const int rank = (int)cluster_ctarank();
+        const int per = (E + a.split - 1) / a.split;
+        float *slots = smem + WK * 16 * BN;         // [split][per]
+        cluster_wait();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int m = e / BN, c = e - m * BN;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < WK; ++w) v += red[(w * 16 + m) * BN + c];
+            const int q = e / per;
+            st_cluster_f32(map_to_rank(smem_u32(slots + rank * per + (e - q * per)), q), v);
+        }
+        cluster_arrive();
+        cluster_wait();
+        const int e0 = rank * per, e1 = min(E, e0 + per);
+        for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+            float v = 0.f;
+            for (int q = 0; q < a.split; ++q) v += slots[q * per + (e - e0)];
+            const int m = e / BN, c = e - m * BN;
+            const int col = blockIdx.x * BN + c;
+            if (col < a.N)
+                o.out[(size_t)(m_base + m) * a.N + col] = to_out<BF>(v);
+        }
+        return;
+    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int m = e / BN, c = e - m * BN;
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < WK; ++w) v += red[(w * 16 + m) * BN + c];
-        if (a.split == 1) {
-            const int col = blockIdx.x * BN + c;
-            if (col < a.N)
-                o.out[(size_t)(m_base + m) * a.N + col] = to_out<BF>(v);
-        } else {
-            part[e] = v;
-        }
-    }
-    if (a.split == 1) return;
-
-    // ---- reduction 2: the CTAs of the cluster, through distributed shared
-    // memory, in rank order.  Rank r finalizes a contiguous slice of outputs.
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    const int rank = (int)cluster.block_rank();
-    const int per = (E + a.split - 1) / a.split;
-    const int e_end = min(E, (rank + 1) * per);
-    for (int e = rank * per + threadIdx.x; e < e_end; e += blockDim.x) {
-        float v = 0.f;
-        for (int q = 0; q < a.split; ++q) v += cluster.map_shared_rank(part, q)[e];
-        const int m = e / BN, c = e - m * BN;
         const int col = blockIdx.x * BN + c;
         if (col < a.N)
             o.out[(size_t)(m_base + m) * a.N + col] = to_out<BF>(v);
     }
-    cluster.sync();   // keep this CTA's shared memory alive until all peers have read it
 }
 
 // Grid: (ceil(N / (32*WN)), split, ceil(M / 16)); cluster (1, split, 1).
@@ -352,7 +361,7 @@ cudaError_t launch_one(const DecodeArgs &da, int strips, int mchunks, bool pdl,
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(strips, da.split, mchunks);
     lc.blockDim = dim3(32 * WN * WK, 1, 1);
-    lc.dynamicSmemBytes = (size_t)(WK + 1) * 16 * BN * sizeof(float);
+    lc.dynamicSmemBytes = ((size_t)(WK + 1) * 16 * BN + 8) * sizeof(float);
     lc.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -380,7 +389,7 @@ cudaError_t launch_grouped_one(const DecodeArgs &da, const ExpertTable &tab, int
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(strips, da.split, zdim);
     lc.blockDim = dim3(32 * WN * WK, 1, 1);
-    lc.dynamicSmemBytes = (size_t)(WK + 1) * 16 * BN * sizeof(float);
+    lc.dynamicSmemBytes = ((size_t)(WK + 1) * 16 * BN + 8) * sizeof(float);
     lc.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -450,7 +459,7 @@ int decode_ctas_per_sm(const w4a16_config &cfg, int M, int group) {
     else if (U == 2) fn = nt2 ? kernel_for<2, 2>(cfg.warps_n, cfg.warps_k) : kernel_for<1, 2>(cfg.warps_n, cfg.warps_k);
     else fn = nt2 ? kernel_for<2, 1>(cfg.warps_n, cfg.warps_k) : kernel_for<1, 1>(cfg.warps_n, cfg.warps_k);
     const int threads = 32 * cfg.warps_n * cfg.warps_k;
-    const size_t smem = (size_t)(cfg.warps_k + 1) * 16 * 32 * cfg.warps_n * sizeof(float);
+    const size_t smem = ((size_t)(cfg.warps_k + 1) * 16 * 32 * cfg.warps_n + 8) * sizeof(float);
     // occupancy is a property of the kernel, so the answer is cached per kernel
     static std::mutex mu;
     static std::map<const void *, int> cache;
