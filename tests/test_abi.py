@@ -213,3 +213,27 @@ def test_bf16_entries_validate_before_touching_the_gpu(lib):
     assert lib.w4a16_quantize_pack_bf16(16, 500, 256, 128, 16, 16, 16, None) == 1   # K % group
     assert lib.w4a16_dequantize_bf16(16, 16, 17, 16, 512, 256, 128, None) == 3     # misaligned
     assert lib.w4a16_quantize_pack_bf16(16, 512, 0, 128, 16, 16, 16, None) == 0    # N == 0
+
+
+def test_repacked_entries_validate_before_touching_the_gpu(lib):
+    """The repacked GEMM entries refuse bad shapes, variants, dtypes and
+    pointers on the host (no pointer below is ever dereferenced)."""
+    cfg = lambda **kw: ctypes.byref(native.Config.make(kw))
+    call = lambda M, K=1024, c=None, ptrs=(16, 32, 48): lib.w4a16_gemm_repacked(
+        *ptrs, M, 512, K, 128, c, None)
+    assert call(1, K=384) == 2                                  # K % 256 != 0
+    assert call(9, c=cfg(path="decode", variant="warp")) == 2   # warp kernel: M <= 8
+    assert b"M <= 8" in lib.w4a16_last_error()
+    assert call(1, c=cfg(path="decode", variant="registers")) == 2
+    assert call(1, c=cfg(dtype="bf16")) == 2 and b"fp16" in lib.w4a16_last_error()
+    assert call(1, ptrs=(None, None, None)) == 1 and b"null" in lib.w4a16_last_error()
+    assert call(1, ptrs=(16, 40, 48)) == 3                      # misaligned repacked
+    assert call(0) == 0                                         # nothing to do
+    P = ctypes.c_void_p
+    good = (P * 2)(16, 32)
+    gcall = lambda E, M, t=good, c=None: lib.w4a16_gemm_grouped_repacked(
+        E, t, t, t, M, 512, 1024, 128, c, None)
+    assert gcall(0, 1) == 1 and gcall(65, 1) == 1               # 1..64 experts
+    assert gcall(2, 17) == 2                                    # M <= 16
+    assert gcall(2, 1, t=(P * 2)(16, None)) == 1
+    assert gcall(2, 1, t=(P * 2)(16, 8)) == 3
